@@ -1,0 +1,21 @@
+"""FP8 weight-only (w8a16) decode GEMV for GB300 (sm_103a).
+
+y[m,n] = bf16(scale[n] * sum_k bf16(W[n,k]) * x[m,k]) with W an E4M3fn plane
+and one fp32 scale per row (ATOM PR #2980, "FP8 reads for mono decode",
+Summary and Changes); bf16 planes run through the same entry point.
+
+The compute path is the C-ABI library ``libw8.so`` (include/w8.h) built from
+``csrc/``; ``fp8_weight_only_w8a16_gb300.w8`` is its thin ctypes binding.
+Importing the package does not load the library; ``w8`` does, and raises if
+the library is missing or no CUDA device is present.
+"""
+
+__all__ = ["w8", "synth", "workloads"]
+
+
+def __getattr__(name):
+    if name == "w8":
+        from . import w8 as _w8
+
+        return _w8
+    raise AttributeError(name)

@@ -1,0 +1,98 @@
+"""Seeded synthetic inputs for the w8a16 GEMV: weight planes and activations.
+
+This module is the one piece both sides share: the tests feed the same bytes
+to the CPU oracle and to the CUDA path.  It holds none of the GEMV's
+arithmetic (no widening, no accumulation, no scaling of a reduced row, no
+output rounding).  Its only numeric steps are input preparation, done with
+library routines:
+
+* draws: numpy PCG64 (``default_rng(seed)``), standard normal in fp32; the
+  weights are N(0, 0.02) and the activations N(0, 1);
+* activations: fp32 -> bf16 through ``torch.Tensor.to(torch.bfloat16)``;
+* FP8 planes: the ptpc_fp8 weight format of ATOM PR #2980 (Summary: "E4M3 ...,
+  an fp32 scale per row"): scale[n] = amax_n / 448 in fp32 (an all-zero row
+  gets scale 1), codes = E4M3(W / scale) clamped to +-448 and rounded through
+  ``torch.float8_e4m3fn`` (round to nearest even);
+* bf16 planes: fp32 -> bf16 through torch.
+
+Draw order per workload: the weight plane first, then a [64, K] activation
+block whose first M rows are the M decode tokens, so every M of one workload
+sees the same prefix of tokens.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+E4M3_MAX = 448.0
+X_ROWS = 64  # largest decode-token count of the workloads
+
+
+@dataclass
+class Plane:
+    """A source weight plane as a checkpoint would hold it (row-major)."""
+
+    dtype: str            # "e4m3fn" or "bf16"
+    n: int
+    k: int                # logical columns
+    ldw: int              # row stride in elements (>= k); columns k..ldw-1 are zero
+    w: np.ndarray         # [n, ldw] uint8 codes or uint16 bf16 bits
+    scale: np.ndarray | None  # [n] fp32 row scales (FP8 only)
+
+
+def _normal(rng: np.random.Generator, shape, std: float) -> np.ndarray:
+    z = rng.standard_normal(shape, dtype=np.float32)
+    if std != 1.0:
+        z *= np.float32(std)
+    return z
+
+
+def to_bf16_bits(v: np.ndarray) -> np.ndarray:
+    """fp32 array -> bf16 bit patterns (uint16), via torch's conversion."""
+    t = torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def quantize_ptpc_fp8(w: np.ndarray):
+    """fp32 [n, k] -> (E4M3fn codes uint8 [n, k], fp32 row scales [n])."""
+    t = torch.from_numpy(np.ascontiguousarray(w, dtype=np.float32))
+    amax = t.abs().amax(dim=1) if t.shape[1] > 0 else torch.zeros(t.shape[0])
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    q = (t / scale[:, None]).clamp_(-E4M3_MAX, E4M3_MAX)
+    codes = q.to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes.numpy().copy(), scale.numpy().astype(np.float32)
+
+
+def weight_plane(rng: np.random.Generator, n: int, k: int, dtype: str = "e4m3fn",
+                 ldw: int | None = None, std: float = 0.02) -> Plane:
+    ldw = k if ldw is None else ldw
+    assert ldw >= k
+    w32 = _normal(rng, (n, k), std)
+    if dtype == "e4m3fn":
+        codes, scale = quantize_ptpc_fp8(w32)
+        w = np.zeros((n, ldw), dtype=np.uint8)
+        w[:, :k] = codes
+        return Plane("e4m3fn", n, k, ldw, w, scale)
+    if dtype == "bf16":
+        w = np.zeros((n, ldw), dtype=np.uint16)
+        w[:, :k] = to_bf16_bits(w32)
+        return Plane("bf16", n, k, ldw, w, None)
+    raise ValueError(dtype)
+
+
+def activations(rng: np.random.Generator, k: int, rows: int = X_ROWS,
+                ldx: int | None = None) -> np.ndarray:
+    """[rows, ldx] bf16 bits ~ N(0, 1); columns k..ldx-1 (if any) are drawn too."""
+    ldx = k if ldx is None else ldx
+    return to_bf16_bits(_normal(rng, (rows, ldx), 1.0))
+
+
+def workload(n: int, k: int, dtype: str = "e4m3fn", seed: int = 0, ldw: int | None = None,
+             x_rows: int = X_ROWS):
+    """(plane, x_all) for one workload: the plane is drawn before the tokens."""
+    rng = np.random.default_rng(seed)
+    plane = weight_plane(rng, n, k, dtype, ldw)
+    x = activations(rng, k, x_rows)
+    return plane, x

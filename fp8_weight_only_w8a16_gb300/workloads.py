@@ -1,0 +1,73 @@
+"""Decode projection shapes of the w8a16 GEMV workloads.
+
+Shapes are the GLM-5.2 checkpoint tensors read from the safetensors headers
+on the "GLM-5.2 anatomy" page (section "weights measured", tensor table):
+fused_qkv_a_proj is q_a_proj [2048, 6144] and kv_a_proj_with_mqa [576, 6144]
+merged into one [2624, 6144] plane (section "one merge at construction");
+o_proj [6144, 16384]; a shared expert is 6144 <-> 2048 (gate and up merged
+into [4096, 6144], down [6144, 2048]); q_b_proj [16384, 2048]; kv_b_proj
+[28672, 512]; the indexer's wq_b [4096, 2048], wk [128, 6144] and
+weights_proj [32, 6144]; lm_head [154880, 6144] in bf16.
+
+W is [N, K]: N output rows, K reduction columns, K contiguous in memory.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+
+@dataclass(frozen=True)
+class Projection:
+    name: str
+    n: int
+    k: int
+    dtype: str                  # "e4m3fn" or "bf16"
+    ms: tuple                   # decode-token counts exercised
+    ldw: int | None = None      # source row stride when the plane is padded
+
+    @property
+    def weight_bytes(self) -> int:
+        return self.n * self.k * (1 if self.dtype == "e4m3fn" else 2)
+
+    def algorithmic_bytes(self, m: int) -> int:
+        """W + fp32 scales (FP8) + x + y, with the logical K (pad excluded)."""
+        b = self.weight_bytes + 2 * m * self.k + 2 * m * self.n
+        if self.dtype == "e4m3fn":
+            b += 4 * self.n
+        return b
+
+    def flops(self, m: int) -> int:
+        return 2 * m * self.n * self.k + (m * self.n if self.dtype == "e4m3fn" else 0)
+
+
+SWEEP_M = (1, 2, 4, 8, 16, 32, 64)
+
+TINY = Projection("tiny", 256, 512, "e4m3fn", (1,))
+FUSED_QKV_A = Projection("fused_qkv_a_proj", 2624, 6144, "e4m3fn", (1, 4, 16))
+O_PROJ = Projection("o_proj", 6144, 16384, "e4m3fn", (1, 2, 8, 32))
+O_PROJ_BF16 = Projection("o_proj_bf16", 6144, 16384, "bf16", (1, 2, 8, 32))
+SHARED_GATE_UP = Projection("shared_expert_gate_up", 4096, 6144, "e4m3fn", (8,))
+SHARED_DOWN = Projection("shared_expert_down", 6144, 2048, "e4m3fn", (8,))
+SHARED_GATE_UP_KPAD = Projection("shared_expert_gate_up_kpad", 4096, 6144, "e4m3fn", (8,),
+                                 ldw=6144 + 128)
+Q_B = Projection("q_b_proj", 16384, 2048, "e4m3fn", SWEEP_M)
+KV_B = Projection("kv_b_proj", 28672, 512, "e4m3fn", SWEEP_M)
+WQ_B = Projection("indexer_wq_b", 4096, 2048, "e4m3fn", SWEEP_M)
+WK = Projection("indexer_wk", 128, 6144, "bf16", SWEEP_M)
+WEIGHTS_PROJ = Projection("indexer_weights_proj", 32, 6144, "bf16", SWEEP_M)
+LM_HEAD = Projection("lm_head", 154880, 6144, "bf16", (1,))
+
+ALL = (TINY, FUSED_QKV_A, O_PROJ, O_PROJ_BF16, SHARED_GATE_UP, SHARED_DOWN,
+       SHARED_GATE_UP_KPAD, Q_B, KV_B, WQ_B, WK, WEIGHTS_PROJ, LM_HEAD)
+BY_NAME = {p.name: p for p in ALL}
+
+# The five workload groups, in order: the tiny correctness case, the fused
+# qkv_a projection, o_proj (FP8 and bf16), the shared-expert pair with its
+# K-padded variant, and the full-layer sweep.
+GROUPS = {
+    "tiny": (TINY,),
+    "fused_qkv_a_proj": (FUSED_QKV_A,),
+    "o_proj": (O_PROJ, O_PROJ_BF16),
+    "shared_expert": (SHARED_GATE_UP, SHARED_DOWN, SHARED_GATE_UP_KPAD),
+    "layer_sweep": (Q_B, KV_B, WQ_B, WK, WEIGHTS_PROJ, LM_HEAD),
+}

@@ -1,0 +1,271 @@
+"""CPU oracle for the FP8 weight-only (w8a16) decode GEMV.
+
+TEST INFRASTRUCTURE ONLY: the product path (the C-ABI library and its Python
+binding) never imports this package.  Only ``tests/``,
+``__graft_entry__.smoke()`` and the ``cpu_baseline`` / ``--impl reference``
+legs of ``bench.py`` use it.
+
+The arithmetic lives in ``w8_oracle.c`` (plain C, fp32 ascending-k
+accumulation, one fp32 scale multiply, one bf16 round to nearest even), which
+follows ATOM PR #2980 ("FP8 reads for mono decode"), sections Summary and
+Changes: the E4M3 plane widens exactly to bf16 and the fp32 row scale
+multiplies each reduced row before the bf16 rounding.  ``brute.py`` is an
+independent numpy fp64 recompute used to pin it.
+
+Every function here is pinned by a ``-m "not gpu"`` test
+(tests/test_oracle_codecs.py, tests/test_oracle_gemv.py).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+from .build import build_oracle, ORACLE_SO
+
+DT_E4M3FN = 1
+DT_BF16 = 2
+
+_default = None
+_lock = threading.Lock()
+
+
+def _ptr(a: np.ndarray | None):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _declare(lib):
+    c_i64 = ctypes.c_int64
+    vp = ctypes.c_void_p
+    lib.orc_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+    lib.orc_e4m3_to_f32.restype = ctypes.c_float
+    lib.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    lib.orc_bf16_to_f32.restype = ctypes.c_float
+    lib.orc_f32_to_bf16_rne.argtypes = [ctypes.c_float]
+    lib.orc_f32_to_bf16_rne.restype = ctypes.c_uint16
+    lib.orc_f32_to_e4m3_sat.argtypes = [ctypes.c_float]
+    lib.orc_f32_to_e4m3_sat.restype = ctypes.c_uint8
+    lib.orc_quantize_rows.argtypes = [vp, c_i64, c_i64, c_i64, vp, c_i64, vp]
+    lib.orc_quantize_rows.restype = None
+    lib.orc_gemv.argtypes = [vp, ctypes.c_int, c_i64, c_i64, c_i64, vp, vp, c_i64, c_i64,
+                             vp, c_i64, ctypes.c_int]
+    lib.orc_gemv.restype = ctypes.c_int
+    lib.orc_gemv_f64.argtypes = [vp, ctypes.c_int, c_i64, c_i64, c_i64, vp, vp, c_i64,
+                                 c_i64, vp, vp, ctypes.c_int]
+    lib.orc_gemv_f64.restype = ctypes.c_int
+    lib.orc_max_threads.argtypes = []
+    lib.orc_max_threads.restype = ctypes.c_int
+    return lib
+
+
+def _check_plane(w: np.ndarray, dtype: int, k: int | None):
+    if dtype == DT_E4M3FN:
+        assert w.dtype == np.uint8, "E4M3 planes are uint8 codes"
+    elif dtype == DT_BF16:
+        assert w.dtype == np.uint16, "bf16 planes are uint16 bit patterns"
+    else:
+        raise ValueError(f"unknown dtype {dtype}")
+    assert w.ndim == 2 and w.strides[1] == w.itemsize
+    n, ldw = w.shape[0], w.strides[0] // w.itemsize
+    kk = w.shape[1] if k is None else k
+    return n, kk, ldw
+
+
+class Oracle:
+    """The oracle's functions bound to one compiled copy of w8_oracle.c."""
+
+    DT_E4M3FN = DT_E4M3FN
+    DT_BF16 = DT_BF16
+
+    def __init__(self, lib):
+        self.lib = _declare(lib)
+
+    # ---- codecs -------------------------------------------------------
+    def e4m3_to_f32(self, code: int) -> float:
+        return float(self.lib.orc_e4m3_to_f32(int(code) & 0xFF))
+
+    def bf16_to_f32(self, bits: int) -> float:
+        return float(self.lib.orc_bf16_to_f32(int(bits) & 0xFFFF))
+
+    def f32_to_bf16_rne(self, values) -> np.ndarray:
+        """fp32 values -> bf16 bit patterns (uint16), round to nearest even."""
+        v = np.ascontiguousarray(values, dtype=np.float32).ravel()
+        out = np.empty(v.shape, dtype=np.uint16)
+        f = self.lib.orc_f32_to_bf16_rne
+        for i, x in enumerate(v):
+            out[i] = f(ctypes.c_float(x))
+        return out.reshape(np.shape(values))
+
+    def f32_to_e4m3_sat(self, values) -> np.ndarray:
+        """fp32 values -> E4M3fn codes (uint8), RNE, saturating at +-448."""
+        v = np.ascontiguousarray(values, dtype=np.float32).ravel()
+        out = np.empty(v.shape, dtype=np.uint8)
+        f = self.lib.orc_f32_to_e4m3_sat
+        for i, x in enumerate(v):
+            out[i] = f(ctypes.c_float(x))
+        return out.reshape(np.shape(values))
+
+    def quantize_rows(self, w: np.ndarray):
+        """ptpc_fp8 row quantizer: returns (codes uint8 [n,k], scale fp32 [n])."""
+        w = np.ascontiguousarray(w, dtype=np.float32)
+        n, k = w.shape
+        q = np.empty((n, k), dtype=np.uint8)
+        s = np.empty((n,), dtype=np.float32)
+        self.lib.orc_quantize_rows(_ptr(w), n, k, k, _ptr(q), k, _ptr(s))
+        return q, s
+
+    # ---- the GEMV -----------------------------------------------------
+    def gemv(self, w: np.ndarray, dtype: int, scale: np.ndarray | None, x: np.ndarray,
+             k: int | None = None, threads: int = 1) -> np.ndarray:
+        """y = bf16(scale * sum_k W x) in fp32, ascending k.  Returns uint16 [m, n].
+
+        ``w``: [n, >=k] codes (uint8) or bf16 bits (uint16); its row stride is
+        taken from the array.  ``x``: [m, >=k] bf16 bits (uint16).
+        """
+        n, k, ldw = _check_plane(w, dtype, k)
+        assert x.dtype == np.uint16 and x.ndim == 2 and x.strides[1] == 2
+        m, ldx = x.shape[0], x.strides[0] // 2
+        sc = None
+        if dtype == DT_E4M3FN:
+            sc = np.ascontiguousarray(scale, dtype=np.float32)
+            assert sc.shape == (n,)
+        y = np.zeros((m, n), dtype=np.uint16)
+        rc = self.lib.orc_gemv(_ptr(w), dtype, n, k, ldw, _ptr(sc), _ptr(x), ldx, m, _ptr(y),
+                               n, int(threads))
+        if rc != 0:
+            raise ValueError("orc_gemv rejected its arguments")
+        return y
+
+    def gemv_f64(self, w: np.ndarray, dtype: int, scale: np.ndarray | None, x: np.ndarray,
+                 k: int | None = None, threads: int = 1):
+        """fp64 recompute: (y64 [m,n] float64, mag64 [m,n] = sum|scale*W*x|)."""
+        n, k, ldw = _check_plane(w, dtype, k)
+        assert x.dtype == np.uint16 and x.ndim == 2 and x.strides[1] == 2
+        m, ldx = x.shape[0], x.strides[0] // 2
+        sc = None
+        if dtype == DT_E4M3FN:
+            sc = np.ascontiguousarray(scale, dtype=np.float32)
+        y64 = np.zeros((m, n), dtype=np.float64)
+        mag = np.zeros((m, n), dtype=np.float64)
+        rc = self.lib.orc_gemv_f64(_ptr(w), dtype, n, k, ldw, _ptr(sc), _ptr(x), ldx, m,
+                                   _ptr(y64), _ptr(mag), int(threads))
+        if rc != 0:
+            raise ValueError("orc_gemv_f64 rejected its arguments")
+        return y64, mag
+
+    def max_threads(self) -> int:
+        return int(self.lib.orc_max_threads())
+
+    # ---- helpers that hold no method arithmetic ------------------------
+    bf16_bits_to_f64 = staticmethod(lambda bits: bf16_bits_to_f64(bits))
+    within_tolerance = staticmethod(lambda y, y64, mag: within_tolerance(y, y64, mag))
+
+
+def _load() -> Oracle:
+    global _default
+    with _lock:
+        if _default is not None:
+            return _default
+        src = os.path.join(os.path.dirname(__file__), "w8_oracle.c")
+        if not os.path.exists(ORACLE_SO) or os.path.getmtime(ORACLE_SO) < os.path.getmtime(src):
+            build_oracle()
+        _default = Oracle(ctypes.CDLL(ORACLE_SO))
+        return _default
+
+
+def load_variant(so_path: str) -> Oracle:
+    """Bind the API to another compiled copy (the mutation tests use this)."""
+    return Oracle(ctypes.CDLL(so_path))
+
+
+def e4m3_to_f32(code):
+    return _load().e4m3_to_f32(code)
+
+
+def bf16_to_f32(bits):
+    return _load().bf16_to_f32(bits)
+
+
+def f32_to_bf16_rne(values):
+    return _load().f32_to_bf16_rne(values)
+
+
+def f32_to_e4m3_sat(values):
+    return _load().f32_to_e4m3_sat(values)
+
+
+def quantize_rows(w):
+    return _load().quantize_rows(w)
+
+
+def gemv(w, dtype, scale, x, k=None, threads=1):
+    return _load().gemv(w, dtype, scale, x, k, threads)
+
+
+def gemv_f64(w, dtype, scale, x, k=None, threads=1):
+    return _load().gemv_f64(w, dtype, scale, x, k, threads)
+
+
+def max_threads():
+    return _load().max_threads()
+
+
+# --------------------------------------------------------------------------
+# the tolerance of the parity tests
+# --------------------------------------------------------------------------
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    b = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def within_tolerance(y_bits: np.ndarray, y64: np.ndarray, mag64: np.ndarray):
+    """|y - y64| <= 2^-7 |y64| + 2^-12 sum|scale W x|, NaN matching NaN.
+
+    This is the stated parity tolerance for the w8a16 GEMV: twice the bf16
+    half-ulp for the final rounding plus 2^-12 of the absolute sum for the
+    fp32 accumulation.  Returns (ok: bool, worst ratio |err|/bound).
+    """
+    y = bf16_bits_to_f64(y_bits)
+    nan_ref = np.isnan(y64)
+    nan_y = np.isnan(y)
+    if not np.array_equal(nan_ref, nan_y):
+        return False, float("inf")
+    fin = ~nan_ref
+    err = np.abs(y[fin] - y64[fin])
+    bound = 2.0 ** -7 * np.abs(y64[fin]) + 2.0 ** -12 * mag64[fin]
+    ratio = np.where(bound > 0, err / np.where(bound > 0, bound, 1.0),
+                     np.where(err > 0, np.inf, 0.0))
+    worst = float(ratio.max()) if ratio.size else 0.0
+    return bool(worst <= 1.0), worst
+
+
+def same_values(a_bits: np.ndarray, b_bits: np.ndarray) -> bool:
+    """Bit-for-bit equality of bf16 results, with +0 == -0 and NaN == NaN.
+
+    The sign of an exact zero depends on where a sum starts, and a NaN's
+    payload is not part of the method; every other pattern must match.
+    """
+    a = np.ascontiguousarray(a_bits, dtype=np.uint16)
+    b = np.ascontiguousarray(b_bits, dtype=np.uint16)
+    if a.shape != b.shape:
+        return False
+    za = (a & 0x7FFF) == 0
+    zb = (b & 0x7FFF) == 0
+    na = ((a & 0x7F80) == 0x7F80) & ((a & 0x7F) != 0)
+    nb = ((b & 0x7F80) == 0x7F80) & ((b & 0x7F) != 0)
+    if not np.array_equal(za, zb) or not np.array_equal(na, nb):
+        return False
+    rest = ~(za | na)
+    return bool(np.array_equal(a[rest], b[rest]))
+
+
+__all__ = [
+    "DT_E4M3FN", "DT_BF16", "Oracle", "load_variant", "e4m3_to_f32", "bf16_to_f32",
+    "f32_to_bf16_rne", "f32_to_e4m3_sat", "quantize_rows", "gemv", "gemv_f64",
+    "max_threads", "bf16_bits_to_f64", "within_tolerance", "same_values", "build_oracle",
+]

@@ -1,0 +1,244 @@
+/*
+ * w8_oracle.c -- CPU oracle for the FP8 weight-only (w8a16) decode GEMV.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file: only tests/, __graft_entry__.smoke() and the cpu_baseline
+ * leg of bench.py use it.  It shares no code, header, table or constant with
+ * the CUDA path under fp8_weight_only_w8a16_gb300/csrc.
+ *
+ * What it computes (ATOM PR #2980 "FP8 reads for mono decode", sections
+ * Summary and Changes): for every output row n and decode token m
+ *
+ *     y[m,n] = bf16_rne( scale[n] * sum_k widen(W[n,k]) * x[m,k] )
+ *
+ * with W an E4M3fn plane (one fp32 scale per row; the scale multiplies the
+ * fully reduced row, before the single bf16 rounding), x bf16 activations and
+ * fp32 accumulation.  A bf16 plane runs through the same computation with no
+ * scale ("bf16 planes run as before").  The FP8 codes widen exactly to bf16
+ * ("FP8 widens exactly to bf16"), so the widening is the exact value of the
+ * code.
+ *
+ * Everything here is the plain definition: scalar loops, ascending k, fp32
+ * accumulation, one fp32 multiply by the scale, one round-to-nearest-even to
+ * bf16.  Build with -ffp-contract=off and without -ffast-math.  An fp64
+ * recompute and a brute-force E4M3 encoder (the ptpc_fp8 quantizer's rounding)
+ * are included for the tolerance checks and pins.
+ *
+ * Pins (tests/test_oracle_*.py) hold each function to something other than
+ * itself: the 256 codes against their closed-form values and against
+ * torch.float8_e4m3fn, bf16 rounding against torch.bfloat16, the GEMV against
+ * a numpy fp64 matmul on tiny inputs, one-hot and exact-sum inputs against
+ * exact rational results, and power-of-two scale invariance.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_DT_E4M3FN 1
+#define ORC_DT_BF16 2
+
+/* ------------------------------------------------------------------ */
+/* Codecs                                                              */
+/* ------------------------------------------------------------------ */
+
+/* E4M3fn code -> value, bit by bit from the OCP 8-bit floating point format
+ * (E4M3: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits; no
+ * infinities; S.1111.111 is NaN; exponent field 0 is subnormal).  The PR page
+ * (Summary) relies on every such value widening exactly to bf16. */
+float orc_e4m3_to_f32(uint8_t c)
+{
+    int s = (c >> 7) & 1;
+    int e = (c >> 3) & 15;
+    int m = c & 7;
+    float v;
+    if (e == 15 && m == 7) {
+        v = NAN;
+        return s ? -v : v;
+    }
+    if (e == 0)
+        v = ldexpf((float)m, -9);                 /* m/8 * 2^(1-7)  */
+    else
+        v = ldexpf(1.0f + (float)m / 8.0f, e - 7); /* 1.m * 2^(e-7) */
+    return s ? -v : v;
+}
+
+/* bf16 bits -> fp32: a bf16 is the upper half of an fp32. */
+float orc_bf16_to_f32(uint16_t u)
+{
+    uint32_t b = (uint32_t)u << 16;
+    float f;
+    memcpy(&f, &b, sizeof f);
+    return f;
+}
+
+/* fp32 -> bf16, round to nearest, ties to even.  NaN stays NaN (quieted,
+ * sign kept); values past the largest bf16 round to infinity. */
+uint16_t orc_f32_to_bf16_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t kept = u >> 16;          /* truncation toward zero      */
+    uint32_t dropped = u & 0xFFFFu;   /* the 16 bits that are cut    */
+    int up;
+    if (dropped > 0x8000u)
+        up = 1;                       /* more than half an ulp       */
+    else if (dropped < 0x8000u)
+        up = 0;                       /* less than half an ulp       */
+    else
+        up = (int)(kept & 1u);        /* exactly half: go to even    */
+    /* bf16 patterns of one sign are ordered by magnitude, so adding one to
+     * the kept pattern steps to the next larger magnitude (or to inf). */
+    return (uint16_t)(kept + (uint32_t)up);
+}
+
+/* fp32 -> E4M3fn code, round to nearest with ties to even mantissa,
+ * saturating at +-448.  A brute-force nearest search over the 127
+ * non-negative finite codes; used by the ptpc_fp8 quantizer below. */
+uint8_t orc_f32_to_e4m3_sat(float v)
+{
+    if (isnan(v))
+        return 0x7F;
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs((double)v);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7E);
+    int best = 0;
+    double best_d = a; /* distance to code 0 */
+    for (int c = 1; c <= 0x7E; ++c) {
+        double d = fabs((double)orc_e4m3_to_f32((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+/* ptpc_fp8 row quantizer (weight side of "per-token per-channel"): one fp32
+ * scale per output row, scale = amax_row / 448, codes = E4M3(W / scale)
+ * clamped to +-448.  An all-zero row gets scale 1 and zero codes.  This is
+ * input preparation for the tests, not part of the GEMV. */
+void orc_quantize_rows(const float *w, int64_t n, int64_t k, int64_t ldw,
+                       uint8_t *q, int64_t ldq, float *scale)
+{
+    for (int64_t r = 0; r < n; ++r) {
+        float amax = 0.0f;
+        for (int64_t j = 0; j < k; ++j) {
+            float a = fabsf(w[r * ldw + j]);
+            if (a > amax)
+                amax = a;
+        }
+        float s = (amax > 0.0f) ? amax / 448.0f : 1.0f;
+        scale[r] = s;
+        for (int64_t j = 0; j < k; ++j) {
+            float t = w[r * ldw + j] / s;
+            if (t > 448.0f)
+                t = 448.0f;
+            if (t < -448.0f)
+                t = -448.0f;
+            q[r * ldq + j] = orc_f32_to_e4m3_sat(t);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* GEMV                                                                */
+/* ------------------------------------------------------------------ */
+
+static float weight_value(const void *w, int dtype, int64_t idx)
+{
+    if (dtype == ORC_DT_E4M3FN)
+        return orc_e4m3_to_f32(((const uint8_t *)w)[idx]);
+    return orc_bf16_to_f32(((const uint16_t *)w)[idx]);
+}
+
+/* The method, as the plain definition.  W is [n][ldw] (logical k columns),
+ * x is [m][ldx] bf16, y is [m][ldy] bf16.  For dtype E4M3FN, scale[n] is the
+ * fp32 row scale; for BF16 it is ignored (may be NULL).  `threads` > 1
+ * splits the output rows over OpenMP threads; every row is still summed in
+ * ascending k by one thread, so the result does not depend on it.
+ * Returns 0, or -1 on a bad argument. */
+int orc_gemv(const void *w, int dtype, int64_t n, int64_t k, int64_t ldw,
+             const float *scale, const uint16_t *x, int64_t ldx, int64_t m,
+             uint16_t *y, int64_t ldy, int threads)
+{
+    if (!w || !x || !y || n < 0 || k < 0 || m < 0 || ldw < k || ldx < k || ldy < n)
+        return -1;
+    if (dtype != ORC_DT_E4M3FN && dtype != ORC_DT_BF16)
+        return -1;
+    if (dtype == ORC_DT_E4M3FN && !scale)
+        return -1;
+#ifdef _OPENMP
+    if (threads < 1)
+        threads = 1;
+#pragma omp parallel for schedule(dynamic, 16) num_threads(threads)
+#endif
+    for (int64_t r = 0; r < n; ++r) {
+        for (int64_t i = 0; i < m; ++i) {
+            float acc = 0.0f;
+            for (int64_t j = 0; j < k; ++j) {
+                float wv = weight_value(w, dtype, r * ldw + j);
+                float xv = orc_bf16_to_f32(x[i * ldx + j]);
+                float p = wv * xv; /* exact: 4 x 8 significant bits */
+                acc = acc + p;
+            }
+            float t = (dtype == ORC_DT_E4M3FN) ? scale[r] * acc : acc;
+            y[i * ldy + r] = orc_f32_to_bf16_rne(t);
+        }
+    }
+    (void)threads;
+    return 0;
+}
+
+/* fp64 recompute of the same widened inputs, for the tolerance checks:
+ *   y64[i][r]   = scale[r] * sum_k W[r,k] * x[i,k]      (in double)
+ *   mag64[i][r] = sum_k |scale[r] * W[r,k] * x[i,k]|    (in double)
+ * Both arrays are [m][n]. */
+int orc_gemv_f64(const void *w, int dtype, int64_t n, int64_t k, int64_t ldw,
+                 const float *scale, const uint16_t *x, int64_t ldx, int64_t m,
+                 double *y64, double *mag64, int threads)
+{
+    if (!w || !x || !y64 || !mag64 || n < 0 || k < 0 || m < 0 || ldw < k || ldx < k)
+        return -1;
+    if (dtype != ORC_DT_E4M3FN && dtype != ORC_DT_BF16)
+        return -1;
+    if (dtype == ORC_DT_E4M3FN && !scale)
+        return -1;
+#ifdef _OPENMP
+    if (threads < 1)
+        threads = 1;
+#pragma omp parallel for schedule(dynamic, 16) num_threads(threads)
+#endif
+    for (int64_t r = 0; r < n; ++r) {
+        double s = (dtype == ORC_DT_E4M3FN) ? (double)scale[r] : 1.0;
+        for (int64_t i = 0; i < m; ++i) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t j = 0; j < k; ++j) {
+                double p = (double)weight_value(w, dtype, r * ldw + j) *
+                           (double)orc_bf16_to_f32(x[i * ldx + j]);
+                acc += p;
+                mag += fabs(s * p);
+            }
+            y64[i * n + r] = s * acc;
+            mag64[i * n + r] = mag;
+        }
+    }
+    (void)threads;
+    return 0;
+}
+
+/* Number of threads OpenMP would use (1 without OpenMP). */
+int orc_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

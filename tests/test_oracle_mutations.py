@@ -1,0 +1,94 @@
+"""Negative controls for the oracle's pins (CPU only).
+
+Each case plants one plausible mistake in a copy of oracle/w8_oracle.c,
+compiles the copy to a temporary library and reruns the pins against it: at
+least one pin must fail.  This is how the pins show they would catch a
+dropped term, a wrong sign, index or exponent, a misplaced scale or a wrong
+rounding in the oracle (the PR page, Testing, asks the same of its kernel
+tests: "breaking the row scale or the dword order fails them").  The
+committed oracle is never modified; mistakes are planted only on the CPU.
+"""
+from __future__ import annotations
+
+import os
+
+import pytest
+
+import oracle
+from oracle.build import ORACLE_SRC, build_oracle
+
+from . import test_oracle_codecs as codecs
+from . import test_oracle_gemv as gemv_pins
+
+MUTATIONS = {
+    "scale_dropped": ("float t = (dtype == ORC_DT_E4M3FN) ? scale[r] * acc : acc;",
+                      "float t = acc;"),
+    "scale_of_wrong_row": ("? scale[r] * acc : acc;", "? scale[(r + 1) % n] * acc : acc;"),
+    "scale_after_bf16_rounding": (
+        "float t = (dtype == ORC_DT_E4M3FN) ? scale[r] * acc : acc;",
+        "float t = (dtype == ORC_DT_E4M3FN) ? scale[r] * orc_bf16_to_f32("
+        "orc_f32_to_bf16_rne(acc)) : acc;"),
+    "first_term_dropped": ("for (int64_t j = 0; j < k; ++j) {\n                float wv",
+                           "for (int64_t j = 1; j < k; ++j) {\n                float wv"),
+    "x_index_reversed": ("float xv = orc_bf16_to_f32(x[i * ldx + j]);",
+                         "float xv = orc_bf16_to_f32(x[i * ldx + (k - 1 - j)]);"),
+    "sign_ignored": ("        v = ldexpf(1.0f + (float)m / 8.0f, e - 7); /* 1.m * 2^(e-7) */\n"
+                     "    return s ? -v : v;",
+                     "        v = ldexpf(1.0f + (float)m / 8.0f, e - 7); /* 1.m * 2^(e-7) */\n"
+                     "    return v;"),
+    "exponent_bias_off_by_one": ("e - 7); /* 1.m", "e - 8); /* 1.m"),
+    "subnormal_scale_wrong": ("ldexpf((float)m, -9)", "ldexpf((float)m, -10)"),
+    "mantissa_over_4": ("1.0f + (float)m / 8.0f", "1.0f + (float)m / 4.0f"),
+    "rounding_ties_away": ("up = (int)(kept & 1u);", "up = 1;"),
+    "rounding_truncates": ("if (dropped > 0x8000u)\n        up = 1;",
+                           "if (dropped > 0x8000u)\n        up = 0;"),
+    "bf16_widening_shift_wrong": ("(uint32_t)u << 16;", "(uint32_t)u << 15;"),
+    "accumulate_in_bf16": ("acc = acc + p;",
+                           "acc = orc_bf16_to_f32(orc_f32_to_bf16_rne(acc + p));"),
+}
+
+# pins rerun against each mutated copy (test functions that take the oracle)
+PINS = [
+    lambda o: codecs.test_golden_special_codes(o),
+    lambda o: codecs.test_all_256_codes_match_torch_float8(o),
+    lambda o: codecs.test_bf16_rne_matches_torch(o),
+    lambda o: codecs.test_finite_codes_widen_exactly_to_bf16(o),
+    lambda o: gemv_pins.test_one_hot_returns_scaled_code(o, "random"),
+    lambda o: gemv_pins.test_one_hot_bf16_plane_returns_weight(o),
+    lambda o: gemv_pins.test_exact_sum_inputs_match_rational_result(o),
+    lambda o: gemv_pins.test_scale_multiplies_the_reduced_row_once(o),
+    lambda o: gemv_pins.test_gemv_against_fp64_brute_force(o, True, 2, 33, 64, 16),
+    lambda o: gemv_pins.test_gemv_against_fp64_brute_force(o, False, 5, 40, 63, 9),
+]
+
+
+def _mutant(tmp_path, name):
+    find, repl = MUTATIONS[name]
+    src = open(ORACLE_SRC).read()
+    assert src.count(find) == 1, f"mutation {name} no longer applies"
+    path = os.path.join(tmp_path, f"mut_{name}.c")
+    with open(path, "w") as f:
+        f.write(src.replace(find, repl))
+    so = build_oracle(src=path, out=os.path.join(tmp_path, f"libmut_{name}.so"))
+    return oracle.load_variant(so)
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(tmp_path, name):
+    mut = _mutant(str(tmp_path), name)
+    caught = []
+    for i, pin in enumerate(PINS):
+        try:
+            pin(mut)
+        except AssertionError:
+            caught.append(i)
+    assert caught, f"no pin caught the mutation {name}"
+
+
+def test_unmutated_copy_passes_every_pin(tmp_path):
+    path = os.path.join(str(tmp_path), "copy.c")
+    with open(path, "w") as f:
+        f.write(open(ORACLE_SRC).read())
+    same = oracle.load_variant(build_oracle(src=path, out=os.path.join(str(tmp_path), "c.so")))
+    for pin in PINS:
+        pin(same)
