@@ -6,16 +6,6 @@ Summary and Changes); bf16 planes run through the same entry point.
 
 The compute path is the C-ABI library ``libw8.so`` (include/w8.h) built from
 ``csrc/``; ``fp8_weight_only_w8a16_gb300.w8`` is its thin ctypes binding.
-Importing the package does not load the library; ``w8`` does, and raises if
-the library is missing or no CUDA device is present.
+Importing the package does not load the library; importing ``.w8`` does, and
+raises if the library is missing.
 """
-
-__all__ = ["w8", "synth", "workloads"]
-
-
-def __getattr__(name):
-    if name == "w8":
-        from . import w8 as _w8
-
-        return _w8
-    raise AttributeError(name)

@@ -1,0 +1,352 @@
+// w8_api.cu -- the C ABI of libw8 (declared and documented in include/w8.h).
+//
+// Host-side validation and binding follow the bind/refuse rules of ATOM PR
+// #2980 (Changes: "binds FP8 planes in place and refuses what the kernels
+// can't read, such as a non-E4M3fn or unpadded plane, a bias, or bf16 and
+// FP8 mixed in one build"; Limitations: e4m3fnuz and every other format are
+// refused at bind).  The gemv entry points take the same arguments for both
+// weight dtypes; the FP8 row scales travel with the build and reach the
+// kernel as its trailing data (Changes: "passes the row scales as the last
+// kernel arguments, so bf16 builds keep their argument layout").
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+#include <vector>
+
+#include "w8.h"
+#include "w8_internal.h"
+
+struct w8_build {
+    int device;
+    int sm_count;
+    int32_t dtype;
+    std::vector<w8_plane_info> planes;
+};
+
+namespace {
+
+constexpr int64_t kMaxDim = int64_t(1) << 30;
+
+int elem_bytes(int32_t dtype) { return dtype == W8_DT_BF16 ? 2 : 1; }
+
+w8_status check_plane(const w8_plane_desc &d)
+{
+    if (!d.w)
+        return W8_ERR_NULL;
+    if (d.dtype != W8_DT_E4M3FN && d.dtype != W8_DT_BF16)
+        return W8_ERR_DTYPE;
+    if (d.layout != W8_SRC_ROW_MAJOR)
+        return W8_ERR_LAYOUT;
+    if (d.bias)
+        return W8_ERR_BIAS;
+    if (d.n < 1 || d.k < 1 || d.n > kMaxDim || d.k > kMaxDim || d.ldw < d.k ||
+        d.ldw > 4 * kMaxDim)
+        return W8_ERR_SHAPE;
+    if (d.dtype == W8_DT_E4M3FN && !d.scale)
+        return W8_ERR_SCALE;
+    if (d.dtype == W8_DT_BF16 && d.scale)
+        return W8_ERR_SCALE;
+    if ((reinterpret_cast<uintptr_t>(d.w) & 15u) != 0 || ((d.ldw * elem_bytes(d.dtype)) & 15) != 0)
+        return W8_ERR_UNPADDED;
+    return W8_OK;
+}
+
+size_t plane_packed_bytes(int32_t dtype, int64_t n, int64_t k)
+{
+    const int64_t rt = w8::ceil_div(n, w8::kTileN), kb = w8::ceil_div(k, w8::kTileK);
+    return size_t(rt) * size_t(kb) * size_t(dtype == W8_DT_BF16 ? w8::kRunBf16 : w8::kRunFp8);
+}
+
+size_t plane_scale_bytes(int32_t dtype, int64_t n)
+{
+    if (dtype != W8_DT_E4M3FN)
+        return 0;
+    return size_t(w8::ceil_div(n, w8::kTileN)) * w8::kTileN * sizeof(float);
+}
+
+w8_status gemv_common(const w8_build *b, int plane, int32_t want_dtype, const uint16_t *x,
+                      int64_t ldx, int m, uint16_t *y, int64_t ldy, void *ws, size_t ws_bytes,
+                      w8_stream s)
+{
+    if (!b)
+        return W8_ERR_NULL;
+    if (plane < 0 || plane >= int(b->planes.size()))
+        return W8_ERR_PLANE;
+    const w8_plane_info &p = b->planes[size_t(plane)];
+    if (p.dtype != want_dtype)
+        return W8_ERR_DTYPE;
+    if (m < 0 || m > w8::kMaxM)
+        return W8_ERR_SHAPE;
+    if (m == 0)
+        return W8_OK;
+    if (!x || !y)
+        return W8_ERR_NULL;
+    if (ldx < p.k || ldy < p.n)
+        return W8_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(x) & 1u) || (reinterpret_cast<uintptr_t>(y) & 1u))
+        return W8_ERR_ALIGN;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return W8_ERR_CUDA;
+    if (dev != b->device)
+        return W8_ERR_DEVICE;
+
+    const w8::Plan plan = w8::make_plan(p.n, p.k, m, b->sm_count);
+    w8::GemvArgs a{};
+    a.wp = static_cast<const uint8_t *>(p.packed);
+    a.scale = p.scale;
+    a.x = x;
+    a.ldx = ldx;
+    a.y = y;
+    a.ldy = ldy;
+    a.n = int(p.n);
+    a.k = int(p.k);
+    a.m = m;
+    a.kb = int(plan.kb);
+    a.rt = int(plan.rt);
+    a.splits = plan.splits;
+    a.x_stride = plan.x_stride;
+    a.x_vec = ((reinterpret_cast<uintptr_t>(x) & 15u) == 0 && (ldx & 7) == 0) ? 1 : 0;
+    if (plan.splits > 1) {
+        if (!ws)
+            return W8_ERR_NULL;
+        if (reinterpret_cast<uintptr_t>(ws) & 255u)
+            return W8_ERR_ALIGN;
+        if (ws_bytes < plan.ws_bytes)
+            return W8_ERR_CAPACITY;
+        a.counters = static_cast<int *>(ws);
+        a.partial = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + plan.ws_counters);
+    }
+    if (w8::launch_gemv(want_dtype == W8_DT_E4M3FN, plan, a, reinterpret_cast<cudaStream_t>(s)) !=
+        cudaSuccess)
+        return W8_ERR_CUDA;
+    return W8_OK;
+}
+
+} // namespace
+
+extern "C" {
+
+const char *w8_status_str(w8_status s)
+{
+    switch (s) {
+    case W8_OK: return "ok";
+    case W8_ERR_NULL: return "a required pointer is NULL";
+    case W8_ERR_DTYPE: return "weight dtype the kernels cannot read (only E4M3FN and BF16), "
+                              "or a gemv call of the other dtype";
+    case W8_ERR_UNPADDED: return "unpadded plane: base not 16-byte aligned or row stride not a "
+                                 "multiple of 16 bytes";
+    case W8_ERR_BIAS: return "a bias was given; the GEMV has none";
+    case W8_ERR_MIXED: return "bf16 and FP8 planes mixed in one build";
+    case W8_ERR_SHAPE: return "bad shape: N, K >= 1, ldw >= K, 0 <= m <= 64, ldx >= K, ldy >= N";
+    case W8_ERR_SCALE: return "FP8 planes need fp32 row scales; bf16 planes take none";
+    case W8_ERR_LAYOUT: return "unknown source layout (only row-major)";
+    case W8_ERR_CAPACITY: return "packed buffer or workspace too small";
+    case W8_ERR_ALIGN: return "misaligned buffer (packed/workspace: 256 B; x, y: 2 B)";
+    case W8_ERR_PLANE: return "plane index outside the build";
+    case W8_ERR_DEVICE: return "current device is not the device the build was bound on";
+    case W8_ERR_CUDA: return "CUDA runtime error";
+    }
+    return "unknown status";
+}
+
+int w8_abi_version(void) { return W8_ABI_VERSION; }
+
+w8_status w8_validate(const w8_plane_desc *d, int n_planes)
+{
+    if (!d || n_planes < 1)
+        return W8_ERR_NULL;
+    for (int i = 0; i < n_planes; ++i) {
+        const w8_status st = check_plane(d[i]);
+        if (st != W8_OK)
+            return st;
+    }
+    for (int i = 1; i < n_planes; ++i)
+        if (d[i].dtype != d[0].dtype)
+            return W8_ERR_MIXED;
+    return W8_OK;
+}
+
+w8_status w8_packed_bytes(const w8_plane_desc *d, int n_planes, size_t *bytes)
+{
+    const w8_status st = w8_validate(d, n_planes);
+    if (st != W8_OK)
+        return st;
+    if (!bytes)
+        return W8_ERR_NULL;
+    size_t total = 0;
+    for (int i = 0; i < n_planes; ++i) {
+        total += w8::align256(plane_scale_bytes(d[i].dtype, d[i].n));
+        total += w8::align256(plane_packed_bytes(d[i].dtype, d[i].n, d[i].k));
+    }
+    *bytes = total;
+    return W8_OK;
+}
+
+w8_status w8_bind(const w8_plane_desc *d, int n_planes, void *dst, size_t dst_bytes,
+                  w8_stream s, w8_build **out)
+{
+    if (!out)
+        return W8_ERR_NULL;
+    *out = nullptr;
+    size_t need = 0;
+    w8_status st = w8_packed_bytes(d, n_planes, &need);
+    if (st != W8_OK)
+        return st;
+    if (!dst)
+        return W8_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(dst) & 255u)
+        return W8_ERR_ALIGN;
+    if (dst_bytes < need)
+        return W8_ERR_CAPACITY;
+
+    int dev = -1, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return W8_ERR_CUDA;
+    if (w8::prepare_gemv_kernels() != cudaSuccess)
+        return W8_ERR_CUDA;
+
+    w8_build *b = new (std::nothrow) w8_build;
+    if (!b)
+        return W8_ERR_CAPACITY;
+    b->device = dev;
+    b->sm_count = sms;
+    b->dtype = d[0].dtype;
+    uint8_t *cursor = static_cast<uint8_t *>(dst);
+    for (int i = 0; i < n_planes; ++i) {
+        const w8_plane_desc &pd = d[i];
+        w8_plane_info info{};
+        info.dtype = pd.dtype;
+        info.layout = W8_LAYOUT_MMA_16x32;
+        info.n = pd.n;
+        info.k = pd.k;
+        info.row_tiles = w8::ceil_div(pd.n, w8::kTileN);
+        info.k_blocks = w8::ceil_div(pd.k, w8::kTileK);
+        float *scale_copy = nullptr;
+        const size_t sb = plane_scale_bytes(pd.dtype, pd.n);
+        if (sb) {
+            scale_copy = reinterpret_cast<float *>(cursor);
+            cursor += w8::align256(sb);
+        }
+        info.scale = scale_copy;
+        info.packed = cursor;
+        info.packed_bytes = plane_packed_bytes(pd.dtype, pd.n, pd.k);
+        cursor += w8::align256(info.packed_bytes);
+
+        w8::RepackArgs ra{};
+        ra.src = static_cast<const uint8_t *>(pd.w);
+        ra.ld_bytes = pd.ldw * elem_bytes(pd.dtype);
+        ra.n = pd.n;
+        ra.k = pd.k;
+        ra.kb = info.k_blocks;
+        ra.rt = info.row_tiles;
+        ra.dst = static_cast<uint8_t *>(const_cast<void *>(info.packed));
+        ra.scale_src = pd.scale;
+        ra.scale_dst = scale_copy;
+        if (w8::launch_repack(pd.dtype == W8_DT_E4M3FN, ra, reinterpret_cast<cudaStream_t>(s)) !=
+            cudaSuccess) {
+            delete b;
+            return W8_ERR_CUDA;
+        }
+        b->planes.push_back(info);
+    }
+    *out = b;
+    return W8_OK;
+}
+
+void w8_release(w8_build *b) { delete b; }
+
+int w8_build_planes(const w8_build *b) { return b ? int(b->planes.size()) : 0; }
+
+w8_status w8_build_info(const w8_build *b, int plane, w8_plane_info *info)
+{
+    if (!b || !info)
+        return W8_ERR_NULL;
+    if (plane < 0 || plane >= int(b->planes.size()))
+        return W8_ERR_PLANE;
+    *info = b->planes[size_t(plane)];
+    return W8_OK;
+}
+
+w8_status w8_plan_shape(int64_t n, int64_t k, int m, int sm_count, w8_plan *out)
+{
+    if (!out)
+        return W8_ERR_NULL;
+    if (n < 1 || k < 1 || n > kMaxDim || k > kMaxDim || m < 1 || m > w8::kMaxM || sm_count < 1)
+        return W8_ERR_SHAPE;
+    const w8::Plan pl = w8::make_plan(n, k, m, sm_count);
+    out->grid = pl.grid;
+    out->block = w8::kThreads;
+    out->smem_bytes = pl.smem;
+    out->n_tiles = pl.nt;
+    out->row_tiles_per_warp = pl.r;
+    out->row_groups = pl.row_groups;
+    out->splits = pl.splits;
+    out->k_blocks_per_split_max = pl.kbs_max;
+    out->workspace_bytes = pl.ws_bytes;
+    return W8_OK;
+}
+
+w8_status w8_plan_info(const w8_build *b, int plane, int m, w8_plan *out)
+{
+    if (!b || !out)
+        return W8_ERR_NULL;
+    if (plane < 0 || plane >= int(b->planes.size()))
+        return W8_ERR_PLANE;
+    const w8_plane_info &p = b->planes[size_t(plane)];
+    return w8_plan_shape(p.n, p.k, m, b->sm_count, out);
+}
+
+w8_status w8_workspace_bytes(const w8_build *b, int plane, int m, size_t *bytes)
+{
+    if (!b || !bytes)
+        return W8_ERR_NULL;
+    if (plane < -1 || plane >= int(b->planes.size()))
+        return W8_ERR_PLANE;
+    if (m < 0 || m > w8::kMaxM)
+        return W8_ERR_SHAPE;
+    size_t best = 0;
+    const int p0 = plane < 0 ? 0 : plane;
+    const int p1 = plane < 0 ? int(b->planes.size()) : plane + 1;
+    for (int pi = p0; pi < p1; ++pi) {
+        const w8_plane_info &p = b->planes[size_t(pi)];
+        const int m0 = m == 0 ? 1 : m, m1 = m == 0 ? w8::kMaxM : m;
+        for (int mm = m0; mm <= m1; ++mm) {
+            const size_t ws = w8::make_plan(p.n, p.k, mm, b->sm_count).ws_bytes;
+            if (ws > best)
+                best = ws;
+        }
+    }
+    *bytes = best;
+    return W8_OK;
+}
+
+w8_status w8_gemv(const w8_build *b, int plane, const uint16_t *x, int64_t ldx, int m,
+                  uint16_t *y, int64_t ldy, void *workspace, size_t workspace_bytes, w8_stream s)
+{
+    return gemv_common(b, plane, W8_DT_E4M3FN, x, ldx, m, y, ldy, workspace, workspace_bytes, s);
+}
+
+w8_status bf16_gemv(const w8_build *b, int plane, const uint16_t *x, int64_t ldx, int m,
+                    uint16_t *y, int64_t ldy, void *workspace, size_t workspace_bytes, w8_stream s)
+{
+    return gemv_common(b, plane, W8_DT_BF16, x, ldx, m, y, ldy, workspace, workspace_bytes, s);
+}
+
+int64_t w8_packed_offset(int dtype, int64_t k_blocks, int64_t row, int64_t col)
+{
+    if (k_blocks < 1 || row < 0 || col < 0 || col >= k_blocks * w8::kTileK)
+        return -1;
+    if (dtype == W8_DT_E4M3FN)
+        return w8::packed_offset_fp8(k_blocks, row, col);
+    if (dtype == W8_DT_BF16)
+        return w8::packed_offset_bf16(k_blocks, row, col);
+    return -1;
+}
+
+} // extern "C"

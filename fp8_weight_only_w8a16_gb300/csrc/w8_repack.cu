@@ -1,0 +1,149 @@
+// w8_repack.cu -- bind-time repack of a row-major plane into W8_LAYOUT_MMA_16x32.
+//
+// The PR page (Changes) binds FP8 planes "in place" in AITER's (16, 16)
+// preshuffle; here bind instead copies each plane once into the caller's
+// packed buffer, in the order the GEMV's tensor-core A operand wants (see
+// w8_layout.h).  One CTA per 16-row tile.  Each thread produces one lane's
+// 16-byte vector of one K block: it reads 8 consecutive columns of rows g and
+// g+8 of the tile (8- or 16-byte loads; the source rows are 16-byte aligned),
+// zero-fills columns >= K and rows >= N, interleaves them and writes 16 bytes.
+// FP8 also writes the build's copy of the row scales; a row that holds a NaN
+// code (0x7F or 0xFF) gets a NaN scale, so its outputs are NaN as the
+// definition gives, while the GEMV's widening stays a fixed exact map.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "w8_internal.h"
+
+namespace w8 {
+namespace {
+
+// 8 consecutive bytes of one source row starting at column col (zero past K).
+__device__ __forceinline__ uint2 load8_fp8(const uint8_t *row, int64_t col, int64_t k)
+{
+    if (col + 8 <= k)
+        return *reinterpret_cast<const uint2 *>(row + col);
+    uint8_t b[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        b[e] = (col + e < k) ? row[col + e] : uint8_t(0);
+    uint2 v;
+    v.x = b[0] | (uint32_t(b[1]) << 8) | (uint32_t(b[2]) << 16) | (uint32_t(b[3]) << 24);
+    v.y = b[4] | (uint32_t(b[5]) << 8) | (uint32_t(b[6]) << 16) | (uint32_t(b[7]) << 24);
+    return v;
+}
+
+// 8 consecutive bf16 of one source row starting at column col (zero past K).
+__device__ __forceinline__ uint4 load8_bf16(const uint16_t *row, int64_t col, int64_t k)
+{
+    if (col + 8 <= k)
+        return *reinterpret_cast<const uint4 *>(row + col);
+    uint16_t h[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        h[e] = (col + e < k) ? row[col + e] : uint16_t(0);
+    return make_uint4(h[0] | (uint32_t(h[1]) << 16), h[2] | (uint32_t(h[3]) << 16),
+                      h[4] | (uint32_t(h[5]) << 16), h[6] | (uint32_t(h[7]) << 16));
+}
+
+__device__ __forceinline__ uint32_t byte_of(uint2 v, int j)
+{
+    return ((j < 4 ? v.x : v.y) >> (8 * (j & 3))) & 0xFFu;
+}
+
+__device__ __forceinline__ bool has_nan_code(uint2 v)
+{
+    // a byte whose low 7 bits are all ones is 0x7F or 0xFF
+    uint32_t nan = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        nan |= ((byte_of(v, j) & 0x7Fu) == 0x7Fu);
+    return nan != 0;
+}
+
+__global__ void __launch_bounds__(256) repack_fp8_kernel(const RepackArgs a)
+{
+    __shared__ int nan_row[16];
+    if (threadIdx.x < 16)
+        nan_row[threadIdx.x] = 0;
+    __syncthreads();
+
+    const int64_t rt = blockIdx.x;
+    const int64_t items = a.kb * 32;
+    for (int64_t it = threadIdx.x; it < items; it += blockDim.x) {
+        const int64_t kb = it >> 5;
+        const int lane = int(it & 31);
+        const int g = lane >> 2, t = lane & 3;
+        const int64_t col = kb * kTileK + 8 * t;
+        uint2 lo = make_uint2(0, 0), hi = make_uint2(0, 0);
+        const int64_t n0 = rt * kTileN + g, n1 = n0 + 8;
+        if (n0 < a.n)
+            lo = load8_fp8(a.src + n0 * a.ld_bytes, col, a.k);
+        if (n1 < a.n)
+            hi = load8_fp8(a.src + n1 * a.ld_bytes, col, a.k);
+        if (has_nan_code(lo))
+            atomicOr(&nan_row[g], 1);
+        if (has_nan_code(hi))
+            atomicOr(&nan_row[g + 8], 1);
+        // word w = 2q + h covers columns 4q + 2h (even) and 4q + 2h + 1 (odd):
+        // bytes (row g even, row g+8 even, row g odd, row g+8 odd)
+        uint32_t out[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const int je = 2 * w, jo = 2 * w + 1; // columns 4q+2h, 4q+2h+1 == 2w, 2w+1
+            out[w] = byte_of(lo, je) | (byte_of(hi, je) << 8) | (byte_of(lo, jo) << 16) |
+                     (byte_of(hi, jo) << 24);
+        }
+        *reinterpret_cast<uint4 *>(a.dst + ((rt * a.kb + kb) * 32 + lane) * 16) =
+            make_uint4(out[0], out[1], out[2], out[3]);
+    }
+    __syncthreads();
+    if (threadIdx.x < 16) {
+        const int64_t n = rt * kTileN + threadIdx.x;
+        float s = 0.0f;
+        if (n < a.n)
+            s = nan_row[threadIdx.x] ? __int_as_float(0x7FC00000) : a.scale_src[n];
+        a.scale_dst[n] = s;
+    }
+}
+
+__global__ void __launch_bounds__(256) repack_bf16_kernel(const RepackArgs a)
+{
+    const int64_t rt = blockIdx.x;
+    const int64_t items = a.kb * 32;
+    for (int64_t it = threadIdx.x; it < items; it += blockDim.x) {
+        const int64_t kb = it >> 5;
+        const int lane = int(it & 31);
+        const int g = lane >> 2, t = lane & 3;
+        const int64_t col = kb * kTileK + 8 * t;
+        uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+        const int64_t n0 = rt * kTileN + g, n1 = n0 + 8;
+        if (n0 < a.n)
+            lo = load8_bf16(reinterpret_cast<const uint16_t *>(a.src + n0 * a.ld_bytes), col, a.k);
+        if (n1 < a.n)
+            hi = load8_bf16(reinterpret_cast<const uint16_t *>(a.src + n1 * a.ld_bytes), col, a.k);
+        // half q: a01 = row g cols 4q+0,1; a23 = row g+8 cols 4q+0,1;
+        //         a45 = row g cols 4q+2,3;  a67 = row g+8 cols 4q+2,3
+        const uint4 h0 = make_uint4(lo.x, hi.x, lo.y, hi.y);
+        const uint4 h1 = make_uint4(lo.z, hi.z, lo.w, hi.w);
+        uint8_t *d = a.dst + (rt * a.kb + kb) * 2 * 512 + lane * 16;
+        *reinterpret_cast<uint4 *>(d) = h0;
+        *reinterpret_cast<uint4 *>(d + 512) = h1;
+    }
+}
+
+} // namespace
+
+cudaError_t launch_repack(bool fp8, const RepackArgs &a, cudaStream_t s)
+{
+    if (a.rt <= 0)
+        return cudaSuccess;
+    if (fp8)
+        repack_fp8_kernel<<<dim3(unsigned(a.rt)), 256, 0, s>>>(a);
+    else
+        repack_bf16_kernel<<<dim3(unsigned(a.rt)), 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+} // namespace w8

@@ -1,0 +1,281 @@
+"""Thin ctypes binding of libw8 (include/w8.h): argument marshalling only.
+
+Every step of the GEMV runs in the library's CUDA kernels; this module turns
+torch tensors into pointers, sizes and a stream handle and turns status codes
+into exceptions.  PyTorch provides device memory and streams only.  There is
+no fallback: if libw8.so is missing, importing this module raises.
+
+Names follow the C ABI: ``validate``, ``packed_bytes``, ``bind`` (w8_bind),
+``w8_gemv``, ``bf16_gemv``, ``workspace_bytes``, ``plan_info``,
+``packed_offset``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+from . import build_lib
+
+LIB_PATH = build_lib.LIB
+
+DT_E4M3FN, DT_BF16, DT_E4M3FNUZ, DT_E5M2, DT_FP16 = 1, 2, 3, 4, 5
+SRC_ROW_MAJOR = 0
+LAYOUT_MMA_16x32 = 1
+MAX_M = 64
+
+STATUS = {
+    0: "W8_OK", 1: "W8_ERR_NULL", 2: "W8_ERR_DTYPE", 3: "W8_ERR_UNPADDED", 4: "W8_ERR_BIAS",
+    5: "W8_ERR_MIXED", 6: "W8_ERR_SHAPE", 7: "W8_ERR_SCALE", 8: "W8_ERR_LAYOUT",
+    9: "W8_ERR_CAPACITY", 10: "W8_ERR_ALIGN", 11: "W8_ERR_PLANE", 12: "W8_ERR_DEVICE",
+    13: "W8_ERR_CUDA",
+}
+
+
+class W8Error(RuntimeError):
+    def __init__(self, status: int, text: str):
+        super().__init__(f"{STATUS.get(status, status)}: {text}")
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+
+
+class PlaneDesc(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("layout", ctypes.c_int32),
+                ("n", ctypes.c_int64), ("k", ctypes.c_int64), ("ldw", ctypes.c_int64),
+                ("scale", ctypes.c_void_p), ("bias", ctypes.c_void_p)]
+
+
+class PlaneInfo(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int32), ("layout", ctypes.c_int32), ("n", ctypes.c_int64),
+                ("k", ctypes.c_int64), ("row_tiles", ctypes.c_int64),
+                ("k_blocks", ctypes.c_int64), ("packed", ctypes.c_void_p),
+                ("scale", ctypes.c_void_p), ("packed_bytes", ctypes.c_size_t)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("grid", ctypes.c_int32), ("block", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_int32), ("n_tiles", ctypes.c_int32),
+                ("row_tiles_per_warp", ctypes.c_int32), ("row_groups", ctypes.c_int32),
+                ("splits", ctypes.c_int32), ("k_blocks_per_split_max", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"libw8.so is not built ({LIB_PATH}); run `python -c \"import __graft_entry__ as g; "
+            "g.build()\"` first -- there is no CPU fallback")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    st = ctypes.c_int
+    lib.w8_status_str.argtypes = [st]
+    lib.w8_status_str.restype = ctypes.c_char_p
+    lib.w8_abi_version.argtypes = []
+    lib.w8_abi_version.restype = i32
+    lib.w8_validate.argtypes = [ctypes.POINTER(PlaneDesc), i32]
+    lib.w8_validate.restype = st
+    lib.w8_packed_bytes.argtypes = [ctypes.POINTER(PlaneDesc), i32, ctypes.POINTER(sz)]
+    lib.w8_packed_bytes.restype = st
+    lib.w8_bind.argtypes = [ctypes.POINTER(PlaneDesc), i32, vp, sz, vp, ctypes.POINTER(vp)]
+    lib.w8_bind.restype = st
+    lib.w8_release.argtypes = [vp]
+    lib.w8_release.restype = None
+    lib.w8_build_planes.argtypes = [vp]
+    lib.w8_build_planes.restype = i32
+    lib.w8_build_info.argtypes = [vp, i32, ctypes.POINTER(PlaneInfo)]
+    lib.w8_build_info.restype = st
+    lib.w8_plan_info.argtypes = [vp, i32, i32, ctypes.POINTER(PlanInfo)]
+    lib.w8_plan_info.restype = st
+    lib.w8_plan_shape.argtypes = [i64, i64, i32, i32, ctypes.POINTER(PlanInfo)]
+    lib.w8_plan_shape.restype = st
+    lib.w8_workspace_bytes.argtypes = [vp, i32, i32, ctypes.POINTER(sz)]
+    lib.w8_workspace_bytes.restype = st
+    for name in ("w8_gemv", "bf16_gemv"):
+        f = getattr(lib, name)
+        f.argtypes = [vp, i32, vp, i64, i32, vp, i64, vp, sz, vp]
+        f.restype = st
+    lib.w8_packed_offset.argtypes = [i32, i64, i64, i64]
+    lib.w8_packed_offset.restype = i64
+    return lib
+
+
+lib = _load()
+
+# every symbol include/w8.h declares
+EXPORTS = ("w8_status_str", "w8_abi_version", "w8_validate", "w8_packed_bytes", "w8_bind",
+           "w8_release", "w8_build_planes", "w8_build_info", "w8_plan_info", "w8_plan_shape",
+           "w8_workspace_bytes", "w8_gemv", "bf16_gemv", "w8_packed_offset")
+
+
+def _check(status: int):
+    if status != 0:
+        raise W8Error(status, lib.w8_status_str(status).decode())
+
+
+def status_str(status: int) -> str:
+    return lib.w8_status_str(status).decode()
+
+
+# ---------------------------------------------------------------------------
+# plane descriptors
+# ---------------------------------------------------------------------------
+
+@dataclass
+class Plane:
+    """A source plane on the device: w [n, ldw] (uint8 codes or bf16), scale [n] fp32."""
+
+    w: torch.Tensor
+    dtype: int
+    n: int
+    k: int
+    ldw: int
+    scale: torch.Tensor | None = None
+    bias: torch.Tensor | None = None
+    layout: int = SRC_ROW_MAJOR
+
+    @staticmethod
+    def from_tensor(w: torch.Tensor, scale: torch.Tensor | None = None, k: int | None = None,
+                    dtype: int | None = None) -> "Plane":
+        """w: 2-D with unit column stride; uint8 -> E4M3FN codes, bfloat16/int16/uint16 -> bf16."""
+        assert w.dim() == 2 and w.stride(1) == 1, "plane must be row-major with unit column stride"
+        if dtype is None:
+            if w.dtype in (torch.uint8, torch.float8_e4m3fn):
+                dtype = DT_E4M3FN
+            elif w.dtype in (torch.bfloat16, torch.int16, torch.uint16):
+                dtype = DT_BF16
+            elif w.dtype == torch.float8_e5m2:
+                dtype = DT_E5M2
+            elif w.dtype == torch.float8_e4m3fnuz:
+                dtype = DT_E4M3FNUZ
+            elif w.dtype == torch.float16:
+                dtype = DT_FP16
+            else:
+                raise TypeError(f"no w8 dtype for {w.dtype}")
+        return Plane(w=w, dtype=dtype, n=w.shape[0], k=w.shape[1] if k is None else k,
+                     ldw=w.stride(0), scale=scale)
+
+    def desc(self) -> PlaneDesc:
+        return PlaneDesc(self.w.data_ptr() if self.w is not None else None, self.dtype,
+                         self.layout, self.n, self.k, self.ldw,
+                         self.scale.data_ptr() if self.scale is not None else None,
+                         self.bias.data_ptr() if self.bias is not None else None)
+
+
+def _descs(planes):
+    arr = (PlaneDesc * len(planes))()
+    for i, p in enumerate(planes):
+        arr[i] = p.desc() if isinstance(p, Plane) else p
+    return arr
+
+
+def validate(planes) -> None:
+    arr = _descs(planes)
+    _check(lib.w8_validate(arr, len(planes)))
+
+
+def packed_bytes(planes) -> int:
+    arr = _descs(planes)
+    out = ctypes.c_size_t(0)
+    _check(lib.w8_packed_bytes(arr, len(planes), ctypes.byref(out)))
+    return int(out.value)
+
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+class Build:
+    """A bound build: owns the library handle and keeps the packed buffer alive."""
+
+    def __init__(self, handle: int, dst: torch.Tensor, planes):
+        self._h = ctypes.c_void_p(handle)
+        self.dst = dst
+        self.n_planes = lib.w8_build_planes(self._h)
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        if not self._h:
+            raise ValueError("build was released")
+        return self._h
+
+    def info(self, plane: int = 0) -> PlaneInfo:
+        out = PlaneInfo()
+        _check(lib.w8_build_info(self.handle, plane, ctypes.byref(out)))
+        return out
+
+    def plan(self, plane: int, m: int) -> PlanInfo:
+        out = PlanInfo()
+        _check(lib.w8_plan_info(self.handle, plane, m, ctypes.byref(out)))
+        return out
+
+    def workspace_bytes(self, plane: int = -1, m: int = 0) -> int:
+        out = ctypes.c_size_t(0)
+        _check(lib.w8_workspace_bytes(self.handle, plane, m, ctypes.byref(out)))
+        return int(out.value)
+
+    def new_workspace(self, plane: int = -1, m: int = 0, device=None) -> torch.Tensor:
+        """A zero-filled workspace (its counter head must start at zero)."""
+        nbytes = max(self.workspace_bytes(plane, m), 256)
+        return torch.zeros(nbytes, dtype=torch.uint8, device=device or self.dst.device)
+
+    def release(self):
+        if self._h:
+            lib.w8_release(self._h)
+            self._h = ctypes.c_void_p(None)
+
+    def __del__(self):
+        try:
+            self.release()
+        except Exception:
+            pass
+
+
+def bind(planes, dst: torch.Tensor | None = None, stream=None) -> Build:
+    """w8_bind: validate and repack planes into dst (allocated here when None)."""
+    arr = _descs(planes)
+    need = packed_bytes(planes)
+    if dst is None:
+        dev = planes[0].w.device if isinstance(planes[0], Plane) else torch.device("cuda")
+        dst = torch.empty(need, dtype=torch.uint8, device=dev)
+    out = ctypes.c_void_p(None)
+    _check(lib.w8_bind(arr, len(planes), ctypes.c_void_p(dst.data_ptr()),
+                       dst.numel() * dst.element_size(), _stream_ptr(stream), ctypes.byref(out)))
+    return Build(out.value, dst, planes)
+
+
+def _gemv(fn, build: Build, plane: int, x: torch.Tensor, y: torch.Tensor,
+          workspace: torch.Tensor | None, m: int | None, stream):
+    assert x.dim() == 2 and x.stride(1) == 1 and x.element_size() == 2
+    assert y.dim() == 2 and y.stride(1) == 1 and y.element_size() == 2
+    m = x.shape[0] if m is None else m
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(fn(build.handle, plane, ctypes.c_void_p(x.data_ptr()), x.stride(0), m,
+              ctypes.c_void_p(y.data_ptr()), y.stride(0), ws_ptr, ws_bytes, _stream_ptr(stream)))
+    return y
+
+
+def w8_gemv(build: Build, plane: int, x: torch.Tensor, y: torch.Tensor,
+            workspace: torch.Tensor | None = None, m: int | None = None, stream=None):
+    """y[:m, :N] = bf16(scale * W x^T)^T on an E4M3FN build (one kernel launch)."""
+    return _gemv(lib.w8_gemv, build, plane, x, y, workspace, m, stream)
+
+
+def bf16_gemv(build: Build, plane: int, x: torch.Tensor, y: torch.Tensor,
+              workspace: torch.Tensor | None = None, m: int | None = None, stream=None):
+    """y[:m, :N] = bf16(W x^T)^T on a BF16 build (one kernel launch)."""
+    return _gemv(lib.bf16_gemv, build, plane, x, y, workspace, m, stream)
+
+
+def plan_shape(n: int, k: int, m: int, sm_count: int) -> PlanInfo:
+    out = PlanInfo()
+    _check(lib.w8_plan_shape(n, k, m, sm_count, ctypes.byref(out)))
+    return out
+
+
+def packed_offset(dtype: int, k_blocks: int, row: int, col: int) -> int:
+    return int(lib.w8_packed_offset(dtype, k_blocks, row, col))

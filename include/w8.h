@@ -1,0 +1,214 @@
+/*
+ * w8.h -- C ABI of libw8: the FP8 weight-only (w8a16) decode GEMV for one
+ * GB300 GPU (sm_103a).
+ *
+ * What the library computes (ATOM PR #2980 "FP8 reads for mono decode",
+ * sections Summary and Changes): for a bound weight plane W [N, K] and M
+ * decode tokens x [M, K] (bf16),
+ *
+ *     y[m, n] = bf16_rne( scale[n] * sum_k bf16(W[n, k]) * x[m, k] )
+ *
+ * W is an E4M3fn plane with one fp32 scale per output row ("E4M3 ..., an fp32
+ * scale per row"); every E4M3fn code widens exactly to bf16 ("FP8 widens
+ * exactly to bf16"); accumulation is fp32 and the scale multiplies each fully
+ * reduced row before the single bf16 rounding ("scales each reduced row before
+ * the bf16 rounding").  A bf16 plane runs through the same computation with no
+ * scale ("bf16 planes run as before").
+ *
+ * Conventions for every function below:
+ *  - Pointers named "device" point into CUDA device memory of the device that
+ *    is current when the call is made; pointers named "host" point into host
+ *    memory.  The caller owns all device memory: source planes, scales, the
+ *    packed buffer, activations, outputs and workspace.  The library owns
+ *    only the small host-side w8_build handle.
+ *  - Every function returns a w8_status.  Arguments are checked on the host
+ *    before anything is enqueued; nothing traps on the device and no function
+ *    exits the process.  A failed launch or CUDA call returns W8_ERR_CUDA.
+ *  - w8_gemv and bf16_gemv are asynchronous on the caller's stream, never
+ *    synchronise and launch exactly one kernel.  w8_bind enqueues its repack
+ *    kernels on the caller's stream and does not synchronise either.
+ *  - A stream argument is a cudaStream_t (NULL is the legacy default stream).
+ */
+#ifndef W8_H
+#define W8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define W8_ABI_VERSION 1
+
+/* A cudaStream_t: the runtime's stream type is this same pointer type. */
+typedef struct CUstream_st *w8_stream;
+
+typedef enum {
+    W8_OK = 0,
+    W8_ERR_NULL = 1,      /* a required pointer is NULL, or no planes given */
+    W8_ERR_DTYPE = 2,     /* plane dtype the kernels cannot read (e4m3fnuz, e5m2, fp16,
+                             unknown), or a gemv call whose dtype is not the build's */
+    W8_ERR_UNPADDED = 3,  /* plane base not 16-byte aligned, or row stride not a multiple
+                             of 16 bytes */
+    W8_ERR_BIAS = 4,      /* a bias pointer was given: the GEMV has no bias */
+    W8_ERR_MIXED = 5,     /* bf16 and FP8 planes mixed in one build */
+    W8_ERR_SHAPE = 6,     /* N or K < 1 or too large, ldw < K, M outside 0..64,
+                             ldx < K, ldy < N */
+    W8_ERR_SCALE = 7,     /* an FP8 plane without row scales, or a bf16 plane with them */
+    W8_ERR_LAYOUT = 8,    /* unknown source layout */
+    W8_ERR_CAPACITY = 9,  /* packed buffer or workspace smaller than required */
+    W8_ERR_ALIGN = 10,    /* packed buffer or workspace not 256-byte aligned, or x / y
+                             not 2-byte aligned */
+    W8_ERR_PLANE = 11,    /* plane index outside the build */
+    W8_ERR_DEVICE = 12,   /* the current device is not the one the build was bound on */
+    W8_ERR_CUDA = 13      /* a CUDA runtime call or kernel launch failed */
+} w8_status;
+
+/* Source element types.  Only E4M3FN and BF16 are readable (PR page, Changes
+ * and Limitations: "refuses what the kernels can't read, such as a
+ * non-E4M3fn ... plane"; "anything else, including e4m3fnuz ..., is refused
+ * at bind"). */
+typedef enum {
+    W8_DT_E4M3FN = 1,
+    W8_DT_BF16 = 2,
+    W8_DT_E4M3FNUZ = 3,
+    W8_DT_E5M2 = 4,
+    W8_DT_FP16 = 5
+} w8_dtype;
+
+/* Source layouts: only plain row-major [n][ldw] planes (K contiguous). */
+#define W8_SRC_ROW_MAJOR 0
+
+/* Packed layout the kernels read (recorded in every build; the PR page,
+ * Limitations, notes its own layout "isn't recorded on the tensor"):
+ * rows in tiles of 16, K in blocks of 32, each (tile, block) a 512-byte
+ * (FP8) or 1024-byte (bf16) run holding the 16x32 weights in the order of
+ * the tensor-core A operand, one 16-byte vector per lane.  The K tail and
+ * the row tail are zero-filled. */
+#define W8_LAYOUT_MMA_16x32 1
+
+/* One source weight plane: W[n][ldw] in device memory, row-major. */
+typedef struct {
+    const void *w;        /* device; E4M3 codes (1 byte) or bf16 bits (2 bytes);
+                             16-byte aligned */
+    int32_t dtype;        /* w8_dtype */
+    int32_t layout;       /* W8_SRC_ROW_MAJOR */
+    int64_t n;            /* output rows, >= 1 */
+    int64_t k;            /* logical reduction columns, >= 1; columns k..ldw-1 are ignored */
+    int64_t ldw;          /* row stride in elements, >= k, ldw * element bytes % 16 == 0 */
+    const float *scale;   /* device, [n] fp32 row scales: required for E4M3FN, NULL for BF16 */
+    const void *bias;     /* must be NULL */
+} w8_plane_desc;
+
+/* What a build records about one bound plane. */
+typedef struct {
+    int32_t dtype;           /* W8_DT_E4M3FN or W8_DT_BF16 */
+    int32_t layout;          /* W8_LAYOUT_MMA_16x32 */
+    int64_t n, k;
+    int64_t row_tiles;       /* ceil(n / 16) */
+    int64_t k_blocks;        /* ceil(k / 32) */
+    const void *packed;      /* device, inside the caller's packed buffer */
+    const float *scale;      /* device, the build's copy of the row scales (FP8), else NULL */
+    size_t packed_bytes;     /* bytes of the packed weights */
+} w8_plane_info;
+
+/* The launch a gemv call makes for one (plane, m); returned for inspection. */
+typedef struct {
+    int32_t grid;            /* CTAs */
+    int32_t block;           /* threads per CTA */
+    int32_t smem_bytes;      /* dynamic shared memory per CTA */
+    int32_t n_tiles;         /* 8-token groups of the tensor-core N dimension */
+    int32_t row_tiles_per_warp;
+    int32_t row_groups;      /* CTAs along N */
+    int32_t splits;          /* CTAs along K; > 1 means a workspace is needed */
+    int32_t k_blocks_per_split_max;
+    size_t workspace_bytes;  /* 0 when splits == 1 */
+} w8_plan;
+
+typedef struct w8_build w8_build; /* opaque, host-side, library-owned */
+
+/* Text for a status code (static storage; never NULL). */
+const char *w8_status_str(w8_status s);
+
+/* W8_ABI_VERSION of the loaded library. */
+int w8_abi_version(void);
+
+/* Host-only check of n_planes descriptors, as w8_bind makes them: dtype, layout,
+ * bias, shape, scale presence, 16-byte padding and alignment, and that all
+ * planes share one dtype.  Touches no device memory and calls no CUDA API. */
+w8_status w8_validate(const w8_plane_desc *d, int n_planes);
+
+/* Bytes of the packed buffer w8_bind needs for these planes (host-only).
+ * *bytes is set on W8_OK. */
+w8_status w8_packed_bytes(const w8_plane_desc *d, int n_planes, size_t *bytes);
+
+/* Validate the planes, then repack each into the caller's device buffer dst
+ * (256-byte aligned, at least w8_packed_bytes) on stream s: the weights in
+ * W8_LAYOUT_MMA_16x32 and, for FP8, a copy of the row scales.  An FP8 row
+ * holding a NaN code (0x7F / 0xFF) gets a NaN scale in that copy, so its
+ * outputs are NaN, as the definition gives.  On W8_OK *out is a new handle
+ * for the device current at the call; the source planes and scales may be
+ * freed once the stream has run the repack.  dst must outlive the handle. */
+w8_status w8_bind(const w8_plane_desc *d, int n_planes, void *dst, size_t dst_bytes,
+                  w8_stream s, w8_build **out);
+
+/* Free a handle (host memory only; NULL is ignored).  The caller's buffers
+ * are untouched. */
+void w8_release(w8_build *b);
+
+/* Number of planes in a build, and what one of them holds. */
+int w8_build_planes(const w8_build *b);
+w8_status w8_build_info(const w8_build *b, int plane, w8_plane_info *info);
+
+/* The launch plan of a gemv call on this plane with m tokens (1..64). */
+w8_status w8_plan_info(const w8_build *b, int plane, int m, w8_plan *plan);
+
+/* The same plan for a plane of n rows and k columns on a GPU with sm_count
+ * SMs, computed on the host without a build (no CUDA call).  The plan depends
+ * on (n, k, m, sm_count) only, never on the weight dtype. */
+w8_status w8_plan_shape(int64_t n, int64_t k, int m, int sm_count, w8_plan *plan);
+
+/* Workspace bytes a gemv call on `plane` with `m` tokens needs (0 if none).
+ * plane = -1 takes the largest over all planes, m = 0 the largest over
+ * m = 1..64, so one workspace can serve every call of a build.
+ *
+ * Workspace contract: 256-byte aligned device memory, zero-filled once by the
+ * caller before its first use (its head holds arrival counters that every
+ * call leaves at zero again).  Calls that share a workspace must not overlap
+ * on the GPU: order them on one stream or synchronise between them. */
+w8_status w8_workspace_bytes(const w8_build *b, int plane, int m, size_t *bytes);
+
+/* The FP8 (w8a16) GEMV on an E4M3FN build:
+ *   y[i*ldy + n] = bf16(scale[n] * sum_k W[n,k] * x[i*ldx + k]),  0 <= i < m, 0 <= n < N.
+ * x: device bf16 [m][ldx], ldx >= K, 2-byte aligned (rows that are 16-byte
+ *    aligned with ldx % 8 == 0 are read with 16-byte loads);
+ * y: device bf16 [m][ldy], ldy >= N, written for n < N only;
+ * m: decode tokens, 0..64 (0 is a no-op);
+ * workspace / workspace_bytes: see w8_workspace_bytes (may be NULL / 0 when
+ *    that returns 0).
+ * Returns W8_ERR_DTYPE on a bf16 build.  One kernel launch on s. */
+w8_status w8_gemv(const w8_build *b, int plane, const uint16_t *x, int64_t ldx, int m,
+                  uint16_t *y, int64_t ldy, void *workspace, size_t workspace_bytes,
+                  w8_stream s);
+
+/* The bf16-weight GEMV on a BF16 build: the same call without the scale,
+ *   y[i*ldy + n] = bf16(sum_k W[n,k] * x[i*ldx + k]).
+ * Same summation order as w8_gemv for the same (N, K, m), so a bf16 plane of
+ * widened codes gives bit for bit the FP8 result with unit scales.
+ * Returns W8_ERR_DTYPE on an FP8 build.  One kernel launch on s. */
+w8_status bf16_gemv(const w8_build *b, int plane, const uint16_t *x, int64_t ldx, int m,
+                    uint16_t *y, int64_t ldy, void *workspace, size_t workspace_bytes,
+                    w8_stream s);
+
+/* Host-side address map of W8_LAYOUT_MMA_16x32: byte offset, inside one
+ * plane's packed weights, of element (row, col) of a plane with k_blocks
+ * blocks of 32 columns.  dtype is W8_DT_E4M3FN or W8_DT_BF16; returns -1 on a
+ * bad argument.  The repack kernel places every element at this offset. */
+int64_t w8_packed_offset(int dtype, int64_t k_blocks, int64_t row, int64_t col);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W8_H */

@@ -1,0 +1,207 @@
+"""Host-side tests of the C ABI (no GPU): the library loads and exports every
+symbol include/w8.h declares; w8_validate refuses what the PR page says bind
+refuses (Changes: "a non-E4M3fn or unpadded plane, a bias, or bf16 and FP8
+mixed in one build"; Limitations: e4m3fnuz and every other format); the
+packed address map is a bijection that keeps each lane's 16-byte vector
+inside one (row tile, K block); the launch planner covers K exactly and does
+not depend on the weight dtype.  No compute call is made here.
+"""
+from __future__ import annotations
+
+import os
+import re
+import subprocess
+import sys
+
+import pytest
+
+from fp8_weight_only_w8a16_gb300 import w8
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w8.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w \*]*?\b(\w+)\s*\([^;{]*\)\s*;", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "while")))
+
+
+def test_every_declared_function_is_exported():
+    declared = _declared_functions()
+    assert "w8_gemv" in declared and "bf16_gemv" in declared and "w8_bind" in declared
+    assert sorted(w8.EXPORTS) == declared
+    for name in declared:
+        assert hasattr(w8.lib, name), name
+    nm = subprocess.run(["nm", "-D", "--defined-only", w8.LIB_PATH], capture_output=True,
+                        text=True)
+    if nm.returncode == 0:
+        exported = set(line.split()[-1] for line in nm.stdout.splitlines() if line.strip())
+        assert set(declared) <= exported
+
+
+def test_abi_version_and_status_strings():
+    assert w8.lib.w8_abi_version() == 1
+    for code in range(14):
+        assert w8.status_str(code)
+    assert w8.status_str(99) == "unknown status"
+
+
+FAKE = 0x10000  # a 16-byte aligned address; validate never dereferences it
+
+
+def _desc(**kw):
+    d = dict(w=FAKE, dtype=w8.DT_E4M3FN, layout=0, n=64, k=128, ldw=128, scale=FAKE + 4096,
+             bias=None)
+    d.update(kw)
+    return w8.PlaneDesc(d["w"], d["dtype"], d["layout"], d["n"], d["k"], d["ldw"], d["scale"],
+                        d["bias"])
+
+
+def _status(*descs):
+    arr = (w8.PlaneDesc * len(descs))(*descs)
+    return w8.lib.w8_validate(arr, len(descs))
+
+
+@pytest.mark.parametrize("kw,want", [
+    ({}, "W8_OK"),
+    ({"dtype": w8.DT_BF16, "scale": None, "ldw": 128}, "W8_OK"),
+    ({"w": None}, "W8_ERR_NULL"),
+    ({"dtype": w8.DT_E4M3FNUZ}, "W8_ERR_DTYPE"),
+    ({"dtype": w8.DT_E5M2}, "W8_ERR_DTYPE"),
+    ({"dtype": w8.DT_FP16}, "W8_ERR_DTYPE"),
+    ({"dtype": 99}, "W8_ERR_DTYPE"),
+    ({"layout": 1}, "W8_ERR_LAYOUT"),
+    ({"bias": FAKE}, "W8_ERR_BIAS"),
+    ({"n": 0}, "W8_ERR_SHAPE"),
+    ({"k": 0}, "W8_ERR_SHAPE"),
+    ({"ldw": 64}, "W8_ERR_SHAPE"),
+    ({"n": 1 << 31}, "W8_ERR_SHAPE"),
+    ({"scale": None}, "W8_ERR_SCALE"),
+    ({"dtype": w8.DT_BF16}, "W8_ERR_SCALE"),
+    ({"w": FAKE + 8}, "W8_ERR_UNPADDED"),
+    ({"ldw": 136}, "W8_ERR_UNPADDED"),
+    ({"k": 130, "ldw": 130}, "W8_ERR_UNPADDED"),
+    ({"k": 130, "ldw": 144}, "W8_OK"),
+    ({"dtype": w8.DT_BF16, "scale": None, "ldw": 132}, "W8_ERR_UNPADDED"),
+    ({"dtype": w8.DT_BF16, "scale": None, "ldw": 136}, "W8_OK"),
+])
+def test_validate_refusal_matrix(kw, want):
+    assert w8.STATUS[_status(_desc(**kw))] == want
+
+
+def test_mixed_build_refused_and_empty_list():
+    bf = _desc(dtype=w8.DT_BF16, scale=None)
+    assert w8.STATUS[_status(_desc(), bf)] == "W8_ERR_MIXED"
+    assert w8.STATUS[_status(bf, _desc())] == "W8_ERR_MIXED"
+    assert w8.STATUS[_status(_desc(), _desc(n=7, k=33, ldw=48))] == "W8_OK"
+    assert w8.STATUS[w8.lib.w8_validate(None, 0)] == "W8_ERR_NULL"
+    # a bad plane anywhere in the list is reported before the mix check
+    assert w8.STATUS[_status(_desc(), _desc(bias=FAKE))] == "W8_ERR_BIAS"
+
+
+def test_packed_bytes_formula():
+    # FP8 [100, 200]: 7 tiles x 7 blocks x 512 B, scales 7*16*4 B (each 256-aligned)
+    assert w8.packed_bytes([_desc(n=100, k=200, ldw=208)]) == 25088 + 512
+    # bf16 [16, 32]: one run of 1024 B
+    assert w8.packed_bytes([_desc(dtype=w8.DT_BF16, scale=None, n=16, k=32, ldw=32)]) == 1024
+    two = w8.packed_bytes([_desc(n=100, k=200, ldw=208), _desc(n=16, k=32, ldw=32)])
+    assert two == 25088 + 512 + 512 + 256
+
+
+@pytest.mark.parametrize("dtype,elt", [(w8.DT_E4M3FN, 1), (w8.DT_BF16, 2)])
+def test_packed_offset_is_a_bijection(dtype, elt):
+    rt, kb = 3, 4
+    offs = [w8.packed_offset(dtype, kb, r, c) for r in range(rt * 16) for c in range(kb * 32)]
+    assert all(o % elt == 0 for o in offs)
+    assert sorted(o // elt for o in offs) == list(range(rt * 16 * kb * 32))
+
+
+@pytest.mark.parametrize("dtype,run", [(w8.DT_E4M3FN, 512), (w8.DT_BF16, 1024)])
+def test_packed_offset_lane_vectors(dtype, run):
+    """Each 16-byte vector holds rows g and g+8 of one tile and columns 8t..8t+7
+    of one block, with lane = 4g + t; runs are tile-major then block."""
+    kb = 5
+    for r in range(32):
+        for c in range(kb * 32):
+            o = w8.packed_offset(dtype, kb, r, c)
+            tile, blk = r // 16, c // 32
+            assert o // run == tile * kb + blk
+            lane = (o % 512) // 16
+            assert lane == 4 * (r % 8) + (c % 32) // 8
+    # the 8 columns of one lane split 4 + 4 between the two tensor-core steps
+    for c in range(32):
+        o = w8.packed_offset(dtype, 1, 0, c)
+        step = (o % 16) // 8 if dtype == w8.DT_E4M3FN else (o // 512)
+        assert step == (c % 8) // 4
+
+
+def test_packed_offset_rejects_bad_arguments():
+    assert w8.packed_offset(w8.DT_E4M3FN, 0, 0, 0) == -1
+    assert w8.packed_offset(w8.DT_E4M3FN, 2, 0, 64) == -1
+    assert w8.packed_offset(w8.DT_E5M2, 2, 0, 0) == -1
+    assert w8.packed_offset(w8.DT_BF16, 2, -1, 0) == -1
+
+
+SHAPES = [(256, 512), (2624, 6144), (6144, 16384), (4096, 6144), (6144, 2048),
+          (16384, 2048), (28672, 512), (4096, 2048), (128, 6144), (32, 6144),
+          (154880, 6144), (1, 1), (37, 77), (100, 4096)]
+
+
+@pytest.mark.parametrize("n,k", SHAPES)
+@pytest.mark.parametrize("m", [1, 2, 4, 8, 9, 16, 17, 32, 33, 64])
+def test_plan_invariants(n, k, m):
+    p = w8.plan_shape(n, k, m, 152)
+    kb = -(-k // 32)
+    rt = -(-n // 16)
+    assert p.grid == p.row_groups * p.splits
+    assert 1 <= p.splits <= kb
+    assert p.k_blocks_per_split_max == -(-kb // p.splits)
+    assert p.row_groups * 8 * p.row_tiles_per_warp >= rt
+    assert (p.row_groups - 1) * 8 * p.row_tiles_per_warp < rt
+    assert p.n_tiles * 8 >= m and (p.n_tiles == 1 or p.n_tiles * 4 < m)
+    limit = (100 if p.n_tiles <= 2 else 200) * 1024
+    assert p.smem_bytes <= limit
+    assert (p.workspace_bytes == 0) == (p.splits == 1)
+    if p.splits > 1:
+        assert p.workspace_bytes >= p.splits * rt * 16 * m * 4
+    # splits tile the K blocks exactly: floor(s * kb / S) boundaries
+    bounds = [(s * kb) // p.splits for s in range(p.splits + 1)]
+    assert bounds[0] == 0 and bounds[-1] == kb
+    assert all(b1 - b0 >= 1 for b0, b1 in zip(bounds, bounds[1:]))
+    assert max(b1 - b0 for b0, b1 in zip(bounds, bounds[1:])) == p.k_blocks_per_split_max
+
+
+def test_plan_refuses_bad_shapes():
+    for args in [(0, 32, 1, 152), (16, 0, 1, 152), (16, 32, 0, 152), (16, 32, 65, 152),
+                 (16, 32, 1, 0)]:
+        with pytest.raises(w8.W8Error) as e:
+            w8.plan_shape(*args)
+        assert e.value.name == "W8_ERR_SHAPE"
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    """With libw8.so absent the binding raises on import: no CPU fallback."""
+    code = (
+        "import sys; sys.path.insert(0, %r)\n"
+        "from fp8_weight_only_w8a16_gb300 import build_lib\n"
+        "build_lib.LIB = %r\n"
+        "try:\n"
+        "    import fp8_weight_only_w8a16_gb300.w8\n"
+        "except ImportError as e:\n"
+        "    print('raised', e)\n"
+        "else:\n"
+        "    print('imported')\n" % (ROOT, str(tmp_path / "missing" / "libw8.so")))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120)
+    assert "raised" in r.stdout and "no CPU fallback" in r.stdout, r.stdout + r.stderr
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "fp8_weight_only_w8a16_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".h", ".cpp", ".cuh")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "w8_oracle" not in text and "liboracle" not in text, f
