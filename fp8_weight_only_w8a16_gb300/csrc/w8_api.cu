@@ -87,7 +87,7 @@ w8_status gemv_common(const w8_build *b, int plane, int32_t want_dtype, const ui
         return W8_ERR_NULL;
     if (ldx < p.k || ldy < p.n)
         return W8_ERR_SHAPE;
-    if ((reinterpret_cast<uintptr_t>(x) & 1u) || (reinterpret_cast<uintptr_t>(y) & 1u))
+    if ((reinterpret_cast<uintptr_t>(x) & 15u) || (ldx & 7) || (reinterpret_cast<uintptr_t>(y) & 1u))
         return W8_ERR_ALIGN;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess)
@@ -109,8 +109,7 @@ w8_status gemv_common(const w8_build *b, int plane, int32_t want_dtype, const ui
     a.kb = int(plan.kb);
     a.rt = int(plan.rt);
     a.splits = plan.splits;
-    a.x_stride = plan.x_stride;
-    a.x_vec = ((reinterpret_cast<uintptr_t>(x) & 15u) == 0 && (ldx & 7) == 0) ? 1 : 0;
+    a.wk = plan.wk;
     if (plan.splits > 1) {
         if (!ws)
             return W8_ERR_NULL;
@@ -146,7 +145,7 @@ const char *w8_status_str(w8_status s)
     case W8_ERR_SCALE: return "FP8 planes need fp32 row scales; bf16 planes take none";
     case W8_ERR_LAYOUT: return "unknown source layout (only row-major)";
     case W8_ERR_CAPACITY: return "packed buffer or workspace too small";
-    case W8_ERR_ALIGN: return "misaligned buffer (packed/workspace: 256 B; x, y: 2 B)";
+    case W8_ERR_ALIGN: return "misaligned buffer (packed/workspace: 256 B; x: 16 B with ldx % 8 == 0; y: 2 B)";
     case W8_ERR_PLANE: return "plane index outside the build";
     case W8_ERR_DEVICE: return "current device is not the device the build was bound on";
     case W8_ERR_CUDA: return "CUDA runtime error";
@@ -255,6 +254,13 @@ w8_status w8_bind(const w8_plane_desc *d, int n_planes, void *dst, size_t dst_by
         }
         b->planes.push_back(info);
     }
+    // The GEMV kernels start reading the packed weights before they wait for
+    // the previous kernel of their stream (programmatic dependent launch), so
+    // the repack must be complete before any GEMV can be enqueued.
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(s)) != cudaSuccess) {
+        delete b;
+        return W8_ERR_CUDA;
+    }
     *out = b;
     return W8_OK;
 }
@@ -285,9 +291,11 @@ w8_status w8_plan_shape(int64_t n, int64_t k, int m, int sm_count, w8_plan *out)
     out->smem_bytes = pl.smem;
     out->n_tiles = pl.nt;
     out->row_tiles_per_warp = pl.r;
+    out->warps_k = pl.wk;
+    out->depth = pl.dw;
     out->row_groups = pl.row_groups;
     out->splits = pl.splits;
-    out->k_blocks_per_split_max = pl.kbs_max;
+    out->k_blocks_per_warp_max = pl.kbs_max;
     out->workspace_bytes = pl.ws_bytes;
     return W8_OK;
 }
@@ -299,7 +307,10 @@ w8_status w8_plan_info(const w8_build *b, int plane, int m, w8_plan *out)
     if (plane < 0 || plane >= int(b->planes.size()))
         return W8_ERR_PLANE;
     const w8_plane_info &p = b->planes[size_t(plane)];
-    return w8_plan_shape(p.n, p.k, m, b->sm_count, out);
+    const w8_status st = w8_plan_shape(p.n, p.k, m, b->sm_count, out);
+    if (st == W8_OK && p.dtype == W8_DT_BF16)
+        out->depth = w8::depth_w(out->n_tiles, out->row_tiles_per_warp, false);
+    return st;
 }
 
 w8_status w8_workspace_bytes(const w8_build *b, int plane, int m, size_t *bytes)

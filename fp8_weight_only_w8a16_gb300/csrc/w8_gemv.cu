@@ -14,15 +14,16 @@
 // integer/fp pipes only widen.  The weights are still read exactly once, with
 // fully coalesced 16-byte loads that stream past L1.
 //
-// Data flow of one CTA (8 warps, see w8_layout.h for the packed layout):
-//   1. issue the first D weight loads of every warp (they do not depend on x);
-//   2. stage x[0..8*NT)[k range] into shared memory (zero past M and past K);
-//   3. per K block: one 16-byte weight load per lane per row tile (D blocks
-//      ahead), one 16-byte shared-memory load of activations per 8 tokens,
-//      widen, two tensor-core steps per (row tile, 8 tokens);
-//   4. splits == 1: scale, round, store.  splits > 1: store fp32 partials,
-//      count arrivals; the last CTA of the row group sums the partials in
-//      split order, scales, rounds and stores.  No CTA waits on another.
+// Work of one CTA (8 warps; see w8_layout.h for the layout and the plan):
+//   1. each warp walks its K part of its R row tiles, one K block per step,
+//      keeping D blocks of weights (HBM) and activations (L2/L1) in flight in
+//      a register ring; per block: widen, two tensor-core steps per
+//      (row tile, 8 tokens);
+//   2. the warps' accumulators meet in shared memory; the wk K parts of each
+//      row are added in K-part order;
+//   3. splits == 1: scale, round, store.  splits > 1: store the fp32 partial,
+//      count arrivals; the last CTA of the row group sums the partials in split
+//      order, scales, rounds and stores.  No CTA ever waits on another.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -40,7 +41,7 @@ namespace {
 __device__ __forceinline__ uint4 ld_stream(const uint8_t *p)
 {
     uint4 v;
-    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
         : "l"(p));
     return v;
@@ -86,6 +87,29 @@ __device__ __forceinline__ uint16_t to_bf16(float f)
     return h;
 }
 
+// 4-byte asynchronous copy global -> shared (the CTA's row scales).
+__device__ __forceinline__ void cp_async4(float *smem, const float *gmem)
+{
+    const uint32_t s = uint32_t(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+}
+
+// Programmatic dependent launch: let the next kernel of the stream begin
+// launching, and wait until the previous one has finished and its writes are
+// visible.  Both are no-ops when the launch carries no programmatic edge.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ float ld_cg_f32(const float *p)
 {
     float v;
@@ -109,6 +133,26 @@ __device__ __forceinline__ void load_w(WFrag<kFp8> &f, const uint8_t *p)
     }
 }
 
+// Predicated weight load: fills f only when ok (f keeps its value otherwise).
+__device__ __forceinline__ void ld_stream_pred(uint4 &v, const uint8_t *p, uint32_t ok)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %5, 0;\n\t"
+                 "@q ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];\n\t}"
+                 : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+                 : "l"(p), "r"(ok));
+}
+
+template <bool kFp8>
+__device__ __forceinline__ void load_w_pred(WFrag<kFp8> &f, const uint8_t *p, uint32_t ok)
+{
+    if constexpr (kFp8) {
+        ld_stream_pred(f.v, p, ok);
+    } else {
+        ld_stream_pred(f.v[0], p, ok);
+        ld_stream_pred(f.v[1], p + 512, ok);
+    }
+}
+
 template <bool kFp8>
 __device__ __forceinline__ void zero_w(WFrag<kFp8> &f)
 {
@@ -118,14 +162,6 @@ __device__ __forceinline__ void zero_w(WFrag<kFp8> &f)
         f.v[0] = make_uint4(0, 0, 0, 0);
         f.v[1] = make_uint4(0, 0, 0, 0);
     }
-}
-
-// The two tensor-core steps of one K block for one (row tile, 8 tokens).
-template <bool kFp8>
-__device__ __forceinline__ void block_mma(float (&c)[4], const uint32_t (&a)[8], uint4 xb)
-{
-    mma_bf16(c, a[0], a[1], a[2], a[3], xb.x, xb.y);
-    mma_bf16(c, a[4], a[5], a[6], a[7], xb.z, xb.w);
 }
 
 template <bool kFp8>
@@ -146,79 +182,129 @@ __device__ __forceinline__ void a_operands(uint32_t (&a)[8], const WFrag<kFp8> &
     }
 }
 
+// 8 activations x[tok][col .. col+7] of one lane, loaded only when `ok`;
+// otherwise v keeps its value (the ring slots of tokens >= m stay zero).
+__device__ __forceinline__ void ld_act_pred(uint4 &v, const uint16_t *p, uint32_t ok)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %5, 0;\n\t"
+                 "@q ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];\n\t}"
+                 : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+                 : "l"(p), "r"(ok));
+}
+
+// The activations of the K-tail block, element by element (zero past K).
+__device__ __forceinline__ uint4 load_x_tail(const uint16_t *p, bool ok, int64_t col, int64_t k)
+{
+    uint16_t h[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        h[e] = (ok && col + e < k) ? p[e] : uint16_t(0);
+    return make_uint4(h[0] | (uint32_t(h[1]) << 16), h[2] | (uint32_t(h[3]) << 16),
+                      h[4] | (uint32_t(h[5]) << 16), h[6] | (uint32_t(h[7]) << 16));
+}
+
+// One K block: widen the R weight fragments and run the two tensor-core steps
+// of every (row tile, 8 tokens) into its accumulator.
+template <bool kFp8, int NT, int R>
+__device__ __forceinline__ void block_step(float (&acc)[R][NT][4], const WFrag<kFp8> (&w)[R],
+                                           const uint4 (&x)[NT])
+{
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        uint32_t aop[8];
+        a_operands<kFp8>(aop, w[r]);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            mma_bf16(acc[r][j], aop[0], aop[1], aop[2], aop[3], x[j].x, x[j].y);
+            mma_bf16(acc[r][j], aop[4], aop[5], aop[6], aop[7], x[j].z, x[j].w);
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <bool kFp8, int NT, int R, int D, int kMinBlocks>
+template <bool kFp8, int NT, int R, int DW, int DX, int kMinBlocks>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvArgs a)
 {
-    extern __shared__ __align__(16) uint8_t xs[];
+    static_assert(DW % DX == 0, "the activation ring depth divides the weight ring depth");
+    extern __shared__ __align__(16) float red[]; // [warp][R][NT][4][32]
     constexpr int kRun = kFp8 ? kRunFp8 : kRunBf16;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2;
     const int t = lane & 3;
+    const int wk = a.wk;
+    const int wt = kWarps / wk;
+    const int tg = warp / wk;       // tile group of this warp
+    const int kp = warp - tg * wk;  // K part of this warp
 
     const int rg = blockIdx.x / a.splits;
     const int sp = blockIdx.x - rg * a.splits;
-    const int kb0 = int((int64_t(sp) * a.kb) / a.splits);
-    const int kb1 = int((int64_t(sp + 1) * a.kb) / a.splits);
-    const int nkb = kb1 - kb0;
+    const int cb0 = int((int64_t(sp) * a.kb) / a.splits);   // CTA's K blocks
+    const int cnb = int((int64_t(sp + 1) * a.kb) / a.splits) - cb0;
+    const int kb0 = cb0 + (kp * cnb) / wk;                  // warp's K blocks
+    const int nkb = cb0 + ((kp + 1) * cnb) / wk - kb0;
 
-    // ---- 1. the warp's row tiles and its first D weight loads ------------
-    int rt[R];
-    bool valid[R];
+    // ---- the warp's row tiles and activation rows ----------------------------
+    // Blocks [0, nmain) of the warp's K part lie wholly inside K; when K is not
+    // a multiple of 32 the plane's last block is partial and is handled after
+    // the pipeline (it can only be the last block of the last K part).
+    const int full_blocks = a.k / kTileK;
+    int nmain = full_blocks - kb0;
+    nmain = nmain < 0 ? 0 : (nmain > nkb ? nkb : nmain);
+    const bool has_tail = nkb > nmain;
+
     const uint8_t *wptr[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-        rt[r] = rg * (kWarps * R) + r * kWarps + warp;
-        valid[r] = rt[r] < a.rt;
-        const int64_t tile = valid[r] ? rt[r] : 0; // idle warps re-read tile 0
-        wptr[r] = a.wp + (tile * a.kb + kb0) * kRun + lane * 16;
+        const int tile = rg * (wt * R) + r * wt + tg;
+        const int64_t t64 = tile < a.rt ? tile : 0; // idle slots re-read tile 0
+        wptr[r] = a.wp + (t64 * a.kb + kb0) * kRun + lane * 16;
     }
-    WFrag<kFp8> ring[D][R];
+    const uint16_t *xptr[NT];
+    uint32_t tok_ok[NT];
 #pragma unroll
-    for (int i = 0; i < D; ++i)
+    for (int j = 0; j < NT; ++j) {
+        const int tok = 8 * j + g;
+        tok_ok[j] = tok < a.m;
+        xptr[j] = a.x + int64_t(tok < a.m ? tok : 0) * a.ldx + int64_t(kb0) * kTileK + 8 * t;
+    }
+
+    // Weights first: the packed plane is written only by w8_bind, which
+    // finishes before any GEMV can be launched, so these loads may overlap the
+    // tail of the previous kernel on the stream.
+    WFrag<kFp8> wring[DW][R];
+    uint4 xring[DX][NT];
+#pragma unroll
+    for (int i = 0; i < DW; ++i)
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            if (i < nkb)
-                load_w<kFp8>(ring[i][r], wptr[r] + int64_t(i) * kRun);
-            else
-                zero_w<kFp8>(ring[i][r]);
+            zero_w<kFp8>(wring[i][r]);
+            if (i < nmain)
+                load_w<kFp8>(wring[i][r], wptr[r] + i * kRun);
         }
-
-    // ---- 2. stage x[tokens][k range] ----------------------------------------
-    {
-        const int cols8 = nkb * 4;            // 8-column chunks in the range
-        const int64_t kbase = int64_t(kb0) * kTileK;
-        const int items = NT * 8 * cols8;
-        for (int idx = threadIdx.x; idx < items; idx += kThreads) {
-            const int tok = idx / cols8;
-            const int c8 = idx - tok * cols8;
-            const int64_t col = kbase + c8 * 8;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (tok < a.m) {
-                const uint16_t *src = a.x + int64_t(tok) * a.ldx + col;
-                if (a.x_vec && col + 8 <= a.k) {
-                    v = __ldg(reinterpret_cast<const uint4 *>(src));
-                } else {
-                    uint16_t h[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        h[e] = (col + e < a.k) ? src[e] : uint16_t(0);
-                    v.x = h[0] | (uint32_t(h[1]) << 16);
-                    v.y = h[2] | (uint32_t(h[3]) << 16);
-                    v.z = h[4] | (uint32_t(h[5]) << 16);
-                    v.w = h[6] | (uint32_t(h[7]) << 16);
-                }
-            }
-            *reinterpret_cast<uint4 *>(xs + tok * a.x_stride + c8 * 16) = v;
-        }
+    // the CTA's row scales (bind-time data too) into shared memory
+    __shared__ float s_scale[kWarps * 2 * kTileN];
+    const int row0 = rg * wt * R * kTileN;
+    if constexpr (kFp8) {
+        if (threadIdx.x < wt * R * kTileN && row0 + int(threadIdx.x) < a.n)
+            cp_async4(s_scale + threadIdx.x, a.scale + row0 + threadIdx.x);
     }
-    __syncthreads();
+    pdl_launch_dependents();
+    // Activations may be the previous kernel's output: wait for it.
+    pdl_wait();
+#pragma unroll
+    for (int i = 0; i < DX; ++i)
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            xring[i][j] = make_uint4(0, 0, 0, 0);
+            if (i < nmain)
+                ld_act_pred(xring[i][j], xptr[j] + i * kTileK, tok_ok[j]);
+        }
 
-    // ---- 3. stream the K range ---------------------------------------------
+    // ---- stream the K part ------------------------------------------------------
     float acc[R][NT][4];
 #pragma unroll
     for (int r = 0; r < R; ++r)
@@ -228,85 +314,95 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
             for (int e = 0; e < 4; ++e)
                 acc[r][j][e] = 0.0f;
 
-    const uint8_t *xrow = xs + g * a.x_stride + t * 16;
-    for (int base = 0; base < nkb; base += D) {
+    // Blocks in ascending order.  Block b sits in weight slot b % DW and
+    // activation slot b % DX; each slot is computed, then refilled (a
+    // predicated load) with the block DW (weights) or DX (activations)
+    // further on.
+    int b = 0;
+    for (; b + DW <= nmain; b += DW) {
 #pragma unroll
-        for (int i = 0; i < D; ++i) {
-            const int b = base + i;
-            if (b < nkb) {
-                WFrag<kFp8> cur[R];
+        for (int i = 0; i < DW; ++i) {
+            block_step<kFp8, NT, R>(acc, wring[i], xring[i % DX]);
+            const uint32_t more_w = (b + DW + i) < nmain;
 #pragma unroll
-                for (int r = 0; r < R; ++r)
-                    cur[r] = ring[i][r];
-                if (b + D < nkb) {
-#pragma unroll
-                    for (int r = 0; r < R; ++r)
-                        load_w<kFp8>(ring[i][r], wptr[r] + int64_t(b + D) * kRun);
-                }
-                uint32_t aop[R][8];
-#pragma unroll
-                for (int r = 0; r < R; ++r)
-                    a_operands<kFp8>(aop[r], cur[r]);
-#pragma unroll
-                for (int j = 0; j < NT; ++j) {
-                    const uint4 xb =
-                        *reinterpret_cast<const uint4 *>(xrow + j * 8 * a.x_stride + b * 64);
-#pragma unroll
-                    for (int r = 0; r < R; ++r)
-                        block_mma<kFp8>(acc[r][j], aop[r], xb);
-                }
-            }
-        }
-    }
-
-    // ---- 4. epilogue ----------------------------------------------------------
-    // Accumulator e of (r, j): row rt*16 + g + 8*(e >> 1), token 8j + 2t + (e & 1).
-    if (a.splits == 1) {
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            if (!valid[r])
-                continue;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int row = rt[r] * kTileN + g + 8 * h;
-                if (row >= a.n)
-                    continue;
-                const float sc = kFp8 ? a.scale[row] : 1.0f;
-#pragma unroll
-                for (int j = 0; j < NT; ++j)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int tok = 8 * j + 2 * t + e;
-                        if (tok < a.m) {
-                            const float v = acc[r][j][2 * h + e];
-                            a.y[int64_t(tok) * a.ldy + row] = to_bf16(kFp8 ? sc * v : v);
-                        }
-                    }
-            }
-        }
-        return;
-    }
-
-    // splits > 1: partials [split][row][token]
-    const int64_t rows_pad = int64_t(a.rt) * kTileN;
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        if (!valid[r])
-            continue;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int row = rt[r] * kTileN + g + 8 * h;
-            float *dst = a.partial + (int64_t(sp) * rows_pad + row) * a.m;
+            for (int r = 0; r < R; ++r)
+                load_w_pred<kFp8>(wring[i][r], wptr[r] + (b + DW + i) * kRun, more_w);
+            const uint32_t more_x = (b + DX + i) < nmain;
 #pragma unroll
             for (int j = 0; j < NT; ++j)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int tok = 8 * j + 2 * t + e;
-                    if (tok < a.m)
-                        dst[tok] = acc[r][j][2 * h + e];
-                }
+                ld_act_pred(xring[i % DX][j], xptr[j] + (b + DX + i) * kTileK,
+                            tok_ok[j] & more_x);
         }
     }
+    // the last partial group (fewer than DW blocks, all weights in flight)
+#pragma unroll
+    for (int i = 0; i < DW - 1; ++i) {
+        if (b + i < nmain) {
+            block_step<kFp8, NT, R>(acc, wring[i], xring[i % DX]);
+            const uint32_t more_x = (b + DX + i) < nmain;
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+                ld_act_pred(xring[i % DX][j], xptr[j] + (b + DX + i) * kTileK,
+                            tok_ok[j] & more_x);
+        }
+    }
+    if (has_tail) {
+        // the partial last block: zero activations past K (its weights past K
+        // are zero-filled by the repack)
+        WFrag<kFp8> tw[R];
+        uint4 tx[NT];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            load_w<kFp8>(tw[r], wptr[r] + nmain * kRun);
+        const int64_t col = int64_t(kb0 + nmain) * kTileK + 8 * t;
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+            tx[j] = load_x_tail(xptr[j] + nmain * kTileK, tok_ok[j] != 0, col, a.k);
+        block_step<kFp8, NT, R>(acc, tw, tx);
+    }
+
+    // ---- K parts meet in shared memory ---------------------------------------
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                red[(((warp * R + r) * NT + j) * 4 + e) * 32 + lane] = acc[r][j][e];
+    if constexpr (kFp8)
+        cp_async_wait_all();
+    __syncthreads();
+
+    // One item per (tile group, r, j, e, lane): 8 * R * NT * 128 / wk items.
+    // Accumulator e of lane (g, t): row g + 8*(e >> 1), token 8j + 2t + (e & 1).
+    const int items = wt * R * NT * 128;
+    const int64_t rows_pad = int64_t(a.rt) * kTileN;
+    for (int it = threadIdx.x; it < items; it += kThreads) {
+        const int ln = it & 31;
+        const int e = (it >> 5) & 3;
+        const int j = (it >> 7) % NT;
+        const int r = ((it >> 7) / NT) % R;
+        const int grp = ((it >> 7) / NT) / R;
+        const int tile = rg * (wt * R) + r * wt + grp;
+        const int row = tile * kTileN + (ln >> 2) + 8 * (e >> 1);
+        const int tok = 8 * j + 2 * (ln & 3) + (e & 1);
+        if (tile >= a.rt || tok >= a.m)
+            continue;
+        const float *src = red + ((((grp * wk) * R + r) * NT + j) * 4 + e) * 32 + ln;
+        float v = src[0];
+        for (int q = 1; q < wk; ++q)
+            v += src[q * R * NT * 128];
+        if (a.splits == 1) {
+            if (row < a.n)
+                a.y[int64_t(tok) * a.ldy + row] = to_bf16(kFp8 ? s_scale[row - row0] * v : v);
+        } else {
+            a.partial[(int64_t(sp) * rows_pad + row) * a.m + tok] = v;
+        }
+    }
+    if (a.splits == 1)
+        return;
+
+    // ---- splits > 1: the last CTA of the row group adds the partials ---------
     __threadfence();
     __syncthreads();
     __shared__ int s_last;
@@ -319,44 +415,53 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
         return;
     __threadfence();
 
-    // The last CTA of the row group: sum the partials in split order.
-    const int row0 = rg * kWarps * R * kTileN;
-    int row_end = row0 + kWarps * R * kTileN;
+    int row_end = row0 + wt * R * kTileN;
     if (row_end > a.n)
         row_end = a.n;
-    const int nrows = row_end - row0;
-    const int items = nrows * a.m;
-    for (int idx = threadIdx.x; idx < items; idx += kThreads) {
-        const int tok = idx / nrows;
-        const int row = row0 + (idx - tok * nrows);
+    const int cnt = (row_end - row0) * a.m; // (row, token) pairs, token fastest
+    const float *base = a.partial + int64_t(row0) * a.m;
+    const int64_t split_stride = rows_pad * a.m;
+    for (int idx = threadIdx.x; idx < cnt; idx += kThreads) {
         float v = 0.0f;
-        for (int s = 0; s < a.splits; ++s)
-            v += ld_cg_f32(a.partial + (int64_t(s) * rows_pad + row) * a.m + tok);
-        a.y[int64_t(tok) * a.ldy + row] = to_bf16(kFp8 ? a.scale[row] * v : v);
+        int s = 0;
+        for (; s + 8 <= a.splits; s += 8) {
+            float p[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                p[q] = ld_cg_f32(base + (s + q) * split_stride + idx);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                v += p[q];
+        }
+        for (; s < a.splits; ++s)
+            v += ld_cg_f32(base + s * split_stride + idx);
+        const int row = row0 + idx / a.m;
+        const int tok = idx - (idx / a.m) * a.m;
+        a.y[int64_t(tok) * a.ldy + row] = to_bf16(kFp8 ? s_scale[row - row0] * v : v);
     }
     if (threadIdx.x == 0)
         a.counters[rg] = 0; // ready for the next call on this workspace
 }
 
 // ---------------------------------------------------------------------------
-// instance table
+// instance table: one kernel per (dtype, NT, R) with the depths of w8_layout.h
 // ---------------------------------------------------------------------------
-template <bool kFp8, int NT>
-struct Inst {
-    static constexpr int R = NT <= 2 ? 1 : 2;
-    static constexpr int D = NT <= 2 ? 8 : 4;
-    static constexpr int B = NT <= 2 ? 2 : 1;
-    static void *fn() { return reinterpret_cast<void *>(&gemv_kernel<kFp8, NT, R, D, B>); }
-};
+template <bool kFp8, int NT, int R>
+void *inst()
+{
+    return reinterpret_cast<void *>(
+        &gemv_kernel<kFp8, NT, R, depth_w(NT, R, kFp8), depth_x(NT, R, kFp8),
+                     ctas_per_sm_for_nt(NT)>);
+}
 
 template <bool kFp8>
-void *pick(int nt)
+void *pick(int nt, int r)
 {
     switch (nt) {
-    case 1: return Inst<kFp8, 1>::fn();
-    case 2: return Inst<kFp8, 2>::fn();
-    case 4: return Inst<kFp8, 4>::fn();
-    default: return Inst<kFp8, 8>::fn();
+    case 1: return r == 1 ? inst<kFp8, 1, 1>() : inst<kFp8, 1, 2>();
+    case 2: return inst<kFp8, 2, 2>();
+    case 4: return inst<kFp8, 4, 2>();
+    default: return inst<kFp8, 8, 2>();
     }
 }
 
@@ -364,13 +469,14 @@ void *pick(int nt)
 
 cudaError_t prepare_gemv_kernels()
 {
-    const int nts[4] = {1, 2, 4, 8};
-    for (int i = 0; i < 4; ++i) {
+    // the K-part reduction buffer: 8 warps x R x NT x 128 floats, at most 64 KB
+    const int nts[5] = {1, 1, 2, 4, 8};
+    const int rs[5] = {1, 2, 2, 2, 2};
+    for (int i = 0; i < 5; ++i) {
         for (int f = 0; f < 2; ++f) {
-            void *fn = f ? pick<true>(nts[i]) : pick<false>(nts[i]);
-            const int budget = (nts[i] <= 2 ? 100 : 200) * 1024;
+            void *fn = f ? pick<true>(nts[i], rs[i]) : pick<false>(nts[i], rs[i]);
             cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 budget);
+                                                 64 * 1024);
             if (e != cudaSuccess)
                 return e;
         }
@@ -380,9 +486,22 @@ cudaError_t prepare_gemv_kernels()
 
 cudaError_t launch_gemv(bool fp8, const Plan &plan, const GemvArgs &a, cudaStream_t s)
 {
-    void *fn = fp8 ? pick<true>(plan.nt) : pick<false>(plan.nt);
+    void *fn = fp8 ? pick<true>(plan.nt, plan.r) : pick<false>(plan.nt, plan.r);
     void *args[] = {const_cast<GemvArgs *>(&a)};
-    return cudaLaunchKernel(fn, dim3(plan.grid), dim3(kThreads), args, size_t(plan.smem), s);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(unsigned(plan.grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = size_t(plan.smem);
+    cfg.stream = s;
+    // programmatic dependent launch: this kernel may start while the previous
+    // kernel of the stream drains; it reads no activation and writes nothing
+    // before griddepcontrol.wait
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 } // namespace w8

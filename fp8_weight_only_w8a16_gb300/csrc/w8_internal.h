@@ -19,8 +19,7 @@ struct GemvArgs {
     int kb;                 // K blocks
     int rt;                 // row tiles
     int splits;
-    int x_stride;           // bytes between staged token rows
-    int x_vec;              // 1: x rows may be read with 16-byte loads
+    int wk;                 // warps of a tile group along K
     int *counters;          // workspace head (splits > 1)
     float *partial;         // workspace body: [splits][rt*16][m] fp32 (splits > 1)
 };

@@ -75,70 +75,124 @@ W8_HD int64_t packed_offset_bf16(int64_t k_blocks, int64_t row, int64_t col)
 // Launch plan.  A function of (N, K, m, SM count) only -- never of the weight
 // dtype -- so FP8 and bf16 planes of one shape sum in the same order.
 //
-// The grid is row_groups x splits CTAs.  A CTA owns kWarps*R row tiles (warp w
-// takes tiles w, w+8, ...) and one contiguous range of K blocks; it stages
-// that range of x in shared memory once and streams its weight runs straight
-// into registers.  With splits > 1 each CTA writes fp32 partial sums to the
+// A CTA has kWarps warps arranged as wt tile groups x wk K parts (wt*wk = 8).
+// It owns wt*R row tiles (tile group tg takes tiles tg, tg+wt, ...; each warp
+// of the group holds R of them) and one range of K blocks (split sp of
+// `splits`), which the wk warps of a group cut into wk contiguous parts.  Each
+// warp streams its (R tiles x K part) straight from HBM into registers, D
+// blocks ahead, with the matching activations from L2/L1.  The wk partial
+// sums of a tile meet in shared memory and are added in K-part order.  With
+// splits > 1 (only for planes with few row tiles) the CTA partials go to the
 // workspace and the last CTA of a row group to arrive (an atomic counter; no
-// CTA ever waits on another) adds them in split order, scales and rounds.
+// CTA waits on another) adds them in split order.  Every sum therefore has a
+// fixed order that depends only on the plan.
 // ---------------------------------------------------------------------------
 struct Plan {
     int nt;          // 8-token groups (tensor-core N = 8): 1, 2, 4 or 8
     int r;           // row tiles per warp
-    int d;           // prefetch depth in blocks
-    int ctas_per_sm; // occupancy the kernel is built for
+    int dw;          // weight prefetch depth in K blocks (FP8 instance; see depth_w)
+    int wk;          // warps of a tile group along K: 1, 2, 4 or 8
+    int ctas_per_sm; // occupancy the kernel instance is built for
     int64_t rt;      // row tiles of the plane
     int64_t kb;      // K blocks of the plane
     int row_groups;
     int splits;
-    int kbs_max;     // most K blocks in one split
+    int kbs_max;     // most K blocks one warp streams
     int grid;
-    int smem;        // dynamic shared memory bytes
-    int x_stride;    // bytes between token rows of the staged x
+    int smem;        // dynamic shared memory bytes (the K-part reduction)
     size_t ws_counters; // bytes of the counter head of the workspace
     size_t ws_bytes;    // total workspace bytes (0 when splits == 1)
 };
 
 W8_HD int nt_for_m(int m) { return m <= 8 ? 1 : m <= 16 ? 2 : m <= 32 ? 4 : 8; }
-W8_HD int r_for_nt(int nt) { return nt <= 2 ? 1 : 2; }
-W8_HD int d_for_nt(int nt) { return nt <= 2 ? 8 : 4; }
-W8_HD int ctas_per_sm_for_nt(int nt) { return nt <= 2 ? 2 : 1; }
 
-// Token rows of the staged x are kbs*64 bytes long; the stride is padded so
-// that it is 64 modulo 128 and the lanes' 16-byte reads hit distinct banks.
-W8_HD int x_stride_bytes(int kbs) { return kbs * 64 + ((kbs & 1) ? 0 : 64); }
+// The kernel instances.  For each token-group count NT and row tiles per
+// warp R: the weight ring depth DW and the activation ring depth DX (in K
+// blocks; DX divides DW) and the CTAs per SM the instance is built for.  The
+// depths are the only dtype-dependent choice -- a bf16 block takes twice the
+// registers of an FP8 block, so its ring holds half the blocks and the same
+// bytes -- and no depth changes a summation order.  Activations come from
+// L2/L1, so their ring can be shallower than the HBM weight ring.
+W8_HD constexpr int depth_w(int nt, int r, bool fp8)
+{
+    return fp8 ? (nt == 1 ? (r == 1 ? 16 : 8) : nt == 2 ? 6 : nt == 4 ? 8 : 6)
+               : (nt == 1 ? (r == 1 ? 8 : 4) : 4);
+}
+W8_HD constexpr int depth_x(int nt, int r, bool fp8)
+{
+    return fp8 ? (nt == 1 ? (r == 1 ? 8 : 4) : nt == 2 ? 3 : nt == 4 ? 4 : 2)
+               : (nt == 1 ? (r == 1 ? 4 : 2) : 2);
+}
+W8_HD constexpr int ctas_per_sm_for_nt(int nt) { return nt <= 2 ? 2 : 1; }
 
+inline int64_t plan_ctas(int64_t rt, int r, int wk, int splits)
+{
+    const int64_t tiles_per_cta = int64_t(kWarps / wk) * r;
+    return ceil_div(rt, tiles_per_cta) * splits;
+}
+
+// Choose (wk, R): the fewest waves, then the most weight bytes in flight,
+// then R = 2 (activations reused over two tiles), then the longest K parts.
+// Every warp keeps at least kMinBlocks K blocks when K allows it.  K is split
+// across CTAs only for planes whose row tiles leave most SMs idle.
 inline Plan make_plan(int64_t n, int64_t k, int m, int sm_count)
 {
     Plan p{};
     p.nt = nt_for_m(m);
-    p.r = r_for_nt(p.nt);
-    p.d = d_for_nt(p.nt);
     p.ctas_per_sm = ctas_per_sm_for_nt(p.nt);
     p.rt = ceil_div(n, kTileN);
     p.kb = ceil_div(k, kTileK);
-    const int64_t tiles_per_cta = int64_t(kWarps) * p.r;
-    p.row_groups = int(ceil_div(p.rt, tiles_per_cta));
+    const int sms = sm_count > 0 ? sm_count : 1;
+    const int64_t slots = int64_t(sms) * p.ctas_per_sm;
+    const int64_t kMinBlocks = 8;
 
-    const int smem_budget = (p.ctas_per_sm == 2 ? 100 : 200) * 1024;
-    // largest split whose staged x fits the budget
-    int kbs_cap = 1;
-    while (kbs_cap < p.kb && p.nt * 8 * x_stride_bytes(kbs_cap + 1) <= smem_budget)
-        ++kbs_cap;
-    const int64_t s_min = ceil_div(p.kb, kbs_cap);
-
-    const int64_t target = int64_t(sm_count > 0 ? sm_count : 1) * p.ctas_per_sm;
-    int64_t s = (target + p.row_groups / 2) / p.row_groups; // round(target / row_groups)
-    const int64_t s_cap = p.kb / 4 > 1 ? p.kb / 4 : 1;     // keep >= 4 blocks per split
-    if (s > s_cap) s = s_cap;
-    if (s < 1) s = 1;
-    if (s < s_min) s = s_min;
-    if (s > p.kb) s = p.kb;
-    p.splits = int(s);
-    p.kbs_max = int(ceil_div(p.kb, s));
+    bool have = false;
+    int64_t best_waves = 0, best_inflight = 0, best_bpw = 0;
+    int best_r = 1, best_wk = 1;
+    for (int r = (p.nt == 1 ? 1 : 2); r <= 2; ++r) {
+        for (int wk = 8; wk >= 1; wk /= 2) {
+            const int64_t bpw = p.kb / wk;
+            if (wk > 1 && bpw < kMinBlocks)
+                continue;
+            const int64_t ctas = plan_ctas(p.rt, r, wk, 1);
+            const int64_t waves = ceil_div(ctas, slots);
+            const int64_t resident = ctas < slots ? ctas : slots;
+            const int64_t per_warp = int64_t(depth_w(p.nt, r, true)) * r * kRunFp8;
+            const int64_t inflight = resident * kWarps * (bpw < depth_w(p.nt, r, true)
+                                                              ? bpw * r * kRunFp8 : per_warp);
+            bool better;
+            if (!have)
+                better = true;
+            else if (waves != best_waves)
+                better = waves < best_waves;
+            else if (inflight != best_inflight)
+                better = inflight > best_inflight;
+            else if (r != best_r)
+                better = r > best_r;
+            else
+                better = bpw > best_bpw;
+            if (better) {
+                have = true;
+                best_waves = waves;
+                best_inflight = inflight;
+                best_bpw = bpw;
+                best_r = r;
+                best_wk = wk;
+            }
+        }
+    }
+    p.r = best_r;
+    p.wk = best_wk;
+    p.dw = depth_w(p.nt, p.r, true);
+    int splits = 1;
+    while (plan_ctas(p.rt, p.r, p.wk, splits) * 2 <= sms &&
+           p.kb / (int64_t(p.wk) * splits * 2) >= 4)
+        splits *= 2;
+    p.splits = splits;
+    p.row_groups = int(ceil_div(p.rt, int64_t(kWarps / p.wk) * p.r));
     p.grid = p.row_groups * p.splits;
-    p.x_stride = x_stride_bytes(p.kbs_max);
-    p.smem = p.nt * 8 * p.x_stride;
+    p.kbs_max = int(ceil_div(ceil_div(p.kb, p.splits), p.wk));
+    p.smem = kWarps * p.r * p.nt * 4 * 32 * int(sizeof(float));
     if (p.splits > 1) {
         p.ws_counters = align256(size_t(p.row_groups) * sizeof(int));
         p.ws_bytes = p.ws_counters + align256(size_t(p.splits) * size_t(p.rt) * kTileN *

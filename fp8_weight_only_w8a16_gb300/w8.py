@@ -57,8 +57,9 @@ class PlaneInfo(ctypes.Structure):
 class PlanInfo(ctypes.Structure):
     _fields_ = [("grid", ctypes.c_int32), ("block", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int32), ("n_tiles", ctypes.c_int32),
-                ("row_tiles_per_warp", ctypes.c_int32), ("row_groups", ctypes.c_int32),
-                ("splits", ctypes.c_int32), ("k_blocks_per_split_max", ctypes.c_int32),
+                ("row_tiles_per_warp", ctypes.c_int32), ("warps_k", ctypes.c_int32),
+                ("depth", ctypes.c_int32), ("row_groups", ctypes.c_int32),
+                ("splits", ctypes.c_int32), ("k_blocks_per_warp_max", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_size_t)]
 
 

@@ -25,8 +25,12 @@
  *    before anything is enqueued; nothing traps on the device and no function
  *    exits the process.  A failed launch or CUDA call returns W8_ERR_CUDA.
  *  - w8_gemv and bf16_gemv are asynchronous on the caller's stream, never
- *    synchronise and launch exactly one kernel.  w8_bind enqueues its repack
- *    kernels on the caller's stream and does not synchronise either.
+ *    synchronise and launch exactly one kernel, with programmatic dependent
+ *    launch: the kernel may begin streaming weights while the previous kernel
+ *    of the stream drains, and reads activations and writes outputs only
+ *    after that kernel has completed.  w8_bind runs its repack kernels on the
+ *    caller's stream and synchronises that stream before it returns (load
+ *    time; it must not be captured in a CUDA graph).
  *  - A stream argument is a cudaStream_t (NULL is the legacy default stream).
  */
 #ifndef W8_H
@@ -58,8 +62,8 @@ typedef enum {
     W8_ERR_SCALE = 7,     /* an FP8 plane without row scales, or a bf16 plane with them */
     W8_ERR_LAYOUT = 8,    /* unknown source layout */
     W8_ERR_CAPACITY = 9,  /* packed buffer or workspace smaller than required */
-    W8_ERR_ALIGN = 10,    /* packed buffer or workspace not 256-byte aligned, or x / y
-                             not 2-byte aligned */
+    W8_ERR_ALIGN = 10,    /* packed buffer or workspace not 256-byte aligned, x not 16-byte
+                             aligned or ldx not a multiple of 8, or y not 2-byte aligned */
     W8_ERR_PLANE = 11,    /* plane index outside the build */
     W8_ERR_DEVICE = 12,   /* the current device is not the one the build was bound on */
     W8_ERR_CUDA = 13      /* a CUDA runtime call or kernel launch failed */
@@ -120,9 +124,13 @@ typedef struct {
     int32_t smem_bytes;      /* dynamic shared memory per CTA */
     int32_t n_tiles;         /* 8-token groups of the tensor-core N dimension */
     int32_t row_tiles_per_warp;
+    int32_t warps_k;         /* warps that share one row tile, each on its own K part */
+    int32_t depth;           /* K blocks each warp keeps in flight (w8_plan_shape gives
+                                the FP8 depth; bf16 rings hold fewer, larger blocks;
+                                the depth never changes a summation order) */
     int32_t row_groups;      /* CTAs along N */
     int32_t splits;          /* CTAs along K; > 1 means a workspace is needed */
-    int32_t k_blocks_per_split_max;
+    int32_t k_blocks_per_warp_max; /* most 32-column K blocks one warp streams */
     size_t workspace_bytes;  /* 0 when splits == 1 */
 } w8_plan;
 
@@ -148,8 +156,9 @@ w8_status w8_packed_bytes(const w8_plane_desc *d, int n_planes, size_t *bytes);
  * W8_LAYOUT_MMA_16x32 and, for FP8, a copy of the row scales.  An FP8 row
  * holding a NaN code (0x7F / 0xFF) gets a NaN scale in that copy, so its
  * outputs are NaN, as the definition gives.  On W8_OK *out is a new handle
- * for the device current at the call; the source planes and scales may be
- * freed once the stream has run the repack.  dst must outlive the handle. */
+ * for the device current at the call, the repack has completed (the stream
+ * is synchronised) and the source planes and scales may be freed.  dst must
+ * outlive the handle and must not be written while gemv calls may read it. */
 w8_status w8_bind(const w8_plane_desc *d, int n_planes, void *dst, size_t dst_bytes,
                   w8_stream s, w8_build **out);
 
@@ -181,8 +190,8 @@ w8_status w8_workspace_bytes(const w8_build *b, int plane, int m, size_t *bytes)
 
 /* The FP8 (w8a16) GEMV on an E4M3FN build:
  *   y[i*ldy + n] = bf16(scale[n] * sum_k W[n,k] * x[i*ldx + k]),  0 <= i < m, 0 <= n < N.
- * x: device bf16 [m][ldx], ldx >= K, 2-byte aligned (rows that are 16-byte
- *    aligned with ldx % 8 == 0 are read with 16-byte loads);
+ * x: device bf16 [m][ldx], ldx >= K, ldx % 8 == 0, 16-byte aligned (every
+ *    row is read with 16-byte loads; columns K..ldx-1 are never read);
  * y: device bf16 [m][ldy], ldy >= N, written for n < N only;
  * m: decode tokens, 0..64 (0 is a no-op);
  * workspace / workspace_bytes: see w8_workspace_bytes (may be NULL / 0 when

@@ -26,8 +26,23 @@ def from_dev(t: torch.Tensor) -> np.ndarray:
     return a
 
 
+def padded(plane: synth.Plane) -> synth.Plane:
+    """The same plane with its rows padded with zeros to a multiple of 16 bytes
+    (bind refuses unpadded planes; the pad columns lie past K)."""
+    elt = plane.w.itemsize
+    step = 16 // elt
+    if plane.ldw % step == 0:
+        return plane
+    ldw = -(-plane.ldw // step) * step
+    w = np.zeros((plane.n, ldw), dtype=plane.w.dtype)
+    w[:, :plane.ldw] = plane.w
+    return synth.Plane(plane.dtype, plane.n, plane.k, ldw, w, plane.scale)
+
+
 def bind_plane(w8, plane: synth.Plane):
-    """Bind one source plane (as generated) and return (build, source tensors)."""
+    """Bind one source plane (rows padded to 16 bytes if needed) and return
+    (build, source tensors)."""
+    plane = padded(plane)
     w_d = to_dev(plane.w)
     s_d = to_dev(plane.scale) if plane.scale is not None else None
     p = w8.Plane.from_tensor(w_d, s_d, k=plane.k,
@@ -41,7 +56,15 @@ def run_gemv(w8, build, plane_idx: int, x: np.ndarray, n: int, ldy: int | None =
     """y [m, n] (uint16) = the library's GEMV of x (uint16 [m, >=k])."""
     m = x.shape[0] if x_dev is None else x_dev.shape[0]
     ldy = n if ldy is None else ldy
-    xd = to_dev(x) if x_dev is None else x_dev
+    if x_dev is None:
+        # rows padded to 8 elements (the ABI reads x with 16-byte loads)
+        k = x.shape[1]
+        ldx = -(-k // 8) * 8
+        xp = torch.zeros((m, ldx), dtype=torch.int16, device=dev())
+        xp[:, :k] = to_dev(x)
+        xd = xp[:, :k]
+    else:
+        xd = x_dev
     y = torch.zeros((m, ldy), dtype=torch.int16, device=dev())
     if ws is None:
         ws = build.new_workspace()

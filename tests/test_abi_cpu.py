@@ -156,21 +156,34 @@ def test_plan_invariants(n, k, m):
     kb = -(-k // 32)
     rt = -(-n // 16)
     assert p.grid == p.row_groups * p.splits
+    assert p.warps_k in (1, 2, 4, 8) and p.depth >= 1
     assert 1 <= p.splits <= kb
-    assert p.k_blocks_per_split_max == -(-kb // p.splits)
-    assert p.row_groups * 8 * p.row_tiles_per_warp >= rt
-    assert (p.row_groups - 1) * 8 * p.row_tiles_per_warp < rt
+    tiles_per_cta = (8 // p.warps_k) * p.row_tiles_per_warp
+    assert p.row_groups * tiles_per_cta >= rt > (p.row_groups - 1) * tiles_per_cta
     assert p.n_tiles * 8 >= m and (p.n_tiles == 1 or p.n_tiles * 4 < m)
-    limit = (100 if p.n_tiles <= 2 else 200) * 1024
-    assert p.smem_bytes <= limit
+    assert p.smem_bytes == 8 * p.row_tiles_per_warp * p.n_tiles * 128 * 4 <= 64 * 1024
     assert (p.workspace_bytes == 0) == (p.splits == 1)
     if p.splits > 1:
         assert p.workspace_bytes >= p.splits * rt * 16 * m * 4
-    # splits tile the K blocks exactly: floor(s * kb / S) boundaries
-    bounds = [(s * kb) // p.splits for s in range(p.splits + 1)]
-    assert bounds[0] == 0 and bounds[-1] == kb
-    assert all(b1 - b0 >= 1 for b0, b1 in zip(bounds, bounds[1:]))
-    assert max(b1 - b0 for b0, b1 in zip(bounds, bounds[1:])) == p.k_blocks_per_split_max
+    # CTA splits and warp K parts tile the K blocks exactly (floor boundaries);
+    # every warp gets at least one block unless K is shorter than the warps
+    parts = []
+    for s in range(p.splits):
+        c0, c1 = (s * kb) // p.splits, ((s + 1) * kb) // p.splits
+        for q in range(p.warps_k):
+            parts.append((c0 + (q * (c1 - c0)) // p.warps_k,
+                          c0 + ((q + 1) * (c1 - c0)) // p.warps_k))
+    assert parts[0][0] == 0 and parts[-1][1] == kb
+    assert all(a1 == b0 for (_, a1), (b0, _) in zip(parts, parts[1:]))
+    assert max(b - a for a, b in parts) == p.k_blocks_per_warp_max
+    if kb >= p.warps_k * p.splits:
+        assert min(b - a for a, b in parts) >= 1
+
+
+def test_plan_does_not_depend_on_anything_but_shape():
+    a = w8.plan_shape(2624, 6144, 4, 152)
+    b = w8.plan_shape(2624, 6144, 4, 152)
+    assert bytes(a) == bytes(b)
 
 
 def test_plan_refuses_bad_shapes():
