@@ -20,13 +20,6 @@
 #include "w8.h"
 #include "w8_internal.h"
 
-struct w8_build {
-    int device;
-    int sm_count;
-    int32_t dtype;
-    std::vector<w8_plane_info> planes;
-};
-
 namespace {
 
 constexpr int64_t kMaxDim = int64_t(1) << 30;
@@ -149,6 +142,8 @@ const char *w8_status_str(w8_status s)
     case W8_ERR_PLANE: return "plane index outside the build";
     case W8_ERR_DEVICE: return "current device is not the device the build was bound on";
     case W8_ERR_CUDA: return "CUDA runtime error";
+    case W8_ERR_SCRATCH: return "w8_gemv_noalloc: the call needs more scratch than the library's "
+                                "fixed W8_NOALLOC_SCRATCH_BYTES";
     }
     return "unknown status";
 }

@@ -4,7 +4,18 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <vector>
+
+#include "w8.h"
 #include "w8_layout.h"
+
+// The library-owned host handle behind the opaque w8_build of include/w8.h.
+struct w8_build {
+    int device;
+    int sm_count;
+    int32_t dtype;
+    std::vector<w8_plane_info> planes;
+};
 
 namespace w8 {
 

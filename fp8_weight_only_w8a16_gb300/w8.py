@@ -30,7 +30,7 @@ STATUS = {
     0: "W8_OK", 1: "W8_ERR_NULL", 2: "W8_ERR_DTYPE", 3: "W8_ERR_UNPADDED", 4: "W8_ERR_BIAS",
     5: "W8_ERR_MIXED", 6: "W8_ERR_SHAPE", 7: "W8_ERR_SCALE", 8: "W8_ERR_LAYOUT",
     9: "W8_ERR_CAPACITY", 10: "W8_ERR_ALIGN", 11: "W8_ERR_PLANE", 12: "W8_ERR_DEVICE",
-    13: "W8_ERR_CUDA",
+    13: "W8_ERR_CUDA", 14: "W8_ERR_SCRATCH",
 }
 
 
@@ -97,6 +97,8 @@ def _load():
         f = getattr(lib, name)
         f.argtypes = [vp, i32, vp, i64, i32, vp, i64, vp, sz, vp]
         f.restype = st
+    lib.w8_gemv_noalloc.argtypes = [vp, i32, vp, i64, i32, vp, i64, vp]
+    lib.w8_gemv_noalloc.restype = st
     lib.w8_packed_offset.argtypes = [i32, i64, i64, i64]
     lib.w8_packed_offset.restype = i64
     return lib
@@ -107,7 +109,7 @@ lib = _load()
 # every symbol include/w8.h declares
 EXPORTS = ("w8_status_str", "w8_abi_version", "w8_validate", "w8_packed_bytes", "w8_bind",
            "w8_release", "w8_build_planes", "w8_build_info", "w8_plan_info", "w8_plan_shape",
-           "w8_workspace_bytes", "w8_gemv", "bf16_gemv", "w8_packed_offset")
+           "w8_workspace_bytes", "w8_gemv", "bf16_gemv", "w8_gemv_noalloc", "w8_packed_offset")
 
 
 def _check(status: int):
@@ -276,6 +278,18 @@ def plan_shape(n: int, k: int, m: int, sm_count: int) -> PlanInfo:
     out = PlanInfo()
     _check(lib.w8_plan_shape(n, k, m, sm_count, ctypes.byref(out)))
     return out
+
+
+def w8_gemv_noalloc(build: Build, plane: int, x: torch.Tensor, y: torch.Tensor,
+                    m: int | None = None, stream=None):
+    """w8_gemv without a workspace: scratch from the library's fixed array."""
+    assert x.dim() == 2 and x.stride(1) == 1 and x.element_size() == 2
+    assert y.dim() == 2 and y.stride(1) == 1 and y.element_size() == 2
+    m = x.shape[0] if m is None else m
+    _check(lib.w8_gemv_noalloc(build.handle, plane, ctypes.c_void_p(x.data_ptr()), x.stride(0),
+                               m, ctypes.c_void_p(y.data_ptr()), y.stride(0),
+                               _stream_ptr(stream)))
+    return y
 
 
 def packed_offset(dtype: int, k_blocks: int, row: int, col: int) -> int:

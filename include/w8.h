@@ -66,7 +66,9 @@ typedef enum {
                              aligned or ldx not a multiple of 8, or y not 2-byte aligned */
     W8_ERR_PLANE = 11,    /* plane index outside the build */
     W8_ERR_DEVICE = 12,   /* the current device is not the one the build was bound on */
-    W8_ERR_CUDA = 13      /* a CUDA runtime call or kernel launch failed */
+    W8_ERR_CUDA = 13,     /* a CUDA runtime call or kernel launch failed */
+    W8_ERR_SCRATCH = 14   /* w8_gemv_noalloc: the call needs more scratch than the
+                             library's fixed W8_NOALLOC_SCRATCH_BYTES */
 } w8_status;
 
 /* Source element types.  Only E4M3FN and BF16 are readable (PR page, Changes
@@ -209,6 +211,33 @@ w8_status w8_gemv(const w8_build *b, int plane, const uint16_t *x, int64_t ldx, 
 w8_status bf16_gemv(const w8_build *b, int plane, const uint16_t *x, int64_t ldx, int m,
                     uint16_t *y, int64_t ldy, void *workspace, size_t workspace_bytes,
                     w8_stream s);
+
+/* The FP8 GEMV for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart of this entry point; it serves callers that
+ * cannot call cudaMalloc where they run the GEMV (a host callback, an
+ * allocator or memory-pool hook, a framework that forbids device allocations
+ * while it records or replays a step) and so cannot provide the workspace
+ * w8_gemv asks for when a plan splits K across CTAs.
+ *
+ * Same arguments and result as w8_gemv without the workspace: the scratch
+ * comes from a fixed array of W8_NOALLOC_SCRATCH_BYTES (1 MiB) inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits.  A call whose plan needs more (w8_plan_info's workspace_bytes)
+ * returns W8_ERR_SCRATCH before any launch.  It allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * The first call on each device that needs the scratch sets it up: with that
+ * device current it looks up the array's device address and zeroes the array,
+ * which synchronises the device, so that first call must come before any
+ * stream capture.  Every call leaves the array's counters at zero again.  All
+ * calls on a device share the one array, so calls that could overlap on the
+ * GPU (different streams without ordering between them) race and must not be
+ * made; calls on one stream are fine.  Returns W8_ERR_DTYPE on a bf16 build.
+ * One kernel launch on s. */
+#define W8_NOALLOC_SCRATCH_BYTES (1u << 20)
+w8_status w8_gemv_noalloc(const w8_build *b, int plane, const uint16_t *x, int64_t ldx, int m,
+                          uint16_t *y, int64_t ldy, w8_stream s);
 
 /* Host-side address map of W8_LAYOUT_MMA_16x32: byte offset, inside one
  * plane's packed weights, of element (row, col) of a plane with k_blocks

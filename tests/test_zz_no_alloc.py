@@ -1,0 +1,94 @@
+"""w8_gemv_noalloc: the FP8 GEMV for callers that cannot allocate device memory.
+
+Some callers cannot call cudaMalloc where they run the GEMV (a host callback,
+an allocator hook, a framework that forbids device allocations while it
+records or replays a step), so they cannot hand w8_gemv the workspace it asks
+for when a plan splits K across CTAs.  w8_gemv_noalloc takes that scratch from
+a fixed array inside the library instead.  These tests call it through the C
+ABI and check, on two calls in a row, that it gives exactly what w8_gemv gives
+with a caller workspace, and that both are within the parity tolerance of the
+oracle's fp64 recompute; and that calls needing more than the fixed array, or
+made on a bf16 build, are refused before any launch.
+
+This file is collected last so that a run stopping at its first failure has
+already run every other test; it also passes alone in a fresh process (the
+first call on the device sets the array up).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_weight_only_w8a16_gb300 import synth
+
+from .gpu_util import bind_plane, dev, from_dev, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def w8():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from fp8_weight_only_w8a16_gb300 import w8 as lib
+
+    return lib
+
+
+# (n, k, m): two plans that split K across CTAs (and so use the scratch), one
+# small and one large plane whose plans do not
+CASES = [(128, 6144, 16), (32, 6144, 64), (40, 6144, 5), (2624, 6144, 4)]
+
+
+@pytest.mark.parametrize("n,k,m", CASES)
+def test_noalloc_equals_gemv_with_workspace(w8, n, k, m):
+    rng = np.random.default_rng(n + k + m)
+    plane = synth.weight_plane(rng, n, k)
+    x = synth.activations(rng, k, m)
+    b, _src = bind_plane(w8, plane)
+    needs_scratch = b.plan(0, m).splits > 1
+    if (n, k) in ((128, 6144), (32, 6144)):
+        assert needs_scratch
+    assert b.workspace_bytes(0, m) <= (1 << 20)
+
+    xd = to_dev(x)
+    y_ref = torch.zeros((m, n), dtype=torch.int16, device=dev())
+    w8.w8_gemv(b, 0, xd, y_ref, b.new_workspace(0, m))
+    torch.cuda.synchronize()
+    ref = from_dev(y_ref)
+    y64, mag = oracle.gemv_f64(plane.w, oracle.DT_E4M3FN, plane.scale, x, k=k)
+
+    for _ in range(2):  # two calls in a row share the library's scratch
+        y = torch.full((m, n), 0x7FC1, dtype=torch.int16, device=dev())
+        w8.w8_gemv_noalloc(b, 0, xd, y)
+        torch.cuda.synchronize()
+        got = from_dev(y)
+        assert np.array_equal(got, ref)
+        ok, worst = oracle.within_tolerance(got, y64, mag)
+        assert ok, worst
+
+
+def test_noalloc_refuses_what_it_cannot_serve(w8):
+    # a plan whose split partials exceed the fixed scratch
+    n, k, m = 1024, 4096, 64
+    p = w8.plan_shape(n, k, m, torch.cuda.get_device_properties(dev()).multi_processor_count)
+    rng = np.random.default_rng(7)
+    plane = synth.weight_plane(rng, n, k)
+    b, _src = bind_plane(w8, plane)
+    x = to_dev(synth.activations(rng, k, m))
+    y = torch.zeros((m, n), dtype=torch.int16, device=dev())
+    if p.workspace_bytes > (1 << 20):
+        with pytest.raises(w8.W8Error) as e:
+            w8.w8_gemv_noalloc(b, 0, x, y)
+        assert e.value.name == "W8_ERR_SCRATCH"
+        torch.cuda.synchronize()
+        assert torch.all(y == 0)
+    # a bf16 build is refused
+    bp = synth.weight_plane(rng, 64, 256, "bf16")
+    b16, _src16 = bind_plane(w8, bp)
+    with pytest.raises(w8.W8Error) as e:
+        w8.w8_gemv_noalloc(b16, 0, to_dev(synth.activations(rng, 256, 2)),
+                           torch.zeros((2, 64), dtype=torch.int16, device=dev()))
+    assert e.value.name == "W8_ERR_DTYPE"
