@@ -363,8 +363,9 @@ def run_ours(args):
 
     # per-batch microseconds and the kernel roofline
     per_m = {}
+    reps = max(5, min(200, args.steps // 50))
     for m in ms:
-        us = b.per_call_us(m)
+        us = b.per_call_us(m, reps=reps)
         per_m[m] = {"us_per_call": round(us, 3),
                     "gbs": round(proj.algorithmic_bytes(m) / (us * 1e-6) / 1e9, 1),
                     "pct_of_8tbs": round(100 * proj.algorithmic_bytes(m) / (us * 1e-6) / 1e9
@@ -514,6 +515,36 @@ def run_sweep(args):
         out.close()
 
 
+def run_one(args):
+    """Bind one workload and run its GEMV a few times, flushing L2 between
+    calls (the small case the ncu captures profile)."""
+    import torch
+    from fp8_weight_only_w8a16_gb300 import w8
+
+    proj = workloads.BY_NAME[args.one]
+    m = args.m
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    plane, x_all = synth.workload(proj.n, proj.k, proj.dtype, seed=0, ldw=proj.ldw)
+    w_d = torch.from_numpy(plane.w).to(device)
+    s_d = torch.from_numpy(plane.scale).to(device) if plane.scale is not None else None
+    dt = w8.DT_E4M3FN if proj.dtype == "e4m3fn" else w8.DT_BF16
+    b = w8.bind([w8.Plane.from_tensor(w_d, s_d, k=proj.k, dtype=dt)])
+    ws = b.new_workspace()
+    x = torch.from_numpy(np.ascontiguousarray(x_all[:m]).view(np.int16)).to(device)
+    y = torch.zeros((m, proj.n), dtype=torch.int16, device=device)
+    fn = w8.w8_gemv if dt == w8.DT_E4M3FN else w8.bf16_gemv
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # 2 x L2
+    for _ in range(args.calls):
+        flush.zero_()
+        fn(b, 0, x, y, ws)
+    torch.cuda.synchronize()
+    p = b.plan(0, m)
+    print(json.dumps({"workload": proj.name, "m": m, "calls": args.calls, "grid": p.grid,
+                      "warps_k": p.warps_k, "row_tiles_per_warp": p.row_tiles_per_warp,
+                      "splits": p.splits, "alg_bytes": proj.algorithmic_bytes(m)}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -527,9 +558,14 @@ def main():
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--only", default="")
     ap.add_argument("--out", default="")
+    ap.add_argument("--one", default="", help="run one workload's GEMV --calls times")
+    ap.add_argument("--m", type=int, default=1)
+    ap.add_argument("--calls", type=int, default=6)
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.one:
+        run_one(args)
     elif args.sweep:
         run_sweep(args)
     else:

@@ -304,7 +304,10 @@ w8_status w8_plan_info(const w8_build *b, int plane, int m, w8_plan *out)
     const w8_plane_info &p = b->planes[size_t(plane)];
     const w8_status st = w8_plan_shape(p.n, p.k, m, b->sm_count, out);
     if (st == W8_OK && p.dtype == W8_DT_BF16)
-        out->depth = w8::depth_w(out->n_tiles, out->row_tiles_per_warp, false);
+    {
+        const w8::Plan pl = w8::make_plan(p.n, p.k, m, b->sm_count);
+        out->depth = w8::depth_w(pl.nt, pl.r, false, pl.occ);
+    }
     return st;
 }
 

@@ -444,24 +444,27 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
 }
 
 // ---------------------------------------------------------------------------
-// instance table: one kernel per (dtype, NT, R) with the depths of w8_layout.h
+// instance table: one kernel per (dtype, NT, R, occupancy) with the depths of
+// w8_layout.h
 // ---------------------------------------------------------------------------
-template <bool kFp8, int NT, int R>
+template <bool kFp8, int NT, int R, int OCC>
 void *inst()
 {
-    return reinterpret_cast<void *>(
-        &gemv_kernel<kFp8, NT, R, depth_w(NT, R, kFp8), depth_x(NT, R, kFp8),
-                     ctas_per_sm_for_nt(NT)>);
+    return reinterpret_cast<void *>(&gemv_kernel<kFp8, NT, R, depth_w(NT, R, kFp8, OCC),
+                                                 depth_x(NT, R, kFp8, OCC), OCC>);
 }
 
 template <bool kFp8>
-void *pick(int nt, int r)
+void *pick(int nt, int r, int occ)
 {
     switch (nt) {
-    case 1: return r == 1 ? inst<kFp8, 1, 1>() : inst<kFp8, 1, 2>();
-    case 2: return inst<kFp8, 2, 2>();
-    case 4: return inst<kFp8, 4, 2>();
-    default: return inst<kFp8, 8, 2>();
+    case 1:
+        if (occ == 3)
+            return r == 1 ? inst<kFp8, 1, 1, 3>() : inst<kFp8, 1, 2, 3>();
+        return r == 1 ? inst<kFp8, 1, 1, 2>() : inst<kFp8, 1, 2, 2>();
+    case 2: return inst<kFp8, 2, 2, 2>();
+    case 4: return inst<kFp8, 4, 2, 1>();
+    default: return inst<kFp8, 8, 2, 1>();
     }
 }
 
@@ -470,11 +473,12 @@ void *pick(int nt, int r)
 cudaError_t prepare_gemv_kernels()
 {
     // the K-part reduction buffer: 8 warps x R x NT x 128 floats, at most 64 KB
-    const int nts[5] = {1, 1, 2, 4, 8};
-    const int rs[5] = {1, 2, 2, 2, 2};
-    for (int i = 0; i < 5; ++i) {
+    const int nts[7] = {1, 1, 1, 1, 2, 4, 8};
+    const int rs[7] = {1, 2, 1, 2, 2, 2, 2};
+    const int occs[7] = {2, 2, 3, 3, 2, 1, 1};
+    for (int i = 0; i < 7; ++i) {
         for (int f = 0; f < 2; ++f) {
-            void *fn = f ? pick<true>(nts[i], rs[i]) : pick<false>(nts[i], rs[i]);
+            void *fn = f ? pick<true>(nts[i], rs[i], occs[i]) : pick<false>(nts[i], rs[i], occs[i]);
             cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  64 * 1024);
             if (e != cudaSuccess)
@@ -486,7 +490,7 @@ cudaError_t prepare_gemv_kernels()
 
 cudaError_t launch_gemv(bool fp8, const Plan &plan, const GemvArgs &a, cudaStream_t s)
 {
-    void *fn = fp8 ? pick<true>(plan.nt, plan.r) : pick<false>(plan.nt, plan.r);
+    void *fn = fp8 ? pick<true>(plan.nt, plan.r, plan.occ) : pick<false>(plan.nt, plan.r, plan.occ);
     void *args[] = {const_cast<GemvArgs *>(&a)};
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(unsigned(plan.grid));

@@ -91,8 +91,8 @@ struct Plan {
     int nt;          // 8-token groups (tensor-core N = 8): 1, 2, 4 or 8
     int r;           // row tiles per warp
     int dw;          // weight prefetch depth in K blocks (FP8 instance; see depth_w)
+    int occ;         // CTAs per SM of the chosen kernel instance
     int wk;          // warps of a tile group along K: 1, 2, 4 or 8
-    int ctas_per_sm; // occupancy the kernel instance is built for
     int64_t rt;      // row tiles of the plane
     int64_t kb;      // K blocks of the plane
     int row_groups;
@@ -106,24 +106,30 @@ struct Plan {
 
 W8_HD int nt_for_m(int m) { return m <= 8 ? 1 : m <= 16 ? 2 : m <= 32 ? 4 : 8; }
 
-// The kernel instances.  For each token-group count NT and row tiles per
-// warp R: the weight ring depth DW and the activation ring depth DX (in K
-// blocks; DX divides DW) and the CTAs per SM the instance is built for.  The
+// The kernel instances.  For each token-group count NT, row tiles per warp R
+// and occupancy OCC (CTAs per SM the instance is built for): the weight ring
+// depth DW and the activation ring depth DX in K blocks (DX divides DW).  For
+// NT = 1 there are two families: OCC = 2 with deep rings (the most bytes in
+// flight per warp) and OCC = 3 with shallow rings (more warps per SM).  The
 // depths are the only dtype-dependent choice -- a bf16 block takes twice the
 // registers of an FP8 block, so its ring holds half the blocks and the same
 // bytes -- and no depth changes a summation order.  Activations come from
 // L2/L1, so their ring can be shallower than the HBM weight ring.
-W8_HD constexpr int depth_w(int nt, int r, bool fp8)
+W8_HD constexpr int depth_w(int nt, int r, bool fp8, int occ)
 {
-    return fp8 ? (nt == 1 ? (r == 1 ? 16 : 8) : nt == 2 ? 6 : nt == 4 ? 8 : 6)
-               : (nt == 1 ? (r == 1 ? 8 : 4) : 4);
+    return nt == 1 ? (occ == 3 ? (fp8 ? (r == 1 ? 8 : 4) : (r == 1 ? 4 : 2))
+                               : (fp8 ? (r == 1 ? 16 : 8) : (r == 1 ? 8 : 4)))
+                   : (fp8 ? (nt == 2 ? 6 : nt == 4 ? 8 : 6) : (nt == 2 ? 2 : 4));
 }
-W8_HD constexpr int depth_x(int nt, int r, bool fp8)
+W8_HD constexpr int depth_x(int nt, int r, bool fp8, int occ)
 {
-    return fp8 ? (nt == 1 ? (r == 1 ? 8 : 4) : nt == 2 ? 3 : nt == 4 ? 4 : 2)
-               : (nt == 1 ? (r == 1 ? 4 : 2) : 2);
+    return nt == 1 ? (occ == 3 ? (fp8 ? (r == 1 ? 4 : 2) : 2)
+                               : (fp8 ? (r == 1 ? 8 : 4) : (r == 1 ? 4 : 2)))
+                   : (fp8 ? (nt == 2 ? 3 : nt == 4 ? 4 : 2) : 2);
 }
-W8_HD constexpr int ctas_per_sm_for_nt(int nt) { return nt <= 2 ? 2 : 1; }
+// occupancies available for a token-group count (highest last)
+W8_HD constexpr int occ_min(int nt) { return nt == 1 ? 2 : nt == 2 ? 2 : 1; }
+W8_HD constexpr int occ_max(int nt) { return nt == 1 ? 3 : nt == 2 ? 2 : 1; }
 
 inline int64_t plan_ctas(int64_t rt, int r, int wk, int splits)
 {
@@ -131,59 +137,68 @@ inline int64_t plan_ctas(int64_t rt, int r, int wk, int splits)
     return ceil_div(rt, tiles_per_cta) * splits;
 }
 
-// Choose (wk, R): the fewest waves, then the most weight bytes in flight,
-// then R = 2 (activations reused over two tiles), then the longest K parts.
-// Every warp keeps at least kMinBlocks K blocks when K allows it.  K is split
-// across CTAs only for planes whose row tiles leave most SMs idle.
+// Choose (occupancy, wk, R): the fewest waves, then the most weight bytes in
+// flight, then the most resident warps, then the higher occupancy, then R = 2
+// (activations reused over two tiles), then the longest K parts.  Every warp keeps at least kMinBlocks
+// K blocks when K allows it.  K is split across CTAs only for planes whose
+// row tiles leave most SMs idle.
 inline Plan make_plan(int64_t n, int64_t k, int m, int sm_count)
 {
     Plan p{};
     p.nt = nt_for_m(m);
-    p.ctas_per_sm = ctas_per_sm_for_nt(p.nt);
     p.rt = ceil_div(n, kTileN);
     p.kb = ceil_div(k, kTileK);
     const int sms = sm_count > 0 ? sm_count : 1;
-    const int64_t slots = int64_t(sms) * p.ctas_per_sm;
     const int64_t kMinBlocks = 8;
 
     bool have = false;
-    int64_t best_waves = 0, best_inflight = 0, best_bpw = 0;
-    int best_r = 1, best_wk = 1;
-    for (int r = (p.nt == 1 ? 1 : 2); r <= 2; ++r) {
-        for (int wk = 8; wk >= 1; wk /= 2) {
-            const int64_t bpw = p.kb / wk;
-            if (wk > 1 && bpw < kMinBlocks)
-                continue;
-            const int64_t ctas = plan_ctas(p.rt, r, wk, 1);
-            const int64_t waves = ceil_div(ctas, slots);
-            const int64_t resident = ctas < slots ? ctas : slots;
-            const int64_t per_warp = int64_t(depth_w(p.nt, r, true)) * r * kRunFp8;
-            const int64_t inflight = resident * kWarps * (bpw < depth_w(p.nt, r, true)
-                                                              ? bpw * r * kRunFp8 : per_warp);
-            bool better;
-            if (!have)
-                better = true;
-            else if (waves != best_waves)
-                better = waves < best_waves;
-            else if (inflight != best_inflight)
-                better = inflight > best_inflight;
-            else if (r != best_r)
-                better = r > best_r;
-            else
-                better = bpw > best_bpw;
-            if (better) {
-                have = true;
-                best_waves = waves;
-                best_inflight = inflight;
-                best_bpw = bpw;
-                best_r = r;
-                best_wk = wk;
+    int64_t best_waves = 0, best_inflight = 0, best_warps = 0, best_bpw = 0;
+    int best_r = 1, best_wk = 1, best_occ = 1;
+    for (int occ = occ_min(p.nt); occ <= occ_max(p.nt); ++occ) {
+        const int64_t slots = int64_t(sms) * occ;
+        for (int r = (p.nt == 1 ? 1 : 2); r <= 2; ++r) {
+            for (int wk = 8; wk >= 1; wk /= 2) {
+                const int64_t bpw = p.kb / wk;
+                if (wk > 1 && bpw < kMinBlocks)
+                    continue;
+                const int64_t ctas = plan_ctas(p.rt, r, wk, 1);
+                const int64_t waves = ceil_div(ctas, slots);
+                const int64_t resident = ctas < slots ? ctas : slots;
+                const int64_t dw = depth_w(p.nt, r, true, occ);
+                const int64_t inflight = resident * kWarps * (bpw < dw ? bpw : dw) * r * kRunFp8;
+                const int64_t warps = resident * kWarps;
+                bool better;
+                if (!have)
+                    better = true;
+                else if (waves != best_waves)
+                    better = waves < best_waves;
+                else if (inflight != best_inflight)
+                    better = inflight > best_inflight;
+                else if (warps != best_warps)
+                    better = warps > best_warps;
+                else if (occ != best_occ)
+                    better = occ > best_occ;
+                else if (r != best_r)
+                    better = r > best_r;
+                else
+                    better = bpw > best_bpw;
+                if (better) {
+                    have = true;
+                    best_waves = waves;
+                    best_inflight = inflight;
+                    best_warps = warps;
+                    best_bpw = bpw;
+                    best_r = r;
+                    best_wk = wk;
+                    best_occ = occ;
+                }
             }
         }
     }
     p.r = best_r;
     p.wk = best_wk;
-    p.dw = depth_w(p.nt, p.r, true);
+    p.occ = best_occ;
+    p.dw = depth_w(p.nt, p.r, true, p.occ);
     int splits = 1;
     while (plan_ctas(p.rt, p.r, p.wk, splits) * 2 <= sms &&
            p.kb / (int64_t(p.wk) * splits * 2) >= 4)

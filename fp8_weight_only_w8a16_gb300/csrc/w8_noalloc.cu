@@ -30,7 +30,7 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = size_t(1) << 20; // W8_NOALLOC_SCRATCH_BYTES
+constexpr size_t kScratchBytes = size_t(256) << 10; // W8_NOALLOC_SCRATCH_BYTES
 static_assert(kScratchBytes == W8_NOALLOC_SCRATCH_BYTES, "keep w8.h in step");
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];

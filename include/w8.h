@@ -221,7 +221,7 @@ w8_status bf16_gemv(const w8_build *b, int plane, const uint16_t *x, int64_t ldx
  * w8_gemv asks for when a plan splits K across CTAs.
  *
  * Same arguments and result as w8_gemv without the workspace: the scratch
- * comes from a fixed array of W8_NOALLOC_SCRATCH_BYTES (1 MiB) inside the
+ * comes from a fixed array of W8_NOALLOC_SCRATCH_BYTES (256 KiB) inside the
  * library, which every GPU that loads the library holds until the process
  * exits.  A call whose plan needs more (w8_plan_info's workspace_bytes)
  * returns W8_ERR_SCRATCH before any launch.  It allocates nothing: no
@@ -235,7 +235,7 @@ w8_status bf16_gemv(const w8_build *b, int plane, const uint16_t *x, int64_t ldx
  * GPU (different streams without ordering between them) race and must not be
  * made; calls on one stream are fine.  Returns W8_ERR_DTYPE on a bf16 build.
  * One kernel launch on s. */
-#define W8_NOALLOC_SCRATCH_BYTES (1u << 20)
+#define W8_NOALLOC_SCRATCH_BYTES (256u << 10)
 w8_status w8_gemv_noalloc(const w8_build *b, int plane, const uint16_t *x, int64_t ldx, int m,
                           uint16_t *y, int64_t ldy, w8_stream s);
 

@@ -27,6 +27,8 @@ from .gpu_util import bind_plane, dev, from_dev, to_dev
 
 pytestmark = pytest.mark.gpu
 
+LIMIT = 256 << 10  # W8_NOALLOC_SCRATCH_BYTES
+
 
 @pytest.fixture(scope="module")
 def w8():
@@ -37,9 +39,9 @@ def w8():
     return lib
 
 
-# (n, k, m): two plans that split K across CTAs (and so use the scratch), one
-# small and one large plane whose plans do not
-CASES = [(128, 6144, 16), (32, 6144, 64), (40, 6144, 5), (2624, 6144, 4)]
+# (n, k, m): plans that split K across CTAs (and so use the scratch) and a
+# large plane whose plan does not
+CASES = [(128, 6144, 16), (32, 6144, 32), (40, 6144, 5), (2624, 6144, 4)]
 
 
 @pytest.mark.parametrize("n,k,m", CASES)
@@ -51,7 +53,7 @@ def test_noalloc_equals_gemv_with_workspace(w8, n, k, m):
     needs_scratch = b.plan(0, m).splits > 1
     if (n, k) in ((128, 6144), (32, 6144)):
         assert needs_scratch
-    assert b.workspace_bytes(0, m) <= (1 << 20)
+    assert b.workspace_bytes(0, m) <= LIMIT
 
     xd = to_dev(x)
     y_ref = torch.zeros((m, n), dtype=torch.int16, device=dev())
@@ -71,20 +73,24 @@ def test_noalloc_equals_gemv_with_workspace(w8, n, k, m):
 
 
 def test_noalloc_refuses_what_it_cannot_serve(w8):
-    # a plan whose split partials exceed the fixed scratch
-    n, k, m = 1024, 4096, 64
-    p = w8.plan_shape(n, k, m, torch.cuda.get_device_properties(dev()).multi_processor_count)
+    # a plan whose split partials exceed the fixed scratch (the first such
+    # shape for this GPU's SM count)
+    sms = torch.cuda.get_device_properties(dev()).multi_processor_count
+    cands = [(n, k, 64) for n in (16, 32, 64, 128, 256, 512, 1024) for k in (6144, 16384)]
+    over = [c for c in cands if w8.plan_shape(*c, sms).workspace_bytes > LIMIT]
+    assert over, "no candidate shape needs more than the fixed scratch"
+    n, k, m = over[0]
     rng = np.random.default_rng(7)
     plane = synth.weight_plane(rng, n, k)
     b, _src = bind_plane(w8, plane)
+    assert b.plan(0, m).workspace_bytes > LIMIT
     x = to_dev(synth.activations(rng, k, m))
     y = torch.zeros((m, n), dtype=torch.int16, device=dev())
-    if p.workspace_bytes > (1 << 20):
-        with pytest.raises(w8.W8Error) as e:
-            w8.w8_gemv_noalloc(b, 0, x, y)
-        assert e.value.name == "W8_ERR_SCRATCH"
-        torch.cuda.synchronize()
-        assert torch.all(y == 0)
+    with pytest.raises(w8.W8Error) as e:
+        w8.w8_gemv_noalloc(b, 0, x, y)
+    assert e.value.name == "W8_ERR_SCRATCH"
+    torch.cuda.synchronize()
+    assert torch.all(y == 0)
     # a bf16 build is refused
     bp = synth.weight_plane(rng, 64, 256, "bf16")
     b16, _src16 = bind_plane(w8, bp)
