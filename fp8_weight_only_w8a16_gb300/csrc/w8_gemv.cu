@@ -27,6 +27,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "w8_internal.h"
 
 namespace w8 {
@@ -454,18 +456,27 @@ void *inst()
                                                  depth_x(NT, R, kFp8, OCC), OCC>);
 }
 
+template <bool kFp8, int I>
+void *inst_at()
+{
+    return inst<kFp8, kInst[I].nt, kInst[I].r, kInst[I].occ>();
+}
+
+template <bool kFp8, int... Is>
+void *pick_from(int idx, std::integer_sequence<int, Is...>)
+{
+    void *fn = nullptr;
+    ((fn = (idx == Is ? inst_at<kFp8, Is>() : fn)), ...);
+    return fn;
+}
+
 template <bool kFp8>
 void *pick(int nt, int r, int occ)
 {
-    switch (nt) {
-    case 1:
-        if (occ == 3)
-            return r == 1 ? inst<kFp8, 1, 1, 3>() : inst<kFp8, 1, 2, 3>();
-        return r == 1 ? inst<kFp8, 1, 1, 2>() : inst<kFp8, 1, 2, 2>();
-    case 2: return inst<kFp8, 2, 2, 2>();
-    case 4: return inst<kFp8, 4, 2, 1>();
-    default: return inst<kFp8, 8, 2, 1>();
-    }
+    const int idx = inst_index(nt, r, occ);
+    if (idx < 0)
+        return nullptr;
+    return pick_from<kFp8>(idx, std::make_integer_sequence<int, kNumInst>{});
 }
 
 } // namespace
@@ -473,12 +484,10 @@ void *pick(int nt, int r, int occ)
 cudaError_t prepare_gemv_kernels()
 {
     // the K-part reduction buffer: 8 warps x R x NT x 128 floats, at most 64 KB
-    const int nts[7] = {1, 1, 1, 1, 2, 4, 8};
-    const int rs[7] = {1, 2, 1, 2, 2, 2, 2};
-    const int occs[7] = {2, 2, 3, 3, 2, 1, 1};
-    for (int i = 0; i < 7; ++i) {
+    for (int i = 0; i < kNumInst; ++i) {
         for (int f = 0; f < 2; ++f) {
-            void *fn = f ? pick<true>(nts[i], rs[i], occs[i]) : pick<false>(nts[i], rs[i], occs[i]);
+            void *fn = f ? pick<true>(kInst[i].nt, kInst[i].r, kInst[i].occ)
+                         : pick<false>(kInst[i].nt, kInst[i].r, kInst[i].occ);
             cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  64 * 1024);
             if (e != cudaSuccess)
@@ -491,6 +500,8 @@ cudaError_t prepare_gemv_kernels()
 cudaError_t launch_gemv(bool fp8, const Plan &plan, const GemvArgs &a, cudaStream_t s)
 {
     void *fn = fp8 ? pick<true>(plan.nt, plan.r, plan.occ) : pick<false>(plan.nt, plan.r, plan.occ);
+    if (!fn)
+        return cudaErrorInvalidValue;
     void *args[] = {const_cast<GemvArgs *>(&a)};
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(unsigned(plan.grid));

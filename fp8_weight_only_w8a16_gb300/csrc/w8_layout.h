@@ -106,30 +106,41 @@ struct Plan {
 
 W8_HD int nt_for_m(int m) { return m <= 8 ? 1 : m <= 16 ? 2 : m <= 32 ? 4 : 8; }
 
-// The kernel instances.  For each token-group count NT, row tiles per warp R
-// and occupancy OCC (CTAs per SM the instance is built for): the weight ring
-// depth DW and the activation ring depth DX in K blocks (DX divides DW).  For
-// NT = 1 there are two families: OCC = 2 with deep rings (the most bytes in
-// flight per warp) and OCC = 3 with shallow rings (more warps per SM).  The
-// depths are the only dtype-dependent choice -- a bf16 block takes twice the
-// registers of an FP8 block, so its ring holds half the blocks and the same
-// bytes -- and no depth changes a summation order.  Activations come from
-// L2/L1, so their ring can be shallower than the HBM weight ring.
-W8_HD constexpr int depth_w(int nt, int r, bool fp8, int occ)
+// The kernel instances: a table of (token groups NT, row tiles per warp R,
+// CTAs per SM OCC) with, per weight dtype, the weight ring depth DW and the
+// activation ring depth DX in K blocks (DX divides DW).  Deep rings give the
+// most bytes in flight per warp, higher occupancy gives more warps per SM; the
+// planner picks per shape.  The depths are the only dtype-dependent choice --
+// a bf16 block takes twice the registers of an FP8 block, so its ring holds
+// about half the blocks and the same bytes -- and no depth changes a
+// summation order.  Activations come from L2/L1, so their ring can be
+// shallower than the HBM weight ring.
+struct Inst {
+    int nt, r, occ;
+    int dw_fp8, dx_fp8, dw_bf16, dx_bf16;
+};
+constexpr int kNumInst = 10;
+constexpr Inst kInst[kNumInst] = {
+    {1, 1, 2, 16, 8, 8, 4}, {1, 2, 2, 8, 4, 4, 2}, {1, 1, 3, 8, 4, 4, 2}, {1, 2, 3, 4, 2, 2, 2},
+    {2, 1, 2, 10, 5, 6, 3}, {2, 2, 2, 6, 3, 2, 2},
+    {4, 1, 2, 6, 2, 4, 2},  {4, 2, 1, 8, 4, 4, 2},
+    {8, 1, 1, 6, 2, 4, 2},  {8, 2, 1, 6, 2, 4, 2},
+};
+constexpr int inst_index(int nt, int r, int occ)
 {
-    return nt == 1 ? (occ == 3 ? (fp8 ? (r == 1 ? 8 : 4) : (r == 1 ? 4 : 2))
-                               : (fp8 ? (r == 1 ? 16 : 8) : (r == 1 ? 8 : 4)))
-                   : (fp8 ? (nt == 2 ? 6 : nt == 4 ? 8 : 6) : (nt == 2 ? 2 : 4));
+    for (int i = 0; i < kNumInst; ++i)
+        if (kInst[i].nt == nt && kInst[i].r == r && kInst[i].occ == occ)
+            return i;
+    return -1;
 }
-W8_HD constexpr int depth_x(int nt, int r, bool fp8, int occ)
+constexpr int depth_w(int nt, int r, bool fp8, int occ)
 {
-    return nt == 1 ? (occ == 3 ? (fp8 ? (r == 1 ? 4 : 2) : 2)
-                               : (fp8 ? (r == 1 ? 8 : 4) : (r == 1 ? 4 : 2)))
-                   : (fp8 ? (nt == 2 ? 3 : nt == 4 ? 4 : 2) : 2);
+    return fp8 ? kInst[inst_index(nt, r, occ)].dw_fp8 : kInst[inst_index(nt, r, occ)].dw_bf16;
 }
-// occupancies available for a token-group count (highest last)
-W8_HD constexpr int occ_min(int nt) { return nt == 1 ? 2 : nt == 2 ? 2 : 1; }
-W8_HD constexpr int occ_max(int nt) { return nt == 1 ? 3 : nt == 2 ? 2 : 1; }
+constexpr int depth_x(int nt, int r, bool fp8, int occ)
+{
+    return fp8 ? kInst[inst_index(nt, r, occ)].dx_fp8 : kInst[inst_index(nt, r, occ)].dx_bf16;
+}
 
 inline int64_t plan_ctas(int64_t rt, int r, int wk, int splits)
 {
@@ -154,9 +165,12 @@ inline Plan make_plan(int64_t n, int64_t k, int m, int sm_count)
     bool have = false;
     int64_t best_waves = 0, best_inflight = 0, best_warps = 0, best_bpw = 0;
     int best_r = 1, best_wk = 1, best_occ = 1;
-    for (int occ = occ_min(p.nt); occ <= occ_max(p.nt); ++occ) {
+    for (int ii = 0; ii < kNumInst; ++ii) {
+        if (kInst[ii].nt != p.nt)
+            continue;
+        const int occ = kInst[ii].occ, r = kInst[ii].r;
         const int64_t slots = int64_t(sms) * occ;
-        for (int r = (p.nt == 1 ? 1 : 2); r <= 2; ++r) {
+        {
             for (int wk = 8; wk >= 1; wk /= 2) {
                 const int64_t bpw = p.kb / wk;
                 if (wk > 1 && bpw < kMinBlocks)
