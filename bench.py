@@ -373,8 +373,11 @@ def run_ours(args):
     peak, peak_kind = measured_peaks()
     launches = len(ms) * args.steps
     achieved = step_bytes * args.steps / (t_ms * 1e-3) / 1e9  # per GPU, kernel-time average
-    dominant = max(ms, key=lambda m: per_m[m]["us_per_call"])
-    traffic = recorded_traffic(proj.name, dominant)
+    # DRAM bytes per launch, averaged over the step's launches like `achieved`
+    # (None unless the committed ncu summary was taken on this kernel source)
+    per_m_traffic = [recorded_traffic(proj.name, m) for m in ms]
+    traffic = (round(sum(per_m_traffic) / len(ms))
+               if all(t is not None for t in per_m_traffic) else None)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": f"hbm_gbs of {peak_kind}",

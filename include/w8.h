@@ -2,7 +2,7 @@
  * w8.h -- C ABI of libw8: the FP8 weight-only (w8a16) decode GEMV for one
  * GB300 GPU (sm_103a).
  *
- * What the library computes (ATOM PR #2980 "FP8 reads for mono decode",
+ * What the library computes (ATOM pull request #2980,
  * sections Summary and Changes): for a bound weight plane W [N, K] and M
  * decode tokens x [M, K] (bf16),
  *

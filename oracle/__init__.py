@@ -7,7 +7,7 @@ legs of ``bench.py`` use it.
 
 The arithmetic lives in ``w8_oracle.c`` (plain C, fp32 ascending-k
 accumulation, one fp32 scale multiply, one bf16 round to nearest even), which
-follows ATOM PR #2980 ("FP8 reads for mono decode"), sections Summary and
+follows ATOM pull request #2980, sections Summary and
 Changes: the E4M3 plane widens exactly to bf16 and the fp32 row scale
 multiplies each reduced row before the bf16 rounding.  ``brute.py`` is an
 independent numpy fp64 recompute used to pin it.

@@ -6,7 +6,7 @@
  * leg of bench.py use it.  It shares no code, header, table or constant with
  * the CUDA path under fp8_weight_only_w8a16_gb300/csrc.
  *
- * What it computes (ATOM PR #2980 "FP8 reads for mono decode", sections
+ * What it computes (ATOM pull request #2980, sections
  * Summary and Changes): for every output row n and decode token m
  *
  *     y[m,n] = bf16_rne( scale[n] * sum_k widen(W[n,k]) * x[m,k] )
