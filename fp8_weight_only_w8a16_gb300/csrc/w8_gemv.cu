@@ -112,6 +112,12 @@ __device__ __forceinline__ void pdl_wait()
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Hint: fetch `bytes` at p into L2 (a bulk prefetch; nothing waits on it).
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ float ld_cg_f32(const float *p)
 {
     float v;
@@ -258,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
     nmain = nmain < 0 ? 0 : (nmain > nkb ? nkb : nmain);
     const bool has_tail = nkb > nmain;
 
-    const uint8_t *wptr[R];
+    const uint8_t *wptr[R]; // this lane's 16 bytes of the warp's first run of each tile
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const int tile = rg * (wt * R) + r * wt + tg;
@@ -276,7 +282,18 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
 
     // Weights first: the packed plane is written only by w8_bind, which
     // finishes before any GEMV can be launched, so these loads may overlap the
-    // tail of the previous kernel on the stream.
+    // tail of the previous kernel on the stream.  The ring holds blocks
+    // [0, DW); blocks up to kPf go to L2 now, and every ring group sends the
+    // kPf-distant group after it (bulk prefetches: no registers, no waits).
+    // Lane 0 issues them, so its wptr is the start of the warp's runs.
+    constexpr int kPf = DW > 16 ? DW : 16;
+    if (lane == 0 && nmain > DW) {
+        const int hi = nmain < kPf ? nmain : kPf;
+        if (hi > DW)
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+                prefetch_l2(wptr[r] + DW * kRun, uint32_t(hi - DW) * kRun);
+    }
     WFrag<kFp8> wring[DW][R];
     uint4 xring[DX][NT];
 #pragma unroll
@@ -322,6 +339,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
     // further on.
     int b = 0;
     for (; b + DW <= nmain; b += DW) {
+        if (lane == 0 && b + kPf < nmain) {
+            const int hi = b + kPf + DW < nmain ? b + kPf + DW : nmain;
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+                prefetch_l2(wptr[r] + (b + kPf) * kRun, uint32_t(hi - b - kPf) * kRun);
+        }
 #pragma unroll
         for (int i = 0; i < DW; ++i) {
             block_step<kFp8, NT, R>(acc, wring[i], xring[i % DX]);
