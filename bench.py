@@ -77,7 +77,7 @@ def measured_peaks():
 
 def gemv_source_sha() -> str:
     h = hashlib.sha256()
-    for f in ("w8_gemv.cu", "w8_layout.h", "w8_internal.h"):
+    for f in ("w8_gemv.cu", "w8_tc.cu", "w8_device.cuh", "w8_layout.h", "w8_internal.h"):
         with open(os.path.join(ROOT, "fp8_weight_only_w8a16_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

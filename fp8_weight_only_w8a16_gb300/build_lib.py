@@ -23,7 +23,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libw8.so")
 
-SOURCES = ["w8_api.cu", "w8_gemv.cu", "w8_repack.cu", "w8_noalloc.cu"]
+SOURCES = ["w8_api.cu", "w8_gemv.cu", "w8_tc.cu", "w8_repack.cu", "w8_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
               "-Xptxas", "-v", "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -103,7 +103,7 @@ w8_status gemv_common(const w8_build *b, int plane, int32_t want_dtype, const ui
     a.rt = int(plan.rt);
     a.splits = plan.splits;
     a.wk = plan.wk;
-    if (plan.splits > 1) {
+    if (plan.ws_bytes > 0) { // register-ring split-K plans (tensor-memory plans need none)
         if (!ws)
             return W8_ERR_NULL;
         if (reinterpret_cast<uintptr_t>(ws) & 255u)
@@ -149,6 +149,15 @@ const char *w8_status_str(w8_status s)
 }
 
 int w8_abi_version(void) { return W8_ABI_VERSION; }
+
+w8_status w8_device_status(int *status, int reset)
+{
+    if (!status)
+        return W8_ERR_NULL;
+    if (w8::tc_status(status, reset != 0) != cudaSuccess)
+        return W8_ERR_CUDA;
+    return W8_OK;
+}
 
 w8_status w8_validate(const w8_plane_desc *d, int n_planes)
 {
@@ -281,8 +290,9 @@ w8_status w8_plan_shape(int64_t n, int64_t k, int m, int sm_count, w8_plan *out)
     if (n < 1 || k < 1 || n > kMaxDim || k > kMaxDim || m < 1 || m > w8::kMaxM || sm_count < 1)
         return W8_ERR_SHAPE;
     const w8::Plan pl = w8::make_plan(n, k, m, sm_count);
+    out->kernel = pl.tc ? 1 : 0;
     out->grid = pl.grid;
-    out->block = w8::kThreads;
+    out->block = pl.tc ? w8::kTcThreadsPerCta : w8::kThreads;
     out->smem_bytes = pl.smem;
     out->n_tiles = pl.nt;
     out->row_tiles_per_warp = pl.r;

@@ -29,47 +29,15 @@
 
 #include <utility>
 
+#include "w8_device.cuh"
 #include "w8_internal.h"
 
 namespace w8 {
 namespace {
 
 // ---------------------------------------------------------------------------
-// device helpers
+// device helpers of this kernel (the shared ones are in w8_device.cuh)
 // ---------------------------------------------------------------------------
-
-// Streaming 16-byte weight load: read-only path, no L1 allocation, 256-byte
-// L2 fetch granule (a warp's 512-byte run is two granules).
-__device__ __forceinline__ uint4 ld_stream(const uint8_t *p)
-{
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-        : "l"(p));
-    return v;
-}
-
-// Two E4M3fn codes -> two bf16, exactly.  `sel` picks bytes (0,2) or (1,3) of
-// the word and puts each code in the low byte of a 16-bit lane with its sign
-// replicated across the high byte (prmt's sign-replicate mode).  Shifting left
-// by 4 and masking leaves the sign at bit 15 and the 7 exponent+mantissa bits
-// at bits 10..4: a bf16 whose exponent field is the E4M3 exponent field
-// (bias 127 instead of 7) and whose top 3 mantissa bits are the E4M3 mantissa
-// (a bf16 subnormal when the exponent field is 0, just as E4M3 subnormals).
-// Multiplying by 2^120 moves the bias from 127 to 7; the product is exact for
-// every finite code, including subnormals and zeros.  (The two NaN codes come
-// out as +-480; their rows carry a NaN scale instead, set at bind.)
-template <uint32_t kSel>
-__device__ __forceinline__ uint32_t widen_e4m3x2(uint32_t w)
-{
-    uint32_t d, r;
-    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(d) : "r"(w), "n"(kSel));
-    d = (d << 4) & 0x87F087F0u;
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(d), "r"(0x7B807B80u)); // 2^120, 2^120
-    return r;
-}
-constexpr uint32_t kSelRowG = 0xA280u;  // bytes 0 and 2 (row g)
-constexpr uint32_t kSelRowG8 = 0xB391u; // bytes 1 and 3 (row g+8)
 
 // D += A * B, m16n8k16, bf16 inputs, fp32 accumulators.
 __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -79,115 +47,6 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// fp32 -> bf16, round to nearest even (NaN stays NaN, overflow gives inf).
-__device__ __forceinline__ uint16_t to_bf16(float f)
-{
-    uint16_t h;
-    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(f));
-    return h;
-}
-
-// 4-byte asynchronous copy global -> shared (the CTA's row scales).
-__device__ __forceinline__ void cp_async4(float *smem, const float *gmem)
-{
-    const uint32_t s = uint32_t(__cvta_generic_to_shared(smem));
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all()
-{
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
-}
-
-// Programmatic dependent launch: let the next kernel of the stream begin
-// launching, and wait until the previous one has finished and its writes are
-// visible.  Both are no-ops when the launch carries no programmatic edge.
-__device__ __forceinline__ void pdl_launch_dependents()
-{
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait()
-{
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-// Hint: fetch `bytes` at p into L2 (a bulk prefetch; nothing waits on it).
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ float ld_cg_f32(const float *p)
-{
-    float v;
-    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
-    return v;
-}
-
-// Weight operand of one (row tile, K block) for one lane.
-template <bool kFp8> struct WFrag;
-template <> struct WFrag<true> { uint4 v; };
-template <> struct WFrag<false> { uint4 v[2]; };
-
-template <bool kFp8>
-__device__ __forceinline__ void load_w(WFrag<kFp8> &f, const uint8_t *p)
-{
-    if constexpr (kFp8) {
-        f.v = ld_stream(p);
-    } else {
-        f.v[0] = ld_stream(p);
-        f.v[1] = ld_stream(p + 512);
-    }
-}
-
-// Predicated weight load: fills f only when ok (f keeps its value otherwise).
-__device__ __forceinline__ void ld_stream_pred(uint4 &v, const uint8_t *p, uint32_t ok)
-{
-    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %5, 0;\n\t"
-                 "@q ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];\n\t}"
-                 : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
-                 : "l"(p), "r"(ok));
-}
-
-template <bool kFp8>
-__device__ __forceinline__ void load_w_pred(WFrag<kFp8> &f, const uint8_t *p, uint32_t ok)
-{
-    if constexpr (kFp8) {
-        ld_stream_pred(f.v, p, ok);
-    } else {
-        ld_stream_pred(f.v[0], p, ok);
-        ld_stream_pred(f.v[1], p + 512, ok);
-    }
-}
-
-template <bool kFp8>
-__device__ __forceinline__ void zero_w(WFrag<kFp8> &f)
-{
-    if constexpr (kFp8) {
-        f.v = make_uint4(0, 0, 0, 0);
-    } else {
-        f.v[0] = make_uint4(0, 0, 0, 0);
-        f.v[1] = make_uint4(0, 0, 0, 0);
-    }
-}
-
-template <bool kFp8>
-__device__ __forceinline__ void a_operands(uint32_t (&a)[8], const WFrag<kFp8> &f)
-{
-    if constexpr (kFp8) {
-        a[0] = widen_e4m3x2<kSelRowG>(f.v.x);
-        a[1] = widen_e4m3x2<kSelRowG8>(f.v.x);
-        a[2] = widen_e4m3x2<kSelRowG>(f.v.y);
-        a[3] = widen_e4m3x2<kSelRowG8>(f.v.y);
-        a[4] = widen_e4m3x2<kSelRowG>(f.v.z);
-        a[5] = widen_e4m3x2<kSelRowG8>(f.v.z);
-        a[6] = widen_e4m3x2<kSelRowG>(f.v.w);
-        a[7] = widen_e4m3x2<kSelRowG8>(f.v.w);
-    } else {
-        a[0] = f.v[0].x; a[1] = f.v[0].y; a[2] = f.v[0].z; a[3] = f.v[0].w;
-        a[4] = f.v[1].x; a[5] = f.v[1].y; a[6] = f.v[1].z; a[7] = f.v[1].w;
-    }
 }
 
 // 8 activations x[tok][col .. col+7] of one lane, loaded only when `ok`;
@@ -517,11 +376,13 @@ cudaError_t prepare_gemv_kernels()
                 return e;
         }
     }
-    return cudaSuccess;
+    return prepare_tc_kernels();
 }
 
 cudaError_t launch_gemv(bool fp8, const Plan &plan, const GemvArgs &a, cudaStream_t s)
 {
+    if (plan.tc)
+        return launch_tc(fp8, plan, a, s);
     void *fn = fp8 ? pick<true>(plan.nt, plan.r, plan.occ) : pick<false>(plan.nt, plan.r, plan.occ);
     if (!fn)
         return cudaErrorInvalidValue;

@@ -42,6 +42,12 @@ cudaError_t launch_gemv(bool fp8, const Plan &plan, const GemvArgs &a, cudaStrea
 // current device (called once per device before the first launch).
 cudaError_t prepare_gemv_kernels();
 
+// The tensor-memory kernel (w8_tc.cu), which launch_gemv runs for plan.tc.
+cudaError_t launch_tc(bool fp8, const Plan &plan, const GemvArgs &a, cudaStream_t s);
+cudaError_t prepare_tc_kernels();
+// Read (and optionally clear) the tc kernel's device status word.
+cudaError_t tc_status(int *out, bool reset);
+
 struct RepackArgs {
     const uint8_t *src;     // source plane (device), row-major
     int64_t ld_bytes;       // source row stride in bytes

@@ -88,6 +88,8 @@ W8_HD int64_t packed_offset_bf16(int64_t k_blocks, int64_t row, int64_t col)
 // fixed order that depends only on the plan.
 // ---------------------------------------------------------------------------
 struct Plan {
+    bool tc;         // the tensor-memory kernel (w8_tc.cu) instead of the register ring
+    int npad;        // tc: tokens rounded up to 16 (the tensor-core N)
     int nt;          // 8-token groups (tensor-core N = 8): 1, 2, 4 or 8
     int r;           // row tiles per warp
     int dw;          // weight prefetch depth in K blocks (FP8 instance; see depth_w)
@@ -153,8 +155,78 @@ inline int64_t plan_ctas(int64_t rt, int r, int wk, int splits)
 // (activations reused over two tiles), then the longest K parts.  Every warp keeps at least kMinBlocks
 // K blocks when K allows it.  K is split across CTAs only for planes whose
 // row tiles leave most SMs idle.
+// The tensor-memory kernel (w8_tc.cu): CTAs of 128 rows x a K range, seven
+// warps, 2 CTAs per SM (256 tensor-memory columns and about 100 KB of shared
+// memory each).  K is split across the CTAs of a cluster (up to 8) until about
+// two CTAs per SM are busy, keeping at least one stage of K blocks per split;
+// the partial sums meet in distributed shared memory, so no workspace.
+constexpr int kTcMinM = 17;       // decode tokens from which the tc kernel may run
+constexpr int kTcMinRowBlocks = 48; // ... on planes of at least this many 128-row blocks
+constexpr int kTcStageBlocks = 4; // K blocks per stage of the tc kernel
+constexpr int kTcCtasPerSm = 2;
+constexpr int kTcThreadsPerCta = 224;
+
+// Stage slots of the tensor-memory kernel in shared memory: nw weight stages
+// (8 row tiles x 4 K blocks of packed runs, filled by bulk copies) and nb
+// activation stages (4 K blocks x npad tokens), about 100 KB per CTA so that
+// two CTAs share an SM.
+struct TcStages {
+    int nw, nb;
+};
+W8_HD constexpr TcStages tc_stages(bool fp8, int npad)
+{
+    return fp8 ? (npad <= 16 ? TcStages{5, 6} : npad <= 32 ? TcStages{4, 5}
+                  : npad <= 48 ? TcStages{4, 3} : TcStages{3, 3})
+               : (npad <= 16 ? TcStages{3, 2} : npad <= 32 ? TcStages{2, 4}
+                  : npad <= 48 ? TcStages{2, 3} : TcStages{2, 2});
+}
+W8_HD constexpr int tc_smem_bytes(bool fp8, int npad)
+{
+    return tc_stages(fp8, npad).nw * 8 * 4 * (fp8 ? kRunFp8 : kRunBf16) +
+           tc_stages(fp8, npad).nb * 4 * npad * 64;
+}
+constexpr int kTcMaxSplits = 8;
+
+inline Plan make_tc_plan(int64_t n, int64_t k, int m, int sm_count)
+{
+    Plan p{};
+    p.tc = true;
+    p.npad = int(ceil_div(m, 16) * 16);
+    p.nt = p.npad / 8;
+    p.r = 8;  // row tiles per CTA
+    p.dw = tc_stages(true, p.npad).nw * kTcStageBlocks; // weight blocks staged ahead (FP8)
+    p.occ = kTcCtasPerSm;
+    p.wk = 1;
+    p.rt = ceil_div(n, kTileN);
+    p.kb = ceil_div(k, kTileK);
+    const int64_t rbs = ceil_div(n, 128);
+    const int64_t target = int64_t(sm_count > 0 ? sm_count : 1) * kTcCtasPerSm;
+    // the splits of a row block form one thread-block cluster: a power of two
+    // up to 8 (the portable cluster size) that keeps one stage per split
+    int splits = 1;
+    while (splits < kTcMaxSplits && rbs * splits * 2 <= target &&
+           p.kb / (int64_t(splits) * 2) >= kTcStageBlocks)
+        splits *= 2;
+    p.splits = splits;
+    p.row_groups = int(rbs);
+    p.grid = int(rbs * splits);
+    p.kbs_max = int(ceil_div(p.kb, splits));
+    p.smem = tc_smem_bytes(true, p.npad); // the FP8 instance; bf16 stages are as large
+    p.ws_counters = p.ws_bytes = 0; // partial sums stay on chip (cluster exchange)
+    return p;
+}
+
+// Which kernel a shape gets (measured on GB300 over the GLM-5.2 projections):
+// the tensor-memory kernel wins from 17 tokens on planes with many row blocks
+// (o_proj, q_b, kv_b), where one activation tile serves 128 rows; the register
+// ring wins below that and on planes with few rows, where the tc kernel's
+// fixed cost per CTA and its cluster reduction dominate.
+inline bool use_tc(int64_t n, int m) { return m >= kTcMinM && ceil_div(n, 128) >= kTcMinRowBlocks; }
+
 inline Plan make_plan(int64_t n, int64_t k, int m, int sm_count)
 {
+    if (use_tc(n, m))
+        return make_tc_plan(n, k, m, sm_count);
     Plan p{};
     p.nt = nt_for_m(m);
     p.rt = ceil_div(n, kTileN);

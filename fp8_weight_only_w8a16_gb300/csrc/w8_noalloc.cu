@@ -30,7 +30,7 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = size_t(256) << 10; // W8_NOALLOC_SCRATCH_BYTES
+constexpr size_t kScratchBytes = size_t(32) << 10; // W8_NOALLOC_SCRATCH_BYTES
 static_assert(kScratchBytes == W8_NOALLOC_SCRATCH_BYTES, "keep w8.h in step");
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
@@ -103,7 +103,7 @@ extern "C" w8_status w8_gemv_noalloc(const w8_build *b, int plane, const uint16_
     a.rt = int(plan.rt);
     a.splits = plan.splits;
     a.wk = plan.wk;
-    if (plan.splits > 1) {
+    if (plan.ws_bytes > 0) {
         void *ws = nullptr;
         const w8_status st = scratch_on(dev, &ws);
         if (st != W8_OK)

@@ -1,0 +1,613 @@
+// w8_tc.cu -- the w8a16 / bf16 GEMV on the fifth-generation tensor cores
+// (tcgen05, tensor memory), for calls with 9..64 decode tokens.
+//
+// Computes, per output row n and decode token m (ATOM pull request #2980,
+// Summary and Changes),
+//     y[m,n] = bf16_rne( scale[n] * sum_k widen(W[n,k]) * x[m,k] )
+// with fp32 accumulation, like the register-ring kernel in w8_gemv.cu, but
+// with the tokens as the N dimension of a 128 x NPAD x 16 tensor-core step
+// (NPAD = tokens rounded up to 16), so that one activation tile in shared
+// memory serves 128 weight rows instead of 16.
+//
+// One CTA = 128 output rows (8 row tiles of the packed layout) x one range of
+// K blocks, seven warps:
+//   warp 6 (weights): one thread copies the CTA's packed runs into shared
+//     memory with bulk asynchronous copies (one per row tile and stage of 4 K
+//     blocks: a tile's runs are contiguous), filling every weight stage
+//     before the dependency wait -- the plane is bind-time data;
+//   warps 0-3 (converters): warp q reads row tiles 2q and 2q+1 of each stage
+//     from shared memory, widens E4M3 to bf16 exactly (bf16 planes pass
+//     through) and stores the A operand into tensor memory, TMEM lanes
+//     32q..32q+31, in natural K order (below);
+//   warp 4 (activations): after the dependency wait, one thread copies the
+//     activation tiles with tensor-map bulk copies (TMA): one 8-column x
+//     tokens box per K group, landing as the 8-row x 16-byte core matrices
+//     of the tensor cores' K-major layout; rows past the tokens and columns
+//     past K arrive as zeros;
+//   warp 5 (issuer): one thread issues the tensor-core steps
+//     D[128 x NPAD] += A[128 x 16] (TMEM) * B[16 x NPAD] (shared memory) and
+//     commits them to the stages' "empty" barriers.
+// Weight, A and activation stages rotate through their slots with mbarriers
+// ("full": the producers arrive or the copies complete; "empty": the
+// consumers arrive or the issuer commits).  After the last step the
+// accumulator D (TMEM columns [0, NPAD)) is read by the converter warps, one
+// row per thread: scale, round, store.  With K split across CTAs, the splits
+// of a row block form a thread-block cluster: each CTA parks its partial tile
+// in its shared memory and rank r adds rows [r R, (r+1) R) of all the tiles
+// in split order through distributed shared memory.
+//
+// K order.  Tensor-core step s of a 32-column block covers columns
+// 16s..16s+15 in order: TMEM column c of the step holds columns 16s+2c,
+// 16s+2c+1.  tcgen05.st 16x256b.x2 gives lane (g, t) columns 2t, 2t+1 of
+// each step for rows g and g+8, i.e. the 4-column units t (step 0) and t+4
+// (step 1).  In the packed layout, unit u of a tile lives in packed lane
+// 4g + u/2: for FP8 in its words 2(u%2), 2(u%2)+1 (8 bytes), for bf16 in half
+// u%2 (16 bytes); the converter reads exactly those from shared memory.
+//
+// Every mbarrier wait is bounded; on timeout the kernel sets a bit in the
+// library's device status word (w8_device_status) and runs to its end, where
+// tensor memory is always released.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "w8_device.cuh"
+#include "w8_internal.h"
+
+namespace w8 {
+
+// Status word of the tensor-core kernel on each device: bit 0 = a stage
+// barrier wait timed out, bit 1 = the accumulator wait timed out.
+__device__ int g_tc_status;
+
+namespace {
+
+constexpr int kTcKs = 4;         // K blocks per stage
+constexpr int kTcStages = 3;     // stage slots
+constexpr int kTcThreads = kTcThreadsPerCta; // 4 converters, activations, issuer, weights
+static_assert(kTcThreads == 224, "seven warps");
+static_assert(kTcKs == kTcStageBlocks, "the planner's stage size");
+constexpr int kTmemCols = 256;   // D: [0, 64); A stages: [64, 256)
+constexpr int kACol = 64;
+constexpr uint32_t kSpinLimit = 1u << 24;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return uint32_t(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Wait for the phase with the given parity to complete; false after
+// kSpinLimit polls (each poll may itself suspend for a short while).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+{
+    const uint32_t addr = smem_u32(bar);
+    for (uint32_t it = 0; it < kSpinLimit; ++it) {
+        uint32_t done;
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(done)
+                     : "r"(addr), "r"(parity)
+                     : "memory");
+        if (done)
+            return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void tc_fence_before()
+{
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after()
+{
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tm_wait_st()
+{
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tm_load16(uint32_t taddr, float *d)
+{
+    uint32_t r[16];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr)
+                 : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        d[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tm_wait_ld()
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, K-major, no swizzle: 8-row x 16-byte core
+// matrices; lbo = byte stride between core matrices along K, sbo = along N.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    return uint64_t((addr >> 4) & 0x3FFFu) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
+           (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46);
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]: bf16 inputs, fp32 accumulate, M = 128.
+__device__ __forceinline__ void umma_ts(uint32_t d_taddr, uint32_t a_taddr, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_taddr),
+                 "r"(a_taddr), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+// Arrive on `bar` once every tensor-core step this thread issued so far is done.
+__device__ __forceinline__ void umma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+// Bulk asynchronous copy global -> shared (16-byte aligned, a multiple of 16
+// bytes) whose completion counts `bytes` on the barrier's transaction count.
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared16(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+// Tensor-map bulk copy of a 2-D box (inner coordinate c0, outer c1) into
+// shared memory; its bytes count on the barrier's transaction count.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+                     dst),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// A operand of one 32-column block for 16 rows, registers in the order of
+// tcgen05.st 16x256b.x2: (row g, step 0 cols 2t, 2t+1), (row g+8, same),
+// (row g, step 1), (row g+8, step 1).
+__device__ __forceinline__ void tm_store_a(uint32_t taddr, const uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.16x256b.x2.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
+// Units t and t+4 of rows g and g+8 of one staged run (see "K order") as the
+// eight A registers of lane (g, t).
+template <bool kFp8>
+__device__ __forceinline__ void a_units(uint32_t (&r)[8], uint32_t run, int g, int t)
+{
+    if constexpr (kFp8) {
+        // 8 bytes = words (row g, g+8 at cols +0,+1), (row g, g+8 at cols +2,+3)
+        const uint32_t o0 = run + uint32_t((4 * g + (t >> 1)) * 16 + (t & 1) * 8);
+        uint32_t u0, u1, v0, v1;
+        asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(u0), "=r"(u1) : "r"(o0));
+        asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v0), "=r"(v1) : "r"(o0 + 32));
+        r[0] = widen_e4m3x2<kSelRowG>(u0);
+        r[1] = widen_e4m3x2<kSelRowG>(u1);
+        r[2] = widen_e4m3x2<kSelRowG8>(u0);
+        r[3] = widen_e4m3x2<kSelRowG8>(u1);
+        r[4] = widen_e4m3x2<kSelRowG>(v0);
+        r[5] = widen_e4m3x2<kSelRowG>(v1);
+        r[6] = widen_e4m3x2<kSelRowG8>(v0);
+        r[7] = widen_e4m3x2<kSelRowG8>(v1);
+    } else {
+        // 16 bytes = (row g, cols +0,+1), (row g+8, +0,+1), (row g, +2,+3), (row g+8, +2,+3)
+        const uint32_t o0 = run + uint32_t((t & 1) * 512 + (4 * g + (t >> 1)) * 16);
+        const uint4 u = ld_shared16(o0), v = ld_shared16(o0 + 32);
+        r[0] = u.x;
+        r[1] = u.z;
+        r[2] = u.y;
+        r[3] = u.w;
+        r[4] = v.x;
+        r[5] = v.z;
+        r[6] = v.y;
+        r[7] = v.w;
+    }
+}
+
+template <bool kFp8, int NPAD>
+__global__ void __launch_bounds__(kTcThreads, 2)
+    tc_gemv_kernel(const GemvArgs a, const __grid_constant__ CUtensorMap tmx)
+{
+    constexpr int kRun = kFp8 ? kRunFp8 : kRunBf16;
+    constexpr int kNW = tc_stages(kFp8, NPAD).nw; // weight stages (shared memory)
+    constexpr int kNB = tc_stages(kFp8, NPAD).nb; // activation stages (shared memory)
+    constexpr int kNA = kTcStages;                // A stages (tensor memory)
+    constexpr int kTileW = kTcKs * kRun;          // one row tile's runs of a stage
+    constexpr int kStageW = 8 * kTileW;
+    constexpr int kBlockB = NPAD * 64;            // activation bytes of one K block
+    constexpr int kStepB = NPAD * 32;             // ... of one 16-column step
+    constexpr int kStageB = kTcKs * kBlockB;
+    constexpr uint32_t kLbo = NPAD * 16;          // core matrices along K
+    constexpr uint32_t kSbo = 128;                // core matrices along the tokens
+    constexpr int kRedPitch = NPAD + 4;           // floats per row of the split-K exchange tile
+    // instruction descriptor: D f32, A and B bf16, both K-major, N = NPAD, M = 128
+    constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(NPAD >> 3) << 17) |
+                                (uint32_t(128 >> 4) << 24);
+    static_assert(NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 64, "M = 128 needs N in 16..256, step 16");
+    static_assert(128 * kRedPitch * 4 <= kNW * kStageW, "the exchange tile reuses the weight stages");
+    static_assert(kNW * kStageW + kNB * kStageB == tc_smem_bytes(kFp8, NPAD), "stage geometry");
+
+    extern __shared__ __align__(1024) uint8_t s_dyn[]; // kNW weight stages, then kNB B stages
+    __shared__ __align__(8) uint64_t bar_full_w[kNW], bar_empty_w[kNW];
+    __shared__ __align__(8) uint64_t bar_full_a[kNA], bar_empty_a[kNA];
+    __shared__ __align__(8) uint64_t bar_full_b[kNB], bar_empty_b[kNB];
+    __shared__ __align__(8) uint64_t bar_done;
+    __shared__ uint32_t s_tmem;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int rb = blockIdx.x / a.splits;               // row block: rows rb*128 ..
+    const int sp = blockIdx.x - rb * a.splits;          // == rank in the cluster
+    const int cb0 = int((int64_t(sp) * a.kb) / a.splits); // this CTA's K blocks
+    const int cnb = int((int64_t(sp + 1) * a.kb) / a.splits) - cb0;
+    const int nst = (cnb + kTcKs - 1) / kTcKs;          // stages
+    const int row0 = rb * 128;
+    const int tile0 = rb * 8;
+    uint8_t *const s_w = s_dyn;
+    uint8_t *const s_b = s_dyn + kNW * kStageW;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kNW; ++s) {
+            mbar_init(&bar_full_w[s], 1);
+            mbar_init(&bar_empty_w[s], 4);
+        }
+        for (int s = 0; s < kNA; ++s) {
+            mbar_init(&bar_full_a[s], 4);
+            mbar_init(&bar_empty_a[s], 1);
+        }
+        for (int s = 0; s < kNB; ++s) {
+            mbar_init(&bar_full_b[s], 1);
+            mbar_init(&bar_empty_b[s], 1);
+        }
+        mbar_init(&bar_done, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&s_tmem)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = s_tmem;
+    pdl_launch_dependents();
+
+    if (warp == 6) {
+        // ---- weights: packed runs -> shared memory (bulk copies) --------------
+        // The packed plane is written only by w8_bind, which finishes before any
+        // GEMV is launched, so this runs ahead of the dependency wait.
+        if (lane == 0) {
+            bool ok = true;
+            for (int st = 0; st < nst && ok; ++st) {
+                const int s = st % kNW;
+                if (st >= kNW)
+                    ok = mbar_wait(&bar_empty_w[s], uint32_t((st / kNW - 1) & 1));
+                if (!ok)
+                    break;
+                const int nb = cnb - st * kTcKs < kTcKs ? cnb - st * kTcKs : kTcKs;
+                int tiles = a.rt - tile0;
+                tiles = tiles > 8 ? 8 : tiles;
+                mbar_expect_tx(&bar_full_w[s], uint32_t(tiles * nb * kRun));
+                const uint32_t dst = smem_u32(s_w + s * kStageW);
+                for (int h = 0; h < tiles; ++h)
+                    bulk_copy(dst + uint32_t(h * kTileW),
+                              a.wp + (int64_t(tile0 + h) * a.kb + cb0 + st * kTcKs) * kRun,
+                              uint32_t(nb * kRun), &bar_full_w[s]);
+            }
+            if (!ok)
+                atomicOr(&g_tc_status, 1);
+        }
+    } else if (warp < 4) {
+        // ---- converters: staged weights -> widened A in tensor memory ---------
+        const uint32_t ok0 = tile0 + 2 * warp < a.rt, ok1 = tile0 + 2 * warp + 1 < a.rt;
+        const uint32_t lanes = uint32_t(32 * warp) << 16;
+        bool ok = true;
+        for (int st = 0; st < nst && ok; ++st) {
+            const int sw = st % kNW, sa_ = st % kNA;
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar_full_w[sw], uint32_t((st / kNW) & 1)));
+            if (ok && st >= kNA)
+                ok = __all_sync(0xffffffffu, mbar_wait(&bar_empty_a[sa_], uint32_t((st / kNA - 1) & 1)));
+            if (!ok)
+                break;
+            const uint32_t w0 = smem_u32(s_w + sw * kStageW + (2 * warp) * kTileW);
+            const uint32_t w1 = w0 + kTileW;
+            const int nb = cnb - st * kTcKs < kTcKs ? cnb - st * kTcKs : kTcKs;
+            const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+            for (int j = 0; j < kTcKs; ++j) {
+                if (j >= nb)
+                    break;
+                uint32_t r0[8] = {0, 0, 0, 0, 0, 0, 0, 0}, r1[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                if (ok0)
+                    a_units<kFp8>(r0, w0 + j * kRun, g, t);
+                if (ok1)
+                    a_units<kFp8>(r1, w1 + j * kRun, g, t);
+                const uint32_t col = uint32_t(kACol + (sa_ * kTcKs + j) * 16);
+                tm_store_a(tbase + lanes + col, r0);
+                tm_store_a(tbase + lanes + (16u << 16) + col, r1);
+            }
+            tm_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&bar_empty_w[sw]); // the stage's weights are in registers/TMEM
+                mbar_arrive(&bar_full_a[sa_]);
+            }
+        }
+        if (!ok && lane == 0)
+            atomicOr(&g_tc_status, 1);
+    } else if (warp == 4) {
+        // ---- activations: x -> B tiles in shared memory (tensor-map copies) -----
+        pdl_wait(); // x may be the previous kernel's output
+        if (lane == 0) {
+            bool ok = true;
+            for (int st = 0; st < nst && ok; ++st) {
+                const int s = st % kNB;
+                if (st >= kNB)
+                    ok = mbar_wait(&bar_empty_b[s], uint32_t((st / kNB - 1) & 1));
+                if (!ok)
+                    break;
+                const int nb = cnb - st * kTcKs < kTcKs ? cnb - st * kTcKs : kTcKs;
+                mbar_expect_tx(&bar_full_b[s], uint32_t(nb * kBlockB));
+                const uint32_t stage = smem_u32(s_b + s * kStageB);
+                for (int j = 0; j < nb; ++j) {
+                    const int kcol = (cb0 + st * kTcKs + j) * kTileK;
+#pragma unroll
+                    for (int kg = 0; kg < 4; ++kg) // K group kg: columns kcol + 8 kg .. + 7
+                        tma_load_2d(stage + uint32_t(j * kBlockB + kg * NPAD * 16), &tmx, kcol + 8 * kg, 0,
+                                    &bar_full_b[s]);
+                }
+            }
+            if (!ok)
+                atomicOr(&g_tc_status, 1);
+        }
+    } else if (lane == 0) {
+        // ---- issuer (warp 5): one thread drives the tensor cores -----------------
+        bool ok = true;
+        for (int st = 0; st < nst && ok; ++st) {
+            const int sa_ = st % kNA, sb = st % kNB;
+            ok = mbar_wait(&bar_full_a[sa_], uint32_t((st / kNA) & 1)) &&
+                 mbar_wait(&bar_full_b[sb], uint32_t((st / kNB) & 1));
+            if (!ok)
+                break;
+            tc_fence_after();
+            const uint32_t stage = smem_u32(s_b + sb * kStageB);
+            for (int j = 0; j < kTcKs; ++j) {
+                const int i = st * kTcKs + j;
+                if (i >= cnb)
+                    break;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const uint32_t a_t = tbase + uint32_t(kACol + (sa_ * kTcKs + j) * 16 + q * 8);
+                    const uint64_t bd = smem_desc(stage + uint32_t(j * kBlockB + q * kStepB), kLbo, kSbo);
+                    umma_ts(tbase, a_t, bd, kIdesc, uint32_t(i | q));
+                }
+            }
+            umma_commit(&bar_empty_a[sa_]);
+            umma_commit(&bar_empty_b[sb]);
+        }
+        umma_commit(&bar_done);
+        if (!ok)
+            atomicOr(&g_tc_status, 1);
+    }
+
+    // ---- epilogue: D (128 rows x NPAD tokens) from tensor memory -------------
+    float d[NPAD];
+    if (warp < 4) {
+        if (!mbar_wait(&bar_done, 0) && lane == 0)
+            atomicOr(&g_tc_status, 2);
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < NPAD / 16; ++c)
+            tm_load16(tbase + (uint32_t(32 * warp) << 16) + uint32_t(16 * c), d + 16 * c);
+        tm_wait_ld();
+    }
+    if (a.splits == 1) {
+        pdl_wait(); // every global write comes after the previous kernel
+        const int row = row0 + 32 * warp + lane;
+        if (warp < 4 && row < a.n) {
+            const float sc = kFp8 ? __ldg(a.scale + row) : 1.0f;
+#pragma unroll
+            for (int tok = 0; tok < NPAD; ++tok)
+                if (tok < a.m)
+                    a.y[int64_t(tok) * a.ldy + row] = to_bf16(kFp8 ? sc * d[tok] : d[tok]);
+        }
+    } else {
+        // Split K across the CTAs of a cluster (rank = split): each CTA parks
+        // its partial tile in its own shared memory (the weight stages are
+        // free: every step has completed), then rank r adds the splits of rows
+        // [r R, (r+1) R) in split order, reading the others' tiles directly.
+        float *red = reinterpret_cast<float *>(s_w);
+        if (warp < 4) {
+            float4 *dst = reinterpret_cast<float4 *>(red + (32 * warp + lane) * kRedPitch);
+#pragma unroll
+            for (int q = 0; q < NPAD / 4; ++q)
+                dst[q] = make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
+        }
+        __syncwarp(); // the cluster barrier is warp-aligned: reconverge first
+        asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+        pdl_wait();
+        const int rows_per = 128 / a.splits; // splits divides 128 (a power of two <= 8)
+        const int items = rows_per * (NPAD / 4);
+        const uint32_t red_local = smem_u32(red);
+        for (int it = threadIdx.x; it < items; it += kTcThreads) {
+            const int q = it / rows_per;           // token quad
+            const int rl = sp * rows_per + (it - q * rows_per);
+            const int row = row0 + rl;
+            if (4 * q >= a.m || row >= a.n)
+                continue;
+            const uint32_t off = uint32_t((rl * kRedPitch + 4 * q) * 4);
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int r = 0; r < a.splits; ++r) {
+                uint32_t remote;
+                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(red_local + off), "r"(r));
+                float4 p;
+                asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+                             : "=f"(p.x), "=f"(p.y), "=f"(p.z), "=f"(p.w)
+                             : "r"(remote)
+                             : "memory");
+                v.x += p.x;
+                v.y += p.y;
+                v.z += p.z;
+                v.w += p.w;
+            }
+            const float sc = kFp8 ? __ldg(a.scale + row) : 1.0f;
+            const float out[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (4 * q + e < a.m)
+                    a.y[int64_t(4 * q + e) * a.ldy + row] = to_bf16(kFp8 ? sc * out[e] : out[e]);
+        }
+        // no CTA leaves while another may still read its tile
+        __syncwarp();
+        asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    }
+
+    // ---- release tensor memory -------------------------------------------------
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+template <bool kFp8>
+void *tc_instance(int npad)
+{
+    switch (npad) {
+    case 16: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 16>);
+    case 32: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 32>);
+    case 48: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 48>);
+    case 64: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 64>);
+    default: return nullptr;
+    }
+}
+
+} // namespace
+
+cudaError_t prepare_tc_kernels()
+{
+    for (int npad = 16; npad <= 64; npad += 16) {
+        for (int f = 0; f < 2; ++f) {
+            void *fn = f ? tc_instance<true>(npad) : tc_instance<false>(npad);
+            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 tc_smem_bytes(f == 1, npad));
+            if (e != cudaSuccess)
+                return e;
+        }
+    }
+    return cudaSuccess;
+}
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// The activations x [m][ldx] bf16 as a 2-D tensor (K columns, m rows) read in
+// 8-column x npad-row boxes; outside K or m the boxes are zero.
+bool encode_x_map(CUtensorMap *map, const GemvArgs &a, int npad)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[2] = {cuuint64_t(a.k), cuuint64_t(a.m)};
+    const cuuint64_t strides[1] = {cuuint64_t(a.ldx) * 2};
+    const cuuint32_t box[2] = {8, cuuint32_t(npad)};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(a.x), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+} // namespace
+
+cudaError_t launch_tc(bool fp8, const Plan &plan, const GemvArgs &a, cudaStream_t s)
+{
+    void *fn = fp8 ? tc_instance<true>(plan.npad) : tc_instance<false>(plan.npad);
+    if (!fn)
+        return cudaErrorInvalidValue;
+    alignas(64) CUtensorMap tmx;
+    if (!encode_x_map(&tmx, a, plan.npad))
+        return cudaErrorInvalidValue;
+    void *args[] = {const_cast<GemvArgs *>(&a), &tmx};
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(unsigned(plan.grid));
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = size_t(tc_smem_bytes(fp8, plan.npad));
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    // the splits of a row block form one cluster (they exchange partial tiles)
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = unsigned(plan.splits);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = plan.splits > 1 ? 2 : 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+cudaError_t tc_status(int *out, bool reset)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_tc_status, sizeof(int));
+    if (e == cudaSuccess && reset) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_tc_status, &zero, sizeof(int));
+    }
+    return e;
+}
+
+} // namespace w8

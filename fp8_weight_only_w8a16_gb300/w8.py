@@ -55,7 +55,7 @@ class PlaneInfo(ctypes.Structure):
 
 
 class PlanInfo(ctypes.Structure):
-    _fields_ = [("grid", ctypes.c_int32), ("block", ctypes.c_int32),
+    _fields_ = [("kernel", ctypes.c_int32), ("grid", ctypes.c_int32), ("block", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int32), ("n_tiles", ctypes.c_int32),
                 ("row_tiles_per_warp", ctypes.c_int32), ("warps_k", ctypes.c_int32),
                 ("depth", ctypes.c_int32), ("row_groups", ctypes.c_int32),
@@ -101,6 +101,8 @@ def _load():
     lib.w8_gemv_noalloc.restype = st
     lib.w8_packed_offset.argtypes = [i32, i64, i64, i64]
     lib.w8_packed_offset.restype = i64
+    lib.w8_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), i32]
+    lib.w8_device_status.restype = st
     return lib
 
 
@@ -109,7 +111,8 @@ lib = _load()
 # every symbol include/w8.h declares
 EXPORTS = ("w8_status_str", "w8_abi_version", "w8_validate", "w8_packed_bytes", "w8_bind",
            "w8_release", "w8_build_planes", "w8_build_info", "w8_plan_info", "w8_plan_shape",
-           "w8_workspace_bytes", "w8_gemv", "bf16_gemv", "w8_gemv_noalloc", "w8_packed_offset")
+           "w8_workspace_bytes", "w8_gemv", "bf16_gemv", "w8_gemv_noalloc", "w8_packed_offset",
+           "w8_device_status")
 
 
 def _check(status: int):
@@ -290,6 +293,14 @@ def w8_gemv_noalloc(build: Build, plane: int, x: torch.Tensor, y: torch.Tensor,
                                m, ctypes.c_void_p(y.data_ptr()), y.stride(0),
                                _stream_ptr(stream)))
     return y
+
+
+def device_status(reset: bool = False) -> int:
+    """The tensor-memory kernel's status word on the current device (0: every
+    bounded wait ended normally).  Synchronous."""
+    out = ctypes.c_int(0)
+    _check(lib.w8_device_status(ctypes.byref(out), 1 if reset else 0))
+    return int(out.value)
 
 
 def packed_offset(dtype: int, k_blocks: int, row: int, col: int) -> int:

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define W8_ABI_VERSION 1
+#define W8_ABI_VERSION 2
 
 /* A cudaStream_t: the runtime's stream type is this same pointer type. */
 typedef struct CUstream_st *w8_stream;
@@ -119,8 +119,13 @@ typedef struct {
     size_t packed_bytes;     /* bytes of the packed weights */
 } w8_plane_info;
 
-/* The launch a gemv call makes for one (plane, m); returned for inspection. */
+/* The launch a gemv call makes for one (plane, m); returned for inspection.
+ * kernel 0 (m <= 8): the register-ring kernel, 8 warps per CTA.
+ * kernel 1 (m >= 9): the tensor-memory kernel, 128 rows x one K range per CTA;
+ *   there n_tiles = tokens rounded up to 16, over 8; row_tiles_per_warp = the
+ *   CTA's 8 row tiles; warps_k = 1; depth = the converter warps' ring depth. */
 typedef struct {
+    int32_t kernel;          /* 0: register ring (mma.sync), 1: tensor memory (tcgen05) */
     int32_t grid;            /* CTAs */
     int32_t block;           /* threads per CTA */
     int32_t smem_bytes;      /* dynamic shared memory per CTA */
@@ -131,12 +136,21 @@ typedef struct {
                                 the FP8 depth; bf16 rings hold fewer, larger blocks;
                                 the depth never changes a summation order) */
     int32_t row_groups;      /* CTAs along N */
-    int32_t splits;          /* CTAs along K; > 1 means a workspace is needed */
+    int32_t splits;          /* CTAs along K (kernel 1: the CTAs of one cluster, which add
+                                their partial sums on chip and need no workspace) */
     int32_t k_blocks_per_warp_max; /* most 32-column K blocks one warp streams */
-    size_t workspace_bytes;  /* 0 when splits == 1 */
+    size_t workspace_bytes;  /* 0 unless a kernel-0 plan splits K */
 } w8_plan;
 
 typedef struct w8_build w8_build; /* opaque, host-side, library-owned */
+
+/* The tensor-memory kernel's status word on the current device: 0 when every
+ * wait of every launch so far ended normally; bit 0 = a pipeline-stage wait
+ * gave up, bit 1 = the accumulator wait gave up (each wait polls a bounded
+ * number of times, then the kernel runs to its end with that output wrong and
+ * flags it here).  Synchronous (reads device memory); reset != 0 clears it.
+ * No counterpart on the pages: it reports this library's own safety bound. */
+w8_status w8_device_status(int *status, int reset);
 
 /* Text for a status code (static storage; never NULL). */
 const char *w8_status_str(w8_status s);
@@ -221,7 +235,7 @@ w8_status bf16_gemv(const w8_build *b, int plane, const uint16_t *x, int64_t ldx
  * w8_gemv asks for when a plan splits K across CTAs.
  *
  * Same arguments and result as w8_gemv without the workspace: the scratch
- * comes from a fixed array of W8_NOALLOC_SCRATCH_BYTES (256 KiB) inside the
+ * comes from a fixed array of W8_NOALLOC_SCRATCH_BYTES (32 KiB) inside the
  * library, which every GPU that loads the library holds until the process
  * exits.  A call whose plan needs more (w8_plan_info's workspace_bytes)
  * returns W8_ERR_SCRATCH before any launch.  It allocates nothing: no
@@ -235,7 +249,7 @@ w8_status bf16_gemv(const w8_build *b, int plane, const uint16_t *x, int64_t ldx
  * GPU (different streams without ordering between them) race and must not be
  * made; calls on one stream are fine.  Returns W8_ERR_DTYPE on a bf16 build.
  * One kernel launch on s. */
-#define W8_NOALLOC_SCRATCH_BYTES (256u << 10)
+#define W8_NOALLOC_SCRATCH_BYTES (32u << 10)
 w8_status w8_gemv_noalloc(const w8_build *b, int plane, const uint16_t *x, int64_t ldx, int m,
                           uint16_t *y, int64_t ldy, w8_stream s);
 

@@ -42,7 +42,7 @@ def test_every_declared_function_is_exported():
 
 
 def test_abi_version_and_status_strings():
-    assert w8.lib.w8_abi_version() == 1
+    assert w8.lib.w8_abi_version() == 2
     for code in range(15):
         assert w8.status_str(code)
     assert w8.status_str(99) == "unknown status"
@@ -156,6 +156,21 @@ def test_plan_invariants(n, k, m):
     kb = -(-k // 32)
     rt = -(-n // 16)
     assert p.grid == p.row_groups * p.splits
+    assert p.kernel == (1 if m >= 17 and -(-n // 128) >= 48 else 0)
+    if p.kernel == 1:
+        # the tensor-memory kernel: 128 rows x one K range per CTA, tokens
+        # padded to 16, about two CTAs per SM, at least one 4-block stage per split
+        assert p.kernel == 1 and p.block == 224
+        assert p.row_groups == -(-n // 128) and p.n_tiles * 8 == -(-m // 16) * 16
+        assert p.splits in (1, 2, 4, 8) and (p.splits == 1 or kb // p.splits >= 4)
+        assert p.grid <= 2 * 152 or p.splits == 1
+        assert p.k_blocks_per_warp_max == -(-kb // p.splits)
+        npad = p.n_tiles * 8
+        nw, nb = {16: (5, 6), 32: (4, 5), 48: (4, 3), 64: (3, 3)}[npad]  # FP8 stage slots
+        assert p.smem_bytes == nw * 8 * 4 * 512 + nb * 4 * npad * 64 <= 104 * 1024
+        assert p.workspace_bytes == 0  # split partials meet on chip
+        return
+    assert p.block == 256
     assert p.warps_k in (1, 2, 4, 8) and p.depth >= 1
     assert 1 <= p.splits <= kb
     tiles_per_cta = (8 // p.warps_k) * p.row_tiles_per_warp

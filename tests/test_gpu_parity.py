@@ -106,8 +106,9 @@ def test_repack_matches_host_address_map(w8, dtype, n, k, ldw):
 # random inputs within tolerance
 # ---------------------------------------------------------------------------
 
+# (6200, 700) has 49 row blocks of 128: from 17 tokens on, the tensor-memory kernel
 SHAPES = [(256, 512), (100, 200), (37, 77), (1, 1), (16, 32), (513, 1000), (130, 2100),
-          (48, 4096), (2624, 640)]
+          (48, 4096), (2624, 640), (6200, 700)]
 MS = [1, 2, 3, 5, 8, 9, 16, 17, 31, 33, 64]
 
 
@@ -136,7 +137,8 @@ def _exact_sum_case(rng, n, k, m, e_lo=5, e_hi=10):
     return synth.Plane("e4m3fn", n, k, k, codes, scale), x
 
 
-@pytest.mark.parametrize("n,k", [(16, 32), (64, 2048), (300, 700), (2624, 256), (40, 6144)])
+@pytest.mark.parametrize("n,k", [(16, 32), (64, 2048), (300, 700), (2624, 256), (40, 6144),
+                                 (6144, 256)])
 @pytest.mark.parametrize("m", [1, 5, 16, 33, 64])
 def test_exact_sum_inputs_bit_exact(w8, n, k, m):
     rng = np.random.default_rng(n * 7 + k + m)
@@ -198,25 +200,27 @@ def test_unit_scale_fp8_equals_bf16_path(w8, n, k, m):
 
 
 @pytest.mark.parametrize("j", [-4, 5])
-def test_power_of_two_scale_commutes(w8, j):
-    plane, x_all = _case(77, 300, 3000, 8)
-    x = np.ascontiguousarray(x_all[:8])
+@pytest.mark.parametrize("n,k,m", [(300, 3000, 8), (6144, 1000, 40)])
+def test_power_of_two_scale_commutes(w8, j, n, k, m):
+    plane, x_all = _case(77, n, k, m)
+    x = np.ascontiguousarray(x_all[:m])
     b1, _s1 = bind_plane(w8, plane)
-    y1 = run_gemv(w8, b1, 0, x, 300)
-    plane2 = synth.Plane("e4m3fn", 300, 3000, plane.ldw, plane.w,
+    y1 = run_gemv(w8, b1, 0, x, n)
+    plane2 = synth.Plane("e4m3fn", n, k, plane.ldw, plane.w,
                          (plane.scale * np.float32(2.0 ** j)).astype(np.float32))
     b2, _s2 = bind_plane(w8, plane2)
-    y2 = run_gemv(w8, b2, 0, x, 300)
+    y2 = run_gemv(w8, b2, 0, x, n)
     assert np.array_equal(oracle.bf16_bits_to_f64(y2), oracle.bf16_bits_to_f64(y1) * 2.0 ** j)
 
 
-def test_nan_code_poisons_its_row(w8):
-    plane, x_all = _case(78, 50, 500, 4)
+@pytest.mark.parametrize("n,k,m", [(50, 500, 4), (6144, 500, 20)])
+def test_nan_code_poisons_its_row(w8, n, k, m):
+    plane, x_all = _case(78, n, k, m)
     plane.w[7, 123] = 0x7F
     plane.w[40, 499] = 0xFF
-    x = np.ascontiguousarray(x_all[:4])
+    x = np.ascontiguousarray(x_all[:m])
     b, _src = bind_plane(w8, plane)
-    y = run_gemv(w8, b, 0, x, 50)
+    y = run_gemv(w8, b, 0, x, n)
     v = oracle.bf16_bits_to_f64(y)
     assert np.all(np.isnan(v[:, [7, 40]]))
     assert not np.any(np.isnan(np.delete(v, [7, 40], axis=1)))
@@ -295,18 +299,19 @@ def test_zero_tokens_is_a_no_op(w8):
 
 
 def test_workspace_reuse_graph_replay_and_errors(w8):
-    plane, x_all = _case(44, 128, 6144, 16)
-    x = np.ascontiguousarray(x_all[:16])
+    # m = 8: the register-ring kernel, whose split-K plans use the workspace
+    plane, x_all = _case(44, 128, 6144, 8)
+    x = np.ascontiguousarray(x_all[:8])
     b, _src = bind_plane(w8, plane)
-    assert b.plan(0, 16).splits > 1
-    ws = b.new_workspace(0, 16)
+    assert b.plan(0, 8).kernel == 0 and b.plan(0, 8).splits > 1
+    ws = b.new_workspace(0, 8)
     y1 = run_gemv(w8, b, 0, x, 128, ws=ws)
     y2 = run_gemv(w8, b, 0, x, 128, ws=ws)
     assert np.array_equal(y1, y2)
     _check_tol(plane, x, y1)
     # CUDA-graph capture and replay of the same call
     xd = to_dev(x)
-    yd = torch.zeros((16, 128), dtype=torch.int16, device=dev())
+    yd = torch.zeros((8, 128), dtype=torch.int16, device=dev())
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         w8.w8_gemv(b, 0, xd, yd, ws, stream=s)
@@ -320,7 +325,7 @@ def test_workspace_reuse_graph_replay_and_errors(w8):
     torch.cuda.synchronize()
     assert np.array_equal(from_dev(yd), y1)
     # error returns
-    yd2 = torch.zeros((16, 128), dtype=torch.int16, device=dev())
+    yd2 = torch.zeros((8, 128), dtype=torch.int16, device=dev())
     for kw, name in [(dict(workspace=None), "W8_ERR_NULL"),
                      (dict(workspace=ws[:256]), "W8_ERR_CAPACITY"),
                      (dict(workspace=ws[8:]), "W8_ERR_ALIGN")]:
@@ -338,10 +343,45 @@ def test_workspace_reuse_graph_replay_and_errors(w8):
         w8.w8_gemv(b, 0, big, torch.zeros((65, 128), dtype=torch.int16, device=dev()), ws)
     assert e.value.name == "W8_ERR_SHAPE"
     with pytest.raises(w8.W8Error) as e:   # output row stride shorter than N
-        w8.w8_gemv(b, 0, xd, torch.zeros((16, 100), dtype=torch.int16, device=dev()), ws)
+        w8.w8_gemv(b, 0, xd, torch.zeros((8, 100), dtype=torch.int16, device=dev()), ws)
     assert e.value.name == "W8_ERR_SHAPE"
     torch.cuda.synchronize()
     assert torch.all(yd2 == 0)  # no refused call wrote anything
+
+
+@pytest.mark.parametrize("n,k,m", [(6144, 2048, 32), (6200, 1000, 17), (7000, 512, 64),
+                                   (28672, 512, 64)])
+def test_tensor_memory_kernel_clusters_and_graph_replay(w8, n, k, m):
+    """Planes of >= 48 row blocks with >= 17 tokens run the tensor-memory
+    kernel; with split K its CTAs form a cluster and add their partial tiles on
+    chip.  Repeated calls and a
+    CUDA-graph replay give identical bits, within tolerance, and every bounded
+    wait of the kernel ended normally (device status 0)."""
+    plane, x_all = _case(45, n, k, m)
+    x = np.ascontiguousarray(x_all[:m])
+    b, _src = bind_plane(w8, plane)
+    p = b.plan(0, m)
+    assert p.kernel == 1 and p.workspace_bytes == 0
+    w8.device_status(reset=True)
+    y1 = run_gemv(w8, b, 0, x, n)
+    y2 = run_gemv(w8, b, 0, x, n)
+    assert np.array_equal(y1, y2)
+    _check_tol(plane, x, y1)
+    xd = to_dev(x)
+    yd = torch.zeros((m, n), dtype=torch.int16, device=dev())
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        w8.w8_gemv(b, 0, xd, yd, None, stream=s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        w8.w8_gemv(b, 0, xd, yd, None)
+    yd.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(from_dev(yd), y1)
+    assert w8.device_status() == 0
 
 
 def test_bind_refusals_on_device(w8):

@@ -27,7 +27,7 @@ from .gpu_util import bind_plane, dev, from_dev, to_dev
 
 pytestmark = pytest.mark.gpu
 
-LIMIT = 256 << 10  # W8_NOALLOC_SCRATCH_BYTES
+LIMIT = 32 << 10  # W8_NOALLOC_SCRATCH_BYTES
 
 
 @pytest.fixture(scope="module")
@@ -39,9 +39,10 @@ def w8():
     return lib
 
 
-# (n, k, m): plans that split K across CTAs (and so use the scratch) and a
-# large plane whose plan does not
-CASES = [(128, 6144, 16), (32, 6144, 32), (40, 6144, 5), (2624, 6144, 4)]
+# (n, k, m): register-ring plans that split K across CTAs (and so use the
+# scratch), a tensor-memory plan (its split partials meet on chip: no scratch)
+# and a large plane whose plan does not split
+CASES = [(128, 2048, 16), (32, 6144, 12), (40, 6144, 5), (6144, 1024, 32), (2624, 6144, 4)]
 
 
 @pytest.mark.parametrize("n,k,m", CASES)
@@ -51,8 +52,8 @@ def test_noalloc_equals_gemv_with_workspace(w8, n, k, m):
     x = synth.activations(rng, k, m)
     b, _src = bind_plane(w8, plane)
     needs_scratch = b.plan(0, m).splits > 1
-    if (n, k) in ((128, 6144), (32, 6144)):
-        assert needs_scratch
+    if (n, k) in ((128, 2048), (32, 6144), (40, 6144)):
+        assert needs_scratch and b.workspace_bytes(0, m) > 0
     assert b.workspace_bytes(0, m) <= LIMIT
 
     xd = to_dev(x)
@@ -76,7 +77,7 @@ def test_noalloc_refuses_what_it_cannot_serve(w8):
     # a plan whose split partials exceed the fixed scratch (the first such
     # shape for this GPU's SM count)
     sms = torch.cuda.get_device_properties(dev()).multi_processor_count
-    cands = [(n, k, 64) for n in (16, 32, 64, 128, 256, 512, 1024) for k in (6144, 16384)]
+    cands = [(n, k, 8) for n in (16, 32, 64, 128, 256, 512, 1024) for k in (6144, 16384)]
     over = [c for c in cands if w8.plan_shape(*c, sms).workspace_bytes > LIMIT]
     assert over, "no candidate shape needs more than the fixed scratch"
     n, k, m = over[0]
