@@ -155,7 +155,7 @@ inline int64_t plan_ctas(int64_t rt, int r, int wk, int splits)
 // (activations reused over two tiles), then the longest K parts.  Every warp keeps at least kMinBlocks
 // K blocks when K allows it.  K is split across CTAs only for planes whose
 // row tiles leave most SMs idle.
-// The tensor-memory kernel (w8_tc.cu): CTAs of 128 rows x a K range, seven
+// The tensor-memory kernel (w8_tc.cu): CTAs of 128 rows x a K range, eleven
 // warps, 2 CTAs per SM (256 tensor-memory columns and about 100 KB of shared
 // memory each).  K is split across the CTAs of a cluster (up to 8) until about
 // two CTAs per SM are busy, keeping at least one stage of K blocks per split;
@@ -164,7 +164,7 @@ constexpr int kTcMinM = 17;       // decode tokens from which the tc kernel may 
 constexpr int kTcMinRowBlocks = 48; // ... on planes of at least this many 128-row blocks
 constexpr int kTcStageBlocks = 4; // K blocks per stage of the tc kernel
 constexpr int kTcCtasPerSm = 2;
-constexpr int kTcThreadsPerCta = 224;
+constexpr int kTcThreadsPerCta = 352;
 
 // Stage slots of the tensor-memory kernel in shared memory: nw weight stages
 // (8 row tiles x 4 K blocks of packed runs, filled by bulk copies) and nb

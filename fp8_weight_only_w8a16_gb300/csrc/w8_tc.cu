@@ -10,28 +10,29 @@
 // memory serves 128 weight rows instead of 16.
 //
 // One CTA = 128 output rows (8 row tiles of the packed layout) x one range of
-// K blocks, seven warps:
-//   warp 6 (weights): one thread copies the CTA's packed runs into shared
+// K blocks, eleven warps:
+//   warp 10 (weights): one thread copies the CTA's packed runs into shared
 //     memory with bulk asynchronous copies (one per row tile and stage of 4 K
 //     blocks: a tile's runs are contiguous), filling every weight stage
 //     before the dependency wait -- the plane is bind-time data;
-//   warps 0-3 (converters): warp q reads row tiles 2q and 2q+1 of each stage
-//     from shared memory, widens E4M3 to bf16 exactly (bf16 planes pass
-//     through) and stores the A operand into tensor memory, TMEM lanes
-//     32q..32q+31, in natural K order (below);
-//   warp 4 (activations): after the dependency wait, one thread copies the
+//   warps 0-7 (converters): warp w reads row tile 2 (w % 4) + w / 4 of each
+//     stage from shared memory, widens E4M3 to bf16 exactly (bf16 planes pass
+//     through) and stores the stage's A operand into tensor memory with one
+//     tcgen05.st (TMEM lanes 32 (w % 4) + 16 (w / 4) .., the lane quarter warp
+//     w may reach), in natural K order (below);
+//   warp 8 (activations): after the dependency wait, one thread copies the
 //     activation tiles with tensor-map bulk copies (TMA): one 8-column x
 //     tokens box per K group, landing as the 8-row x 16-byte core matrices
 //     of the tensor cores' K-major layout; rows past the tokens and columns
 //     past K arrive as zeros;
-//   warp 5 (issuer): one thread issues the tensor-core steps
+//   warp 9 (issuer): one thread issues the tensor-core steps
 //     D[128 x NPAD] += A[128 x 16] (TMEM) * B[16 x NPAD] (shared memory) and
 //     commits them to the stages' "empty" barriers.
 // Weight, A and activation stages rotate through their slots with mbarriers
 // ("full": the producers arrive or the copies complete; "empty": the
 // consumers arrive or the issuer commits).  After the last step the
-// accumulator D (TMEM columns [0, NPAD)) is read by the converter warps, one
-// row per thread: scale, round, store.  With K split across CTAs, the splits
+// accumulator D (TMEM columns [0, NPAD)) is read by warps 0-3, one row per
+// thread: scale, round, store.  With K split across CTAs, the splits
 // of a row block form a thread-block cluster: each CTA parks its partial tile
 // in its shared memory and rank r adds rows [r R, (r+1) R) of all the tiles
 // in split order through distributed shared memory.
@@ -67,8 +68,9 @@ namespace {
 
 constexpr int kTcKs = 4;         // K blocks per stage
 constexpr int kTcStages = 3;     // stage slots
-constexpr int kTcThreads = kTcThreadsPerCta; // 4 converters, activations, issuer, weights
-static_assert(kTcThreads == 224, "seven warps");
+constexpr int kTcThreads = kTcThreadsPerCta; // 8 converters, activations, issuer, weights
+static_assert(kTcThreads == 352, "eleven warps");
+constexpr int kWarpAct = 8, kWarpIssue = 9, kWarpW = 10;
 static_assert(kTcKs == kTcStageBlocks, "the planner's stage size");
 constexpr int kTmemCols = 256;   // D: [0, 64); A stages: [64, 256)
 constexpr int kACol = 64;
@@ -204,10 +206,24 @@ __device__ __forceinline__ void tm_store_a(uint32_t taddr, const uint32_t (&r)[8
                  : "memory");
 }
 
+// The A operand of a whole stage (4 blocks = 64 columns) for 16 rows:
+// tcgen05.st 16x256b.x8, registers 8j..8j+7 = block j in tm_store_a's order.
+__device__ __forceinline__ void tm_store_stage(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.st.sync.aligned.16x256b.x8.b32 [%0], "
+                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+                 "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+                 "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+                 "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+                 "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+                 : "memory");
+}
+
 // Units t and t+4 of rows g and g+8 of one staged run (see "K order") as the
 // eight A registers of lane (g, t).
 template <bool kFp8>
-__device__ __forceinline__ void a_units(uint32_t (&r)[8], uint32_t run, int g, int t)
+__device__ __forceinline__ void a_units(uint32_t *r, uint32_t run, int g, int t)
 {
     if constexpr (kFp8) {
         // 8 bytes = words (row g, g+8 at cols +0,+1), (row g, g+8 at cols +2,+3)
@@ -283,10 +299,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kNW; ++s) {
             mbar_init(&bar_full_w[s], 1);
-            mbar_init(&bar_empty_w[s], 4);
+            mbar_init(&bar_empty_w[s], 8);
         }
         for (int s = 0; s < kNA; ++s) {
-            mbar_init(&bar_full_a[s], 4);
+            mbar_init(&bar_full_a[s], 8);
             mbar_init(&bar_empty_a[s], 1);
         }
         for (int s = 0; s < kNB; ++s) {
@@ -309,35 +325,39 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     const uint32_t tbase = s_tmem;
     pdl_launch_dependents();
 
-    if (warp == 6) {
+    if (warp == kWarpW) {
         // ---- weights: packed runs -> shared memory (bulk copies) --------------
         // The packed plane is written only by w8_bind, which finishes before any
-        // GEMV is launched, so this runs ahead of the dependency wait.
-        if (lane == 0) {
-            bool ok = true;
-            for (int st = 0; st < nst && ok; ++st) {
-                const int s = st % kNW;
-                if (st >= kNW)
-                    ok = mbar_wait(&bar_empty_w[s], uint32_t((st / kNW - 1) & 1));
-                if (!ok)
-                    break;
-                const int nb = cnb - st * kTcKs < kTcKs ? cnb - st * kTcKs : kTcKs;
-                int tiles = a.rt - tile0;
-                tiles = tiles > 8 ? 8 : tiles;
-                mbar_expect_tx(&bar_full_w[s], uint32_t(tiles * nb * kRun));
-                const uint32_t dst = smem_u32(s_w + s * kStageW);
-                for (int h = 0; h < tiles; ++h)
-                    bulk_copy(dst + uint32_t(h * kTileW),
-                              a.wp + (int64_t(tile0 + h) * a.kb + cb0 + st * kTcKs) * kRun,
-                              uint32_t(nb * kRun), &bar_full_w[s]);
-            }
+        // GEMV is launched, so this runs ahead of the dependency wait.  Lane h
+        // copies row tile h's runs of the stage (the copies go out in parallel).
+        int tiles = a.rt - tile0;
+        tiles = tiles > 8 ? 8 : tiles;
+        bool ok = true;
+        for (int st = 0; st < nst && ok; ++st) {
+            const int s = st % kNW;
+            if (st >= kNW)
+                ok = __all_sync(0xffffffffu, mbar_wait(&bar_empty_w[s], uint32_t((st / kNW - 1) & 1)));
             if (!ok)
-                atomicOr(&g_tc_status, 1);
+                break;
+            const int nb = cnb - st * kTcKs < kTcKs ? cnb - st * kTcKs : kTcKs;
+            if (lane == 0)
+                mbar_expect_tx(&bar_full_w[s], uint32_t(tiles * nb * kRun));
+            __syncwarp();
+            if (lane < tiles)
+                bulk_copy(smem_u32(s_w + s * kStageW + lane * kTileW),
+                          a.wp + (int64_t(tile0 + lane) * a.kb + cb0 + st * kTcKs) * kRun,
+                          uint32_t(nb * kRun), &bar_full_w[s]);
         }
-    } else if (warp < 4) {
+        if (!ok && lane == 0)
+            atomicOr(&g_tc_status, 1);
+    } else if (warp < 8) {
         // ---- converters: staged weights -> widened A in tensor memory ---------
-        const uint32_t ok0 = tile0 + 2 * warp < a.rt, ok1 = tile0 + 2 * warp + 1 < a.rt;
-        const uint32_t lanes = uint32_t(32 * warp) << 16;
+        // warp w widens row tile 2 (w % 4) + w / 4 into TMEM lanes
+        // 32 (w % 4) + 16 (w / 4) .. + 15 (a warp reaches lane quarter w % 4).
+        const int h = 2 * (warp & 3) + (warp >> 2);
+        const uint32_t okt = tile0 + h < a.rt;
+        const uint32_t lanes = uint32_t(32 * (warp & 3) + 16 * (warp >> 2)) << 16;
+        const int g = lane >> 2, t = lane & 3;
         bool ok = true;
         for (int st = 0; st < nst && ok; ++st) {
             const int sw = st % kNW, sa_ = st % kNA;
@@ -346,60 +366,55 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 ok = __all_sync(0xffffffffu, mbar_wait(&bar_empty_a[sa_], uint32_t((st / kNA - 1) & 1)));
             if (!ok)
                 break;
-            const uint32_t w0 = smem_u32(s_w + sw * kStageW + (2 * warp) * kTileW);
-            const uint32_t w1 = w0 + kTileW;
+            const uint32_t w0 = smem_u32(s_w + sw * kStageW + h * kTileW);
             const int nb = cnb - st * kTcKs < kTcKs ? cnb - st * kTcKs : kTcKs;
-            const int g = lane >> 2, t = lane & 3;
+            uint32_t r[32];
 #pragma unroll
             for (int j = 0; j < kTcKs; ++j) {
-                if (j >= nb)
-                    break;
-                uint32_t r0[8] = {0, 0, 0, 0, 0, 0, 0, 0}, r1[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                if (ok0)
-                    a_units<kFp8>(r0, w0 + j * kRun, g, t);
-                if (ok1)
-                    a_units<kFp8>(r1, w1 + j * kRun, g, t);
-                const uint32_t col = uint32_t(kACol + (sa_ * kTcKs + j) * 16);
-                tm_store_a(tbase + lanes + col, r0);
-                tm_store_a(tbase + lanes + (16u << 16) + col, r1);
+                if (okt && j < nb) {
+                    a_units<kFp8>(r + 8 * j, w0 + j * kRun, g, t);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        r[8 * j + e] = 0; // blocks past the stage's end are never read
+                }
             }
+            tm_store_stage(tbase + lanes + uint32_t(kACol + sa_ * kTcKs * 16), r);
             tm_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&bar_empty_w[sw]); // the stage's weights are in registers/TMEM
+                mbar_arrive(&bar_empty_w[sw]); // the stage's weights are in TMEM now
                 mbar_arrive(&bar_full_a[sa_]);
             }
         }
         if (!ok && lane == 0)
             atomicOr(&g_tc_status, 1);
-    } else if (warp == 4) {
+    } else if (warp == kWarpAct) {
         // ---- activations: x -> B tiles in shared memory (tensor-map copies) -----
+        // Lane 4j + g copies K group g of block j of the stage (16 copies in
+        // parallel), each an 8-column x NPAD-row box.
         pdl_wait(); // x may be the previous kernel's output
-        if (lane == 0) {
-            bool ok = true;
-            for (int st = 0; st < nst && ok; ++st) {
-                const int s = st % kNB;
-                if (st >= kNB)
-                    ok = mbar_wait(&bar_empty_b[s], uint32_t((st / kNB - 1) & 1));
-                if (!ok)
-                    break;
-                const int nb = cnb - st * kTcKs < kTcKs ? cnb - st * kTcKs : kTcKs;
-                mbar_expect_tx(&bar_full_b[s], uint32_t(nb * kBlockB));
-                const uint32_t stage = smem_u32(s_b + s * kStageB);
-                for (int j = 0; j < nb; ++j) {
-                    const int kcol = (cb0 + st * kTcKs + j) * kTileK;
-#pragma unroll
-                    for (int kg = 0; kg < 4; ++kg) // K group kg: columns kcol + 8 kg .. + 7
-                        tma_load_2d(stage + uint32_t(j * kBlockB + kg * NPAD * 16), &tmx, kcol + 8 * kg, 0,
-                                    &bar_full_b[s]);
-                }
-            }
+        bool ok = true;
+        for (int st = 0; st < nst && ok; ++st) {
+            const int s = st % kNB;
+            if (st >= kNB)
+                ok = __all_sync(0xffffffffu, mbar_wait(&bar_empty_b[s], uint32_t((st / kNB - 1) & 1)));
             if (!ok)
-                atomicOr(&g_tc_status, 1);
+                break;
+            const int nb = cnb - st * kTcKs < kTcKs ? cnb - st * kTcKs : kTcKs;
+            if (lane == 0)
+                mbar_expect_tx(&bar_full_b[s], uint32_t(nb * kBlockB));
+            __syncwarp();
+            const int j = lane >> 2, kg = lane & 3;
+            if (j < nb)
+                tma_load_2d(smem_u32(s_b + s * kStageB + j * kBlockB + kg * NPAD * 16), &tmx,
+                            (cb0 + st * kTcKs + j) * kTileK + 8 * kg, 0, &bar_full_b[s]);
         }
-    } else if (lane == 0) {
-        // ---- issuer (warp 5): one thread drives the tensor cores -----------------
+        if (!ok && lane == 0)
+            atomicOr(&g_tc_status, 1);
+    } else if (warp == kWarpIssue && lane == 0) {
+        // ---- issuer: one thread drives the tensor cores --------------------------
         bool ok = true;
         for (int st = 0; st < nst && ok; ++st) {
             const int sa_ = st % kNA, sb = st % kNB;
@@ -429,25 +444,30 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     }
 
     // ---- epilogue: D (128 rows x NPAD tokens) from tensor memory -------------
-    float d[NPAD];
+    // Warps 0-3 read their lane quarter, 16 token columns at a time.
     if (warp < 4) {
         if (!mbar_wait(&bar_done, 0) && lane == 0)
             atomicOr(&g_tc_status, 2);
         tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < NPAD / 16; ++c)
-            tm_load16(tbase + (uint32_t(32 * warp) << 16) + uint32_t(16 * c), d + 16 * c);
-        tm_wait_ld();
     }
+    const int row = row0 + 32 * warp + lane;
+    const uint32_t dq = tbase + (uint32_t(32 * (warp & 3)) << 16);
     if (a.splits == 1) {
         pdl_wait(); // every global write comes after the previous kernel
-        const int row = row0 + 32 * warp + lane;
-        if (warp < 4 && row < a.n) {
-            const float sc = kFp8 ? __ldg(a.scale + row) : 1.0f;
+        if (warp < 4) {
+            const float sc = (kFp8 && row < a.n) ? __ldg(a.scale + row) : 1.0f;
 #pragma unroll
-            for (int tok = 0; tok < NPAD; ++tok)
-                if (tok < a.m)
-                    a.y[int64_t(tok) * a.ldy + row] = to_bf16(kFp8 ? sc * d[tok] : d[tok]);
+            for (int c = 0; c < NPAD / 16; ++c) {
+                float d[16];
+                tm_load16(dq + uint32_t(16 * c), d);
+                tm_wait_ld();
+                if (row < a.n) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        if (16 * c + e < a.m)
+                            a.y[int64_t(16 * c + e) * a.ldy + row] = to_bf16(kFp8 ? sc * d[e] : d[e]);
+                }
+            }
         }
     } else {
         // Split K across the CTAs of a cluster (rank = split): each CTA parks
@@ -458,8 +478,14 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         if (warp < 4) {
             float4 *dst = reinterpret_cast<float4 *>(red + (32 * warp + lane) * kRedPitch);
 #pragma unroll
-            for (int q = 0; q < NPAD / 4; ++q)
-                dst[q] = make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
+            for (int c = 0; c < NPAD / 16; ++c) {
+                float d[16];
+                tm_load16(dq + uint32_t(16 * c), d);
+                tm_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    dst[4 * c + q] = make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
+            }
         }
         __syncwarp(); // the cluster barrier is warp-aligned: reconverge first
         asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -470,30 +496,40 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         for (int it = threadIdx.x; it < items; it += kTcThreads) {
             const int q = it / rows_per;           // token quad
             const int rl = sp * rows_per + (it - q * rows_per);
-            const int row = row0 + rl;
-            if (4 * q >= a.m || row >= a.n)
+            const int orow = row0 + rl;
+            if (4 * q >= a.m || orow >= a.n)
                 continue;
-            const uint32_t off = uint32_t((rl * kRedPitch + 4 * q) * 4);
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int r = 0; r < a.splits; ++r) {
-                uint32_t remote;
-                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(red_local + off), "r"(r));
-                float4 p;
-                asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-                             : "=f"(p.x), "=f"(p.y), "=f"(p.z), "=f"(p.w)
-                             : "r"(remote)
-                             : "memory");
-                v.x += p.x;
-                v.y += p.y;
-                v.z += p.z;
-                v.w += p.w;
+            const uint32_t off = red_local + uint32_t((rl * kRedPitch + 4 * q) * 4);
+            // all remote loads first (independent), then the sum in split order
+            float4 p[kTcMaxSplits];
+#pragma unroll
+            for (int r = 0; r < kTcMaxSplits; ++r) {
+                p[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (r < a.splits) {
+                    uint32_t remote;
+                    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(off), "r"(r));
+                    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+                                 : "=f"(p[r].x), "=f"(p[r].y), "=f"(p[r].z), "=f"(p[r].w)
+                                 : "r"(remote)
+                                 : "memory");
+                }
             }
-            const float sc = kFp8 ? __ldg(a.scale + row) : 1.0f;
+            float4 v = p[0];
+#pragma unroll
+            for (int r = 1; r < kTcMaxSplits; ++r) {
+                if (r < a.splits) {
+                    v.x += p[r].x;
+                    v.y += p[r].y;
+                    v.z += p[r].z;
+                    v.w += p[r].w;
+                }
+            }
+            const float sc = kFp8 ? __ldg(a.scale + orow) : 1.0f;
             const float out[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e)
                 if (4 * q + e < a.m)
-                    a.y[int64_t(4 * q + e) * a.ldy + row] = to_bf16(kFp8 ? sc * out[e] : out[e]);
+                    a.y[int64_t(4 * q + e) * a.ldy + orow] = to_bf16(kFp8 ? sc * out[e] : out[e]);
         }
         // no CTA leaves while another may still read its tile
         __syncwarp();

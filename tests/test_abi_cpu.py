@@ -160,7 +160,7 @@ def test_plan_invariants(n, k, m):
     if p.kernel == 1:
         # the tensor-memory kernel: 128 rows x one K range per CTA, tokens
         # padded to 16, about two CTAs per SM, at least one 4-block stage per split
-        assert p.kernel == 1 and p.block == 224
+        assert p.kernel == 1 and p.block == 352
         assert p.row_groups == -(-n // 128) and p.n_tiles * 8 == -(-m // 16) * 16
         assert p.splits in (1, 2, 4, 8) and (p.splits == 1 or kb // p.splits >= 4)
         assert p.grid <= 2 * 152 or p.splits == 1
