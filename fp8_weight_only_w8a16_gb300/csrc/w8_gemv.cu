@@ -142,11 +142,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
     // Weights first: the packed plane is written only by w8_bind, which
     // finishes before any GEMV can be launched, so these loads may overlap the
     // tail of the previous kernel on the stream.  The ring holds blocks
-    // [0, DW); blocks up to kPf go to L2 now, and every ring group sends the
-    // kPf-distant group after it (bulk prefetches: no registers, no waits).
+    // [0, DW); for FP8 planes, blocks up to kPf go to L2 now, and every ring
+    // group sends the kPf-distant group after it (bulk prefetches: no
+    // registers, no waits).  bf16 planes skip it: twice the bytes ahead
+    // crowded L2 on the largest planes (lm_head, o_proj bf16) and cost time.
     // Lane 0 issues them, so its wptr is the start of the warp's runs.
-    constexpr int kPf = DW > 16 ? DW : 16;
-    if (lane == 0 && nmain > DW) {
+    constexpr int kPf = kFp8 ? (DW > 16 ? DW : 16) : DW;
+    if (kPf > DW && lane == 0 && nmain > DW) {
         const int hi = nmain < kPf ? nmain : kPf;
         if (hi > DW)
 #pragma unroll
@@ -198,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
     // further on.
     int b = 0;
     for (; b + DW <= nmain; b += DW) {
-        if (lane == 0 && b + kPf < nmain) {
+        if (kPf > DW && lane == 0 && b + kPf < nmain) {
             const int hi = b + kPf + DW < nmain ? b + kPf + DW : nmain;
 #pragma unroll
             for (int r = 0; r < R; ++r)
