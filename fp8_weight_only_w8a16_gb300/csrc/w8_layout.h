@@ -115,15 +115,17 @@ W8_HD int nt_for_m(int m) { return m <= 8 ? 1 : m <= 16 ? 2 : m <= 32 ? 4 : 8; }
 // planner picks per shape.  The depths are the only dtype-dependent choice --
 // a bf16 block takes twice the registers of an FP8 block, so its ring holds
 // about half the blocks and the same bytes -- and no depth changes a
-// summation order.  Activations come from L2/L1, so their ring can be
-// shallower than the HBM weight ring.
+// summation order.  Activations come from L2/L1; with one token group their
+// ring is as deep as, or half, the weight ring: the ring refills wait an L2
+// round trip, so the ring's depth, not the bandwidth, sets the pace there
+// (measured: depths 16/8 -> 12/6 took fused_qkv_a_proj from 5.8 to 5.4 us).
 struct Inst {
     int nt, r, occ;
     int dw_fp8, dx_fp8, dw_bf16, dx_bf16;
 };
 constexpr int kNumInst = 10;
 constexpr Inst kInst[kNumInst] = {
-    {1, 1, 2, 16, 8, 8, 4}, {1, 2, 2, 8, 4, 4, 2}, {1, 1, 3, 8, 4, 4, 2}, {1, 2, 3, 4, 2, 2, 2},
+    {1, 1, 2, 12, 6, 8, 4}, {1, 2, 2, 6, 6, 4, 2}, {1, 1, 3, 6, 6, 4, 2}, {1, 2, 3, 4, 4, 2, 2},
     {2, 1, 2, 10, 5, 6, 3}, {2, 2, 2, 6, 3, 2, 2},
     {4, 1, 2, 6, 2, 4, 2},  {4, 2, 1, 8, 4, 4, 2},
     {8, 1, 1, 6, 2, 4, 2},  {8, 2, 1, 6, 2, 4, 2},
