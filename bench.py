@@ -312,6 +312,36 @@ def e2e_rate(b: GemvBench, steps, torch):
             "us_per_step": dt / steps * 1e6, "steps": steps}
 
 
+def slowest_time_ms(dist, t_ms: float, device="cpu") -> float:
+    """The whole job's timed region: the slowest rank's (max over ranks; with
+    dist None, one GPU, it passes through)."""
+    if dist is None:
+        return t_ms
+    import torch
+
+    t = torch.tensor([t_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(dist, rate: float, device="cpu") -> float:
+    """Whole-job rate of N independent replicas: the slowest rank's rate times
+    the number of ranks (with dist None it passes through)."""
+    if dist is None:
+        return rate
+    import torch
+
+    t = torch.tensor([rate], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MIN)
+    return float(t.item()) * dist.get_world_size()
+
+
+def job_value(world: int, step_bytes: int, steps: int, t_ms: float) -> float:
+    """GB/s of the whole job: every rank's algorithmic bytes over the slowest
+    rank's time (weak scaling: each replica streams the same workload)."""
+    return world * step_bytes * steps / (t_ms * 1e-3) / 1e9
+
+
 def run_ours(args):
     import torch
 
@@ -352,14 +382,9 @@ def run_ours(args):
     barrier()
     time.sleep(0.25)
     clocks = sampler.stop()
-    t_ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([t_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_ms = float(t.item())
-
+    t_ms = slowest_time_ms(dist, e0.elapsed_time(e1), device)
     step_bytes = b.step_bytes()
-    value = world * step_bytes * args.steps / (t_ms * 1e-3) / 1e9
+    value = job_value(world, step_bytes, args.steps, t_ms)
 
     # per-batch microseconds and the kernel roofline
     per_m = {}
@@ -385,10 +410,7 @@ def run_ours(args):
                 "alg_bytes_per_launch": {str(m): proj.algorithmic_bytes(m) for m in ms}}
 
     e2e = e2e_rate(b, min(args.steps, args.e2e_steps), torch)
-    if dist is not None:
-        t = torch.tensor([e2e["value"]], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MIN)
-        e2e["value"] = float(t.item()) * world
+    e2e["value"] = job_rate(dist, e2e["value"], device)
 
     line = None
     if rank == 0:
