@@ -56,9 +56,13 @@ WQ_B = Projection("indexer_wq_b", 4096, 2048, "e4m3fn", SWEEP_M)
 WK = Projection("indexer_wk", 128, 6144, "bf16", SWEEP_M)
 WEIGHTS_PROJ = Projection("indexer_weights_proj", 32, 6144, "bf16", SWEEP_M)
 LM_HEAD = Projection("lm_head", 154880, 6144, "bf16", (1,))
+# The indexer's wk and weights_proj read the same token rows (hidden states,
+# K = 6144), so their bf16 planes bind as one [160, 6144] plane: one call
+# instead of two, rows 0..127 = wk, 128..159 = weights_proj.
+WK_WEIGHTS_PROJ = Projection("indexer_wk_weights_proj", 160, 6144, "bf16", SWEEP_M)
 
 ALL = (TINY, FUSED_QKV_A, O_PROJ, O_PROJ_BF16, SHARED_GATE_UP, SHARED_DOWN,
-       SHARED_GATE_UP_KPAD, Q_B, KV_B, WQ_B, WK, WEIGHTS_PROJ, LM_HEAD)
+       SHARED_GATE_UP_KPAD, Q_B, KV_B, WQ_B, WK, WEIGHTS_PROJ, WK_WEIGHTS_PROJ, LM_HEAD)
 BY_NAME = {p.name: p for p in ALL}
 
 # The five workload groups, in order: the tiny correctness case, the fused
@@ -69,5 +73,5 @@ GROUPS = {
     "fused_qkv_a_proj": (FUSED_QKV_A,),
     "o_proj": (O_PROJ, O_PROJ_BF16),
     "shared_expert": (SHARED_GATE_UP, SHARED_DOWN, SHARED_GATE_UP_KPAD),
-    "layer_sweep": (Q_B, KV_B, WQ_B, WK, WEIGHTS_PROJ, LM_HEAD),
+    "layer_sweep": (Q_B, KV_B, WQ_B, WK, WEIGHTS_PROJ, WK_WEIGHTS_PROJ, LM_HEAD),
 }
