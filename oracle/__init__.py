@@ -10,10 +10,14 @@ accumulation, one fp32 scale multiply, one bf16 round to nearest even), which
 follows ATOM pull request #2980, sections Summary and
 Changes: the E4M3 plane widens exactly to bf16 and the fp32 row scale
 multiplies each reduced row before the bf16 rounding.  ``brute.py`` is an
-independent numpy fp64 recompute used to pin it.
+independent numpy fp64 recompute used to pin it.  It also holds the MLP
+activation that follows a merged gate_up projection (ATOM Model Support
+Guide, Model architecture details, Llama MLP): h = silu(g) * u in fp64 with
+one bf16 rounding.
 
 Every function here is pinned by a ``-m "not gpu"`` test
-(tests/test_oracle_codecs.py, tests/test_oracle_gemv.py).
+(tests/test_oracle_codecs.py, tests/test_oracle_gemv.py,
+tests/test_oracle_silu.py).
 """
 from __future__ import annotations
 
@@ -59,6 +63,10 @@ def _declare(lib):
     lib.orc_gemv_f64.restype = ctypes.c_int
     lib.orc_max_threads.argtypes = []
     lib.orc_max_threads.restype = ctypes.c_int
+    lib.orc_f64_to_bf16_rne.argtypes = [ctypes.c_double]
+    lib.orc_f64_to_bf16_rne.restype = ctypes.c_uint16
+    lib.orc_silu_mul_f64.argtypes = [vp, vp, c_i64, vp]
+    lib.orc_silu_mul_f64.restype = ctypes.c_int
     return lib
 
 
@@ -157,6 +165,46 @@ class Oracle:
             raise ValueError("orc_gemv_f64 rejected its arguments")
         return y64, mag
 
+    # ---- SiLU-and-multiply of a merged gate_up plane -------------------
+    def f64_to_bf16_rne(self, values) -> np.ndarray:
+        """fp64 values -> bf16 bit patterns (uint16), one round to nearest even."""
+        v = np.ascontiguousarray(values, dtype=np.float64).ravel()
+        out = np.empty(v.shape, dtype=np.uint16)
+        f = self.lib.orc_f64_to_bf16_rne
+        for i, x in enumerate(v):
+            out[i] = f(ctypes.c_double(x))
+        return out.reshape(np.shape(values))
+
+    def silu_mul_f64(self, g, u) -> np.ndarray:
+        """h = silu(g) * u elementwise in fp64 (unrounded); g and u broadcast."""
+        g, u = np.broadcast_arrays(np.asarray(g, dtype=np.float64),
+                                   np.asarray(u, dtype=np.float64))
+        g = np.ascontiguousarray(g)
+        u = np.ascontiguousarray(u)
+        h = np.empty(g.shape, dtype=np.float64)
+        if self.lib.orc_silu_mul_f64(_ptr(g), _ptr(u), g.size, _ptr(h)) != 0:
+            raise ValueError("orc_silu_mul_f64 rejected its arguments")
+        return h
+
+    def silu_mul(self, g_bits: np.ndarray, u_bits: np.ndarray) -> np.ndarray:
+        """bf16(silu(g) * u) from bf16 g and u: fp64 inside, one bf16 rounding."""
+        h = self.silu_mul_f64(bf16_bits_to_f64(g_bits), bf16_bits_to_f64(u_bits))
+        return self.f64_to_bf16_rne(h)
+
+    def gate_up_silu_mul(self, w: np.ndarray, dtype: int, scale: np.ndarray | None,
+                         x: np.ndarray, k: int | None = None, threads: int = 1) -> np.ndarray:
+        """The merged gate_up projection followed by SiLU-and-multiply.
+
+        ``w`` is the merged [2I, >=k] plane (rows 0..I-1 gate, I..2I-1 up),
+        ``scale`` its [2I] row scales (FP8).  The projection is the GEMV
+        above (its bf16 outputs g and u); returns bf16 bits [m, I] of
+        silu(g) * u.
+        """
+        n = w.shape[0]
+        assert n % 2 == 0
+        y = self.gemv(w, dtype, scale, x, k, threads)
+        return self.silu_mul(y[:, : n // 2], y[:, n // 2:])
+
     def max_threads(self) -> int:
         return int(self.lib.orc_max_threads())
 
@@ -214,6 +262,22 @@ def max_threads():
     return _load().max_threads()
 
 
+def f64_to_bf16_rne(values):
+    return _load().f64_to_bf16_rne(values)
+
+
+def silu_mul_f64(g, u):
+    return _load().silu_mul_f64(g, u)
+
+
+def silu_mul(g_bits, u_bits):
+    return _load().silu_mul(g_bits, u_bits)
+
+
+def gate_up_silu_mul(w, dtype, scale, x, k=None, threads=1):
+    return _load().gate_up_silu_mul(w, dtype, scale, x, k, threads)
+
+
 # --------------------------------------------------------------------------
 # the tolerance of the parity tests
 # --------------------------------------------------------------------------
@@ -244,6 +308,46 @@ def within_tolerance(y_bits: np.ndarray, y64: np.ndarray, mag64: np.ndarray):
     return bool(worst <= 1.0), worst
 
 
+# sup |silu'(v)| over the reals (attained near v = 2.40: 1.0998...); the
+# tolerance below uses it as the Lipschitz constant of silu, and a CPU test
+# checks it on a fine grid.
+SILU_LIPSCHITZ = 1.1
+
+
+def silu_mul_within_tolerance(h_bits: np.ndarray, g64: np.ndarray, mag_g: np.ndarray,
+                              u64: np.ndarray, mag_u: np.ndarray):
+    """Parity bound for h = bf16(silu(g) * u) computed from GEMV outputs g, u.
+
+    g64 / u64 are the fp64 recomputes of the two projections and mag_g /
+    mag_u their absolute sums (gemv_f64).  The GEMV's own bound gives
+    |g - g64| <= Eg = 2^-7 |g64| + 2^-12 mag_g (and Eu for u).  Then
+
+      |silu(g) u - silu(g64) u64| <= L Eg (|u64| + Eu) + |silu(g64)| Eu =: D
+
+    with L = SILU_LIPSCHITZ, and the fp32 evaluation (a few fp32 roundings,
+    2^-20 relative) plus the final bf16 rounding (2^-8 relative) add
+    (2^-8 + 2^-20)(|H| + D), H = silu(g64) u64.  A floor of
+    2^-120 (|u64| + Eu + 1) covers fp32 underflow of silu at very negative
+    g.  NaN must match NaN.  Returns (ok, worst ratio |err| / bound).
+    """
+    h = bf16_bits_to_f64(h_bits)
+    big_h = silu_mul_f64(g64, u64)
+    s = np.abs(silu_mul_f64(g64, 1.0))
+    eg = 2.0 ** -7 * np.abs(g64) + 2.0 ** -12 * mag_g
+    eu = 2.0 ** -7 * np.abs(u64) + 2.0 ** -12 * mag_u
+    d = SILU_LIPSCHITZ * eg * (np.abs(u64) + eu) + s * eu
+    nan_ref = np.isnan(big_h)
+    if not np.array_equal(nan_ref, np.isnan(h)):
+        return False, float("inf")
+    fin = ~nan_ref
+    bound = (d + (2.0 ** -8 + 2.0 ** -20) * (np.abs(big_h) + d)
+             + 2.0 ** -120 * (np.abs(u64) + eu + 1.0))[fin]
+    err = np.abs(h[fin] - big_h[fin])
+    ratio = err / bound
+    worst = float(ratio.max()) if ratio.size else 0.0
+    return bool(worst <= 1.0), worst
+
+
 def same_values(a_bits: np.ndarray, b_bits: np.ndarray) -> bool:
     """Bit-for-bit equality of bf16 results, with +0 == -0 and NaN == NaN.
 
@@ -268,4 +372,6 @@ __all__ = [
     "DT_E4M3FN", "DT_BF16", "Oracle", "load_variant", "e4m3_to_f32", "bf16_to_f32",
     "f32_to_bf16_rne", "f32_to_e4m3_sat", "quantize_rows", "gemv", "gemv_f64",
     "max_threads", "bf16_bits_to_f64", "within_tolerance", "same_values", "build_oracle",
+    "f64_to_bf16_rne", "silu_mul_f64", "silu_mul", "gate_up_silu_mul", "SILU_LIPSCHITZ",
+    "silu_mul_within_tolerance",
 ]

@@ -28,7 +28,10 @@
  * itself: the 256 codes against their closed-form values and against
  * torch.float8_e4m3fn, bf16 rounding against torch.bfloat16, the GEMV against
  * a numpy fp64 matmul on tiny inputs, one-hot and exact-sum inputs against
- * exact rational results, and power-of-two scale invariance.
+ * exact rational results, and power-of-two scale invariance; the SiLU-and-
+ * multiply against torch's float64 silu, the odd-part identity
+ * silu(v) - silu(-v) = v and its limits, and the one-step fp64 -> bf16
+ * rounding against the fp32 rounding and on exact bf16 midpoints.
  */
 #include <math.h>
 #include <stdint.h>
@@ -241,4 +244,61 @@ int orc_max_threads(void)
 #else
     return 1;
 #endif
+}
+
+/* ------------------------------------------------------------------ */
+/* SiLU-and-multiply of a merged gate_up projection                    */
+/* ------------------------------------------------------------------ */
+
+/* fp64 -> bf16, round to nearest, ties to even, in one step (no detour
+ * through fp32, whose own rounding could move a value onto a bf16 midpoint).
+ * bf16 keeps 8 significant bits with fp32's exponent range: a value in
+ * [2^(e-1), 2^e) has spacing 2^(e-8), and below 2^-126 the spacing stays
+ * 2^-133 (subnormals).  Dividing by that spacing is exact, nearbyint rounds
+ * to the nearest integer with ties to even (the default rounding mode), and
+ * a result of 2^128 or more is infinity.  NaN stays NaN (quiet, sign kept). */
+uint16_t orc_f64_to_bf16_rne(double v)
+{
+    if (isnan(v))
+        return (uint16_t)(signbit(v) ? 0xFFC0u : 0x7FC0u);
+    double a = fabs(v);
+    uint16_t sign = signbit(v) ? 0x8000u : 0x0000u;
+    if (a == 0.0)
+        return sign;
+    if (isinf(a) || a >= ldexp(1.0, 128))
+        return (uint16_t)(sign | 0x7F80u);
+    int e;
+    frexp(a, &e); /* a = f * 2^e, f in [0.5, 1) */
+    if (e < -125)
+        e = -125;
+    double q = ldexp(1.0, e - 8);
+    double r = nearbyint(a / q) * q;
+    if (r >= ldexp(1.0, 128))
+        return (uint16_t)(sign | 0x7F80u);
+    float f = (float)r; /* exact: r has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | (u >> 16));
+}
+
+/* The MLP activation between a merged gate_up projection and the down
+ * projection (ATOM Model Support Guide, Model architecture details, Llama:
+ * one merged column-parallel projection for gate and up, then SiLU and
+ * multiply, then down; Adding a new model, Step 5: gate_proj is shard 0 and
+ * up_proj shard 1 of gate_up_proj):
+ *
+ *     h = silu(g) * u,   silu(v) = v * sigmoid(v) = v / (1 + exp(-v))
+ *
+ * elementwise over `count` pairs, in fp64, unrounded.  g and u are the values
+ * the projection produced (the GEMV's bf16 outputs, widened by the caller).
+ * At v = -inf the quotient is -inf / inf = NaN, as the formula gives. */
+int orc_silu_mul_f64(const double *g, const double *u, int64_t count, double *h)
+{
+    if (!g || !u || !h || count < 0)
+        return -1;
+    for (int64_t i = 0; i < count; ++i) {
+        double s = g[i] / (1.0 + exp(-g[i]));
+        h[i] = s * u[i];
+    }
+    return 0;
 }

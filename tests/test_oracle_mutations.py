@@ -19,6 +19,7 @@ from oracle.build import ORACLE_SRC, build_oracle
 
 from . import test_oracle_codecs as codecs
 from . import test_oracle_gemv as gemv_pins
+from . import test_oracle_silu as silu_pins
 
 MUTATIONS = {
     "scale_dropped": ("float t = (dtype == ORC_DT_E4M3FN) ? scale[r] * acc : acc;",
@@ -45,6 +46,17 @@ MUTATIONS = {
     "bf16_widening_shift_wrong": ("(uint32_t)u << 16;", "(uint32_t)u << 15;"),
     "accumulate_in_bf16": ("acc = acc + p;",
                            "acc = orc_bf16_to_f32(orc_f32_to_bf16_rne(acc + p));"),
+    # SiLU-and-multiply and its one-step fp64 -> bf16 rounding
+    "silu_exponent_sign": ("double s = g[i] / (1.0 + exp(-g[i]));",
+                           "double s = g[i] / (1.0 + exp(g[i]));"),
+    "silu_of_up_not_gate": ("double s = g[i] / (1.0 + exp(-g[i]));\n        h[i] = s * u[i];",
+                            "double s = u[i] / (1.0 + exp(-u[i]));\n        h[i] = s * g[i];"),
+    "silu_multiply_dropped": ("h[i] = s * u[i];", "h[i] = s;"),
+    "f64_rounding_through_fp32": ("double r = nearbyint(a / q) * q;",
+                                  "double r = (double)orc_bf16_to_f32(orc_f32_to_bf16_rne("
+                                  "(float)a));"),
+    "f64_rounding_ties_away": ("nearbyint(a / q)", "round(a / q)"),
+    "f64_subnormal_spacing": ("if (e < -125)\n        e = -125;", "if (e < -126)\n        e = -126;"),
 }
 
 # pins rerun against each mutated copy (test functions that take the oracle)
@@ -59,6 +71,12 @@ PINS = [
     lambda o: gemv_pins.test_scale_multiplies_the_reduced_row_once(o),
     lambda o: gemv_pins.test_gemv_against_fp64_brute_force(o, True, 2, 33, 64, 16),
     lambda o: gemv_pins.test_gemv_against_fp64_brute_force(o, False, 5, 40, 63, 9),
+    lambda o: silu_pins.test_f64_rounding_agrees_with_fp32_rounding_on_fp32_values(o),
+    lambda o: silu_pins.test_f64_rounding_on_exact_midpoints(o),
+    lambda o: silu_pins.test_silu_mul_matches_torch_float64_silu(o),
+    lambda o: silu_pins.test_silu_closed_forms_and_limits(o),
+    lambda o: silu_pins.test_silu_odd_part_identity(o),
+    lambda o: silu_pins.test_gate_up_silu_mul_is_nearest_bf16_of_exact_result(o),
 ]
 
 
