@@ -180,16 +180,19 @@ class GemvBench:
         w_d = torch.from_numpy(plane.w).to(device)
         s_d = torch.from_numpy(plane.scale).to(device) if plane.scale is not None else None
         dt = w8.DT_E4M3FN if self.fp8 else w8.DT_BF16
-        src = w8.Plane.from_tensor(w_d, s_d, k=proj.k, dtype=dt)
+        silu = proj.act == "silu_mul"
+        src = w8.Plane.from_tensor(w_d, s_d, k=proj.k, dtype=dt,
+                                   layout=w8.SRC_GATE_UP if silu else w8.SRC_ROW_MAJOR)
         self.build = w8.bind([src] * copies)
         torch.cuda.synchronize()
         del w_d, s_d, src
         mmax = max(self.ms)
         self.x_host = np.ascontiguousarray(x_all[:mmax])
         self.x = torch.from_numpy(self.x_host.view(np.int16)).to(device)
-        self.y = {m: torch.zeros((m, proj.n), dtype=torch.int16, device=device) for m in self.ms}
+        self.y = {m: torch.zeros((m, proj.out_n), dtype=torch.int16, device=device)
+                  for m in self.ms}
         self.ws = self.build.new_workspace()
-        self.fn = w8.w8_gemv if self.fp8 else w8.bf16_gemv
+        self.fn = (w8.w8_gemv_silu_mul if silu else w8.w8_gemv if self.fp8 else w8.bf16_gemv)
 
     def step_bytes(self):
         return sum(self.proj.algorithmic_bytes(m) for m in self.ms)
@@ -291,7 +294,7 @@ def e2e_rate(b: GemvBench, steps, torch):
     a CUDA graph and replayed; the host waits for every step."""
     mmax = max(b.ms)
     x_pin = torch.from_numpy(b.x_host.view(np.int16)).pin_memory()
-    y_pin = {m: torch.empty((m, b.proj.n), dtype=torch.int16).pin_memory() for m in b.ms}
+    y_pin = {m: torch.empty((m, b.proj.out_n), dtype=torch.int16).pin_memory() for m in b.ms}
 
     def body(j):
         b.x.copy_(x_pin, non_blocking=True)
@@ -326,7 +329,7 @@ def e2e_rate(b: GemvBench, steps, torch):
         one(j)
     dt = time.perf_counter() - t0
     h2d = mmax * b.proj.k * 2
-    d2h = sum(m * b.proj.n * 2 for m in b.ms)
+    d2h = sum(m * b.proj.out_n * 2 for m in b.ms)
     return {"value": b.step_bytes() * steps / dt / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "us_per_step": dt / steps * 1e6, "steps": steps}
@@ -574,11 +577,13 @@ def run_one(args):
     w_d = torch.from_numpy(plane.w).to(device)
     s_d = torch.from_numpy(plane.scale).to(device) if plane.scale is not None else None
     dt = w8.DT_E4M3FN if proj.dtype == "e4m3fn" else w8.DT_BF16
-    b = w8.bind([w8.Plane.from_tensor(w_d, s_d, k=proj.k, dtype=dt)])
+    silu = proj.act == "silu_mul"
+    b = w8.bind([w8.Plane.from_tensor(w_d, s_d, k=proj.k, dtype=dt,
+                                      layout=w8.SRC_GATE_UP if silu else w8.SRC_ROW_MAJOR)])
     ws = b.new_workspace()
     x = torch.from_numpy(np.ascontiguousarray(x_all[:m]).view(np.int16)).to(device)
-    y = torch.zeros((m, proj.n), dtype=torch.int16, device=device)
-    fn = w8.w8_gemv if dt == w8.DT_E4M3FN else w8.bf16_gemv
+    y = torch.zeros((m, proj.out_n), dtype=torch.int16, device=device)
+    fn = (w8.w8_gemv_silu_mul if silu else w8.w8_gemv if dt == w8.DT_E4M3FN else w8.bf16_gemv)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # 2 x L2
     for _ in range(args.calls):
         flush.zero_()

@@ -32,13 +32,15 @@ w8_status check_plane(const w8_plane_desc &d)
         return W8_ERR_NULL;
     if (d.dtype != W8_DT_E4M3FN && d.dtype != W8_DT_BF16)
         return W8_ERR_DTYPE;
-    if (d.layout != W8_SRC_ROW_MAJOR)
+    if (d.layout != W8_SRC_ROW_MAJOR && d.layout != W8_SRC_GATE_UP)
         return W8_ERR_LAYOUT;
     if (d.bias)
         return W8_ERR_BIAS;
     if (d.n < 1 || d.k < 1 || d.n > kMaxDim || d.k > kMaxDim || d.ldw < d.k ||
         d.ldw > 4 * kMaxDim)
         return W8_ERR_SHAPE;
+    if (d.layout == W8_SRC_GATE_UP && d.n % (2 * 8) != 0)
+        return W8_ERR_SHAPE; // I = n / 2 gate rows, a multiple of 8
     if (d.dtype == W8_DT_E4M3FN && !d.scale)
         return W8_ERR_SCALE;
     if (d.dtype == W8_DT_BF16 && d.scale)
@@ -61,24 +63,27 @@ size_t plane_scale_bytes(int32_t dtype, int64_t n)
     return size_t(w8::ceil_div(n, w8::kTileN)) * w8::kTileN * sizeof(float);
 }
 
-w8_status gemv_common(const w8_build *b, int plane, int32_t want_dtype, const uint16_t *x,
-                      int64_t ldx, int m, uint16_t *y, int64_t ldy, void *ws, size_t ws_bytes,
-                      w8_stream s)
+// want_dtype 0: either dtype (SiLU-and-multiply serves both).
+w8_status gemv_common(const w8_build *b, int plane, int32_t want_dtype, bool silu,
+                      const uint16_t *x, int64_t ldx, int m, uint16_t *y, int64_t ldy, void *ws,
+                      size_t ws_bytes, w8_stream s)
 {
     if (!b)
         return W8_ERR_NULL;
     if (plane < 0 || plane >= int(b->planes.size()))
         return W8_ERR_PLANE;
     const w8_plane_info &p = b->planes[size_t(plane)];
-    if (p.dtype != want_dtype)
+    if (want_dtype != 0 && p.dtype != want_dtype)
         return W8_ERR_DTYPE;
+    if (silu && p.layout != W8_LAYOUT_MMA_16x32_GATE_UP)
+        return W8_ERR_LAYOUT;
     if (m < 0 || m > w8::kMaxM)
         return W8_ERR_SHAPE;
     if (m == 0)
         return W8_OK;
     if (!x || !y)
         return W8_ERR_NULL;
-    if (ldx < p.k || ldy < p.n)
+    if (ldx < p.k || ldy < (silu ? p.n / 2 : p.n))
         return W8_ERR_SHAPE;
     if ((reinterpret_cast<uintptr_t>(x) & 15u) || (ldx & 7) || (reinterpret_cast<uintptr_t>(y) & 1u))
         return W8_ERR_ALIGN;
@@ -103,6 +108,7 @@ w8_status gemv_common(const w8_build *b, int plane, int32_t want_dtype, const ui
     a.rt = int(plan.rt);
     a.splits = plan.splits;
     a.wk = plan.wk;
+    w8::set_output_map(a, p, silu);
     if (plan.ws_bytes > 0) { // register-ring split-K plans (tensor-memory plans need none)
         if (!ws)
             return W8_ERR_NULL;
@@ -113,7 +119,7 @@ w8_status gemv_common(const w8_build *b, int plane, int32_t want_dtype, const ui
         a.counters = static_cast<int *>(ws);
         a.partial = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + plan.ws_counters);
     }
-    if (w8::launch_gemv(want_dtype == W8_DT_E4M3FN, plan, a, reinterpret_cast<cudaStream_t>(s)) !=
+    if (w8::launch_gemv(p.dtype == W8_DT_E4M3FN, plan, a, reinterpret_cast<cudaStream_t>(s)) !=
         cudaSuccess)
         return W8_ERR_CUDA;
     return W8_OK;
@@ -134,9 +140,11 @@ const char *w8_status_str(w8_status s)
                                  "multiple of 16 bytes";
     case W8_ERR_BIAS: return "a bias was given; the GEMV has none";
     case W8_ERR_MIXED: return "bf16 and FP8 planes mixed in one build";
-    case W8_ERR_SHAPE: return "bad shape: N, K >= 1, ldw >= K, 0 <= m <= 64, ldx >= K, ldy >= N";
+    case W8_ERR_SHAPE: return "bad shape: N, K >= 1, ldw >= K, 0 <= m <= 64, ldx >= K, ldy >= N "
+                              "(N/2 for SiLU-and-multiply); a gate_up plane needs N % 16 == 0";
     case W8_ERR_SCALE: return "FP8 planes need fp32 row scales; bf16 planes take none";
-    case W8_ERR_LAYOUT: return "unknown source layout (only row-major)";
+    case W8_ERR_LAYOUT: return "unknown source layout (row-major or gate_up), or SiLU-and-multiply "
+                               "on a plane not bound as gate_up";
     case W8_ERR_CAPACITY: return "packed buffer or workspace too small";
     case W8_ERR_ALIGN: return "misaligned buffer (packed/workspace: 256 B; x: 16 B with ldx % 8 == 0; y: 2 B)";
     case W8_ERR_PLANE: return "plane index outside the build";
@@ -225,7 +233,8 @@ w8_status w8_bind(const w8_plane_desc *d, int n_planes, void *dst, size_t dst_by
         const w8_plane_desc &pd = d[i];
         w8_plane_info info{};
         info.dtype = pd.dtype;
-        info.layout = W8_LAYOUT_MMA_16x32;
+        const bool gated = pd.layout == W8_SRC_GATE_UP;
+        info.layout = gated ? W8_LAYOUT_MMA_16x32_GATE_UP : W8_LAYOUT_MMA_16x32;
         info.n = pd.n;
         info.k = pd.k;
         info.row_tiles = w8::ceil_div(pd.n, w8::kTileN);
@@ -251,6 +260,7 @@ w8_status w8_bind(const w8_plane_desc *d, int n_planes, void *dst, size_t dst_by
         ra.dst = static_cast<uint8_t *>(const_cast<void *>(info.packed));
         ra.scale_src = pd.scale;
         ra.scale_dst = scale_copy;
+        ra.half = gated ? pd.n / 2 : 0;
         if (w8::launch_repack(pd.dtype == W8_DT_E4M3FN, ra, reinterpret_cast<cudaStream_t>(s)) !=
             cudaSuccess) {
             delete b;
@@ -348,13 +358,22 @@ w8_status w8_workspace_bytes(const w8_build *b, int plane, int m, size_t *bytes)
 w8_status w8_gemv(const w8_build *b, int plane, const uint16_t *x, int64_t ldx, int m,
                   uint16_t *y, int64_t ldy, void *workspace, size_t workspace_bytes, w8_stream s)
 {
-    return gemv_common(b, plane, W8_DT_E4M3FN, x, ldx, m, y, ldy, workspace, workspace_bytes, s);
+    return gemv_common(b, plane, W8_DT_E4M3FN, false, x, ldx, m, y, ldy, workspace,
+                       workspace_bytes, s);
 }
 
 w8_status bf16_gemv(const w8_build *b, int plane, const uint16_t *x, int64_t ldx, int m,
                     uint16_t *y, int64_t ldy, void *workspace, size_t workspace_bytes, w8_stream s)
 {
-    return gemv_common(b, plane, W8_DT_BF16, x, ldx, m, y, ldy, workspace, workspace_bytes, s);
+    return gemv_common(b, plane, W8_DT_BF16, false, x, ldx, m, y, ldy, workspace,
+                       workspace_bytes, s);
+}
+
+w8_status w8_gemv_silu_mul(const w8_build *b, int plane, const uint16_t *x, int64_t ldx, int m,
+                           uint16_t *y, int64_t ldy, void *workspace, size_t workspace_bytes,
+                           w8_stream s)
+{
+    return gemv_common(b, plane, 0, true, x, ldx, m, y, ldy, workspace, workspace_bytes, s);
 }
 
 int64_t w8_packed_offset(int dtype, int64_t k_blocks, int64_t row, int64_t col)
@@ -366,6 +385,15 @@ int64_t w8_packed_offset(int dtype, int64_t k_blocks, int64_t row, int64_t col)
     if (dtype == W8_DT_BF16)
         return w8::packed_offset_bf16(k_blocks, row, col);
     return -1;
+}
+
+int64_t w8_gate_up_packed_row(int64_t n, int64_t row)
+{
+    if (n < 16 || n % 16 != 0 || row < 0 || row >= n)
+        return -1;
+    const int64_t half = n / 2;
+    // gate row j sits at 16 (j / 8) + j % 8, up row j at 16 (j / 8) + 8 + j % 8
+    return row < half ? 16 * (row / 8) + row % 8 : 16 * ((row - half) / 8) + 8 + (row - half) % 8;
 }
 
 } // extern "C"

@@ -53,6 +53,30 @@ __device__ __forceinline__ uint16_t to_bf16(float f)
     return h;
 }
 
+// The output column of packed row p: p itself on a plain plane; on a gate_up
+// plane (packed tile t = gate rows 8t..8t+7, then up rows 8t..8t+7, of a
+// [2*half, K] merged projection) the source row, which is also the column of
+// SiLU-and-multiply's output for a gate row.
+__device__ __forceinline__ int out_col(int p, bool gated, int half)
+{
+    if (!gated)
+        return p;
+    const int t = p >> 4, i = p & 15;
+    return i < 8 ? 8 * t + i : half + 8 * t + (i - 8);
+}
+
+// SiLU-and-multiply of one gate/up pair, from the scaled fp32 row sums: g
+// and u are rounded to bf16 first (the projection's outputs), then
+// h = bf16(silu(g) * u) with silu(g) = g / (1 + exp(-g)) in fp32 (CUDA's
+// expf and a correctly rounded division: no fast-math in this build).
+__device__ __forceinline__ uint16_t silu_mul_bf16(float g_sum, float u_sum)
+{
+    const float g = __uint_as_float(uint32_t(to_bf16(g_sum)) << 16);
+    const float u = __uint_as_float(uint32_t(to_bf16(u_sum)) << 16);
+    const float s = g / (1.0f + expf(-g));
+    return to_bf16(s * u);
+}
+
 // 4-byte asynchronous copy global -> shared (the CTA's row scales).
 __device__ __forceinline__ void cp_async4(float *smem, const float *gmem)
 {

@@ -24,6 +24,9 @@
 //   3. splits == 1: scale, round, store.  splits > 1: store the fp32 partial,
 //      count arrivals; the last CTA of the row group sums the partials in split
 //      order, scales, rounds and stores.  No CTA ever waits on another.
+// On a gate_up plane the store maps each packed row to its source row; for
+// SiLU-and-multiply, accumulator e of a lane (tile row g, a gate row) meets
+// accumulator e + 2 (row g + 8, its up row) and one bf16 h is stored.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -279,8 +282,20 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
         for (int q = 1; q < wk; ++q)
             v += src[q * R * NT * 128];
         if (a.splits == 1) {
-            if (row < a.n)
-                a.y[int64_t(tok) * a.ldy + row] = to_bf16(kFp8 ? s_scale[row - row0] * v : v);
+            if (row >= a.n)
+                continue;
+            const int64_t at = int64_t(tok) * a.ldy + out_col(row, a.act != kActPlain, a.half);
+            if (a.act != kActSiluMul) {
+                a.y[at] = to_bf16(kFp8 ? s_scale[row - row0] * v : v);
+            } else if (e < 2) {
+                // a gate row: its up row (row + 8) is accumulator e + 2 of this lane
+                const float *su = src + 2 * 32;
+                float vu = su[0];
+                for (int q = 1; q < wk; ++q)
+                    vu += su[q * R * NT * 128];
+                a.y[at] = silu_mul_bf16(kFp8 ? s_scale[row - row0] * v : v,
+                                        kFp8 ? s_scale[row + 8 - row0] * vu : vu);
+            }
         } else {
             a.partial[(int64_t(sp) * rows_pad + row) * a.m + tok] = v;
         }
@@ -307,23 +322,37 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
     const int cnt = (row_end - row0) * a.m; // (row, token) pairs, token fastest
     const float *base = a.partial + int64_t(row0) * a.m;
     const int64_t split_stride = rows_pad * a.m;
-    for (int idx = threadIdx.x; idx < cnt; idx += kThreads) {
+    // the splits of one (row, token) partial, added in split order
+    auto split_sum = [&](int off) {
         float v = 0.0f;
         int s = 0;
         for (; s + 8 <= a.splits; s += 8) {
             float p[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-                p[q] = ld_cg_f32(base + (s + q) * split_stride + idx);
+                p[q] = ld_cg_f32(base + (s + q) * split_stride + off);
 #pragma unroll
             for (int q = 0; q < 8; ++q)
                 v += p[q];
         }
         for (; s < a.splits; ++s)
-            v += ld_cg_f32(base + s * split_stride + idx);
+            v += ld_cg_f32(base + s * split_stride + off);
+        return v;
+    };
+    for (int idx = threadIdx.x; idx < cnt; idx += kThreads) {
         const int row = row0 + idx / a.m;
         const int tok = idx - (idx / a.m) * a.m;
-        a.y[int64_t(tok) * a.ldy + row] = to_bf16(kFp8 ? s_scale[row - row0] * v : v);
+        if (a.act == kActSiluMul && (row & 8))
+            continue; // an up row: added with its gate row (row - 8)
+        const float v = split_sum(idx);
+        const int64_t at = int64_t(tok) * a.ldy + out_col(row, a.act != kActPlain, a.half);
+        if (a.act != kActSiluMul) {
+            a.y[at] = to_bf16(kFp8 ? s_scale[row - row0] * v : v);
+        } else {
+            const float vu = split_sum(idx + 8 * a.m);
+            a.y[at] = silu_mul_bf16(kFp8 ? s_scale[row - row0] * v : v,
+                                    kFp8 ? s_scale[row + 8 - row0] * vu : vu);
+        }
     }
     if (threadIdx.x == 0)
         a.counters[rg] = 0; // ready for the next call on this workspace

@@ -19,6 +19,14 @@ struct w8_build {
 
 namespace w8 {
 
+// What a gemv call writes (GemvArgs::act).  A gate_up plane is a merged
+// [2I, K] projection whose source rows 0..I-1 are the gate and I..2I-1 the
+// up projection; bind interleaves them so that packed 16-row tile t holds
+// gate rows 8t..8t+7 followed by up rows 8t..8t+7.
+constexpr int kActPlain = 0;   // y[:, n] for packed row n (a plain plane)
+constexpr int kActGateUp = 1;  // a gate_up plane's plain GEMV, y in source row order
+constexpr int kActSiluMul = 2; // a gate_up plane: y[:, j] = bf16(silu(g_j) * u_j), j < I
+
 struct GemvArgs {
     const uint8_t *wp;      // packed weights of the plane (device)
     const float *scale;     // the build's row scales (FP8) or nullptr (bf16)
@@ -33,7 +41,18 @@ struct GemvArgs {
     int wk;                 // warps of a tile group along K
     int *counters;          // workspace head (splits > 1)
     float *partial;         // workspace body: [splits][rt*16][m] fp32 (splits > 1)
+    int act;                // kActPlain, kActGateUp or kActSiluMul
+    int half;               // gate_up planes: I = n / 2
 };
+
+// The output mapping of a plane: gate_up planes (bound with W8_SRC_GATE_UP)
+// store in source row order, or apply SiLU-and-multiply when silu is set.
+inline void set_output_map(GemvArgs &a, const w8_plane_info &p, bool silu)
+{
+    const bool gated = p.layout == W8_LAYOUT_MMA_16x32_GATE_UP;
+    a.act = gated ? (silu ? kActSiluMul : kActGateUp) : kActPlain;
+    a.half = gated ? int(p.n / 2) : 0;
+}
 
 // One launch of the GEMV kernel chosen by the plan (FP8 or bf16 weights).
 cudaError_t launch_gemv(bool fp8, const Plan &plan, const GemvArgs &a, cudaStream_t s);
@@ -56,6 +75,9 @@ struct RepackArgs {
     uint8_t *dst;           // packed weights (device)
     const float *scale_src; // FP8: caller's row scales (device)
     float *scale_dst;       // FP8: the build's copy, rt*16 entries (device)
+    int64_t half;           // 0, or I for a gate_up plane (n = 2I, I % 8 == 0):
+                            // packed row 16t+i reads source row 8t+i (i < 8)
+                            // or I + 8t + i - 8 (i >= 8)
 };
 
 cudaError_t launch_repack(bool fp8, const RepackArgs &a, cudaStream_t s);

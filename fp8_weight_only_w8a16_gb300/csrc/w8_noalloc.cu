@@ -103,6 +103,7 @@ extern "C" w8_status w8_gemv_noalloc(const w8_build *b, int plane, const uint16_
     a.rt = int(plan.rt);
     a.splits = plan.splits;
     a.wk = plan.wk;
+    w8::set_output_map(a, p, false);
     if (plan.ws_bytes > 0) {
         void *ws = nullptr;
         const w8_status st = scratch_on(dev, &ws);

@@ -7,6 +7,9 @@
 // 16-byte vector of one K block: it reads 8 consecutive columns of rows g and
 // g+8 of the tile (8- or 16-byte loads; the source rows are 16-byte aligned),
 // zero-fills columns >= K and rows >= N, interleaves them and writes 16 bytes.
+// A gate_up plane (a merged [2I, K] MLP projection) is read with its gate and
+// up rows interleaved eight at a time, so that a tile's rows g and g+8 are a
+// gate row and its up row.
 // FP8 also writes the build's copy of the row scales; a row that holds a NaN
 // code (0x7F or 0xFF) gets a NaN scale, so its outputs are NaN as the
 // definition gives, while the GEMV's widening stays a fixed exact map.
@@ -62,6 +65,16 @@ __device__ __forceinline__ bool has_nan_code(uint2 v)
     return nan != 0;
 }
 
+// The source row of packed row p (a gate_up plane interleaves gate and up
+// rows eight at a time; a plain plane keeps its order).
+__device__ __forceinline__ int64_t src_row(const RepackArgs &a, int64_t p)
+{
+    if (a.half == 0)
+        return p;
+    const int64_t t = p >> 4, i = p & 15;
+    return i < 8 ? 8 * t + i : a.half + 8 * t + (i - 8);
+}
+
 __global__ void __launch_bounds__(256) repack_fp8_kernel(const RepackArgs a)
 {
     __shared__ int nan_row[16];
@@ -79,9 +92,9 @@ __global__ void __launch_bounds__(256) repack_fp8_kernel(const RepackArgs a)
         uint2 lo = make_uint2(0, 0), hi = make_uint2(0, 0);
         const int64_t n0 = rt * kTileN + g, n1 = n0 + 8;
         if (n0 < a.n)
-            lo = load8_fp8(a.src + n0 * a.ld_bytes, col, a.k);
+            lo = load8_fp8(a.src + src_row(a, n0) * a.ld_bytes, col, a.k);
         if (n1 < a.n)
-            hi = load8_fp8(a.src + n1 * a.ld_bytes, col, a.k);
+            hi = load8_fp8(a.src + src_row(a, n1) * a.ld_bytes, col, a.k);
         if (has_nan_code(lo))
             atomicOr(&nan_row[g], 1);
         if (has_nan_code(hi))
@@ -103,7 +116,7 @@ __global__ void __launch_bounds__(256) repack_fp8_kernel(const RepackArgs a)
         const int64_t n = rt * kTileN + threadIdx.x;
         float s = 0.0f;
         if (n < a.n)
-            s = nan_row[threadIdx.x] ? __int_as_float(0x7FC00000) : a.scale_src[n];
+            s = nan_row[threadIdx.x] ? __int_as_float(0x7FC00000) : a.scale_src[src_row(a, n)];
         a.scale_dst[n] = s;
     }
 }
@@ -120,9 +133,11 @@ __global__ void __launch_bounds__(256) repack_bf16_kernel(const RepackArgs a)
         uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
         const int64_t n0 = rt * kTileN + g, n1 = n0 + 8;
         if (n0 < a.n)
-            lo = load8_bf16(reinterpret_cast<const uint16_t *>(a.src + n0 * a.ld_bytes), col, a.k);
+            lo = load8_bf16(reinterpret_cast<const uint16_t *>(a.src + src_row(a, n0) * a.ld_bytes),
+                            col, a.k);
         if (n1 < a.n)
-            hi = load8_bf16(reinterpret_cast<const uint16_t *>(a.src + n1 * a.ld_bytes), col, a.k);
+            hi = load8_bf16(reinterpret_cast<const uint16_t *>(a.src + src_row(a, n1) * a.ld_bytes),
+                            col, a.k);
         // half q: a01 = row g cols 4q+0,1; a23 = row g+8 cols 4q+0,1;
         //         a45 = row g cols 4q+2,3;  a67 = row g+8 cols 4q+2,3
         const uint4 h0 = make_uint4(lo.x, hi.x, lo.y, hi.y);

@@ -35,7 +35,11 @@
 // thread: scale, round, store.  With K split across CTAs, the splits
 // of a row block form a thread-block cluster: each CTA parks its partial tile
 // in its shared memory and rank r adds rows [r R, (r+1) R) of all the tiles
-// in split order through distributed shared memory.
+// in split order through distributed shared memory.  On a gate_up plane
+// (packed tile rows g and g+8 are a gate row and its up row) the store maps
+// each row to its source row; SiLU-and-multiply pairs TMEM lane l with lane
+// l + 8 of the same warp (a shuffle), or row r with row r + 8 of the
+// cluster's tiles, and stores one bf16 h per gate row.
 //
 // K order.  Tensor-core step s of a 32-column block covers columns
 // 16s..16s+15 in order: TMEM column c of the step holds columns 16s+2c,
@@ -254,6 +258,37 @@ __device__ __forceinline__ void a_units(uint32_t *r, uint32_t run, int g, int t)
     }
 }
 
+// The fp32 sums of one row's four tokens over the cluster's splits: every
+// split CTA's tile at the same shared-memory offset, loaded first (all
+// independent), then added in split order.
+__device__ __forceinline__ float4 cluster_sum4(uint32_t off, int splits)
+{
+    float4 p[kTcMaxSplits];
+#pragma unroll
+    for (int r = 0; r < kTcMaxSplits; ++r) {
+        p[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r < splits) {
+            uint32_t remote;
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(off), "r"(r));
+            asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+                         : "=f"(p[r].x), "=f"(p[r].y), "=f"(p[r].z), "=f"(p[r].w)
+                         : "r"(remote)
+                         : "memory");
+        }
+    }
+    float4 v = p[0];
+#pragma unroll
+    for (int r = 1; r < kTcMaxSplits; ++r) {
+        if (r < splits) {
+            v.x += p[r].x;
+            v.y += p[r].y;
+            v.z += p[r].z;
+            v.w += p[r].w;
+        }
+    }
+    return v;
+}
+
 template <bool kFp8, int NPAD>
 __global__ void __launch_bounds__(kTcThreads, 2)
     tc_gemv_kernel(const GemvArgs a, const __grid_constant__ CUtensorMap tmx)
@@ -456,16 +491,33 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         pdl_wait(); // every global write comes after the previous kernel
         if (warp < 4) {
             const float sc = (kFp8 && row < a.n) ? __ldg(a.scale + row) : 1.0f;
+            const int col = out_col(row, a.act != kActPlain, a.half);
+            // SiLU-and-multiply: lane l (l & 8 == 0, a gate row) takes the up
+            // row's sums from lane l + 8 (row + 8) of the same warp
+            const bool gate = a.act == kActSiluMul && (lane & 8) == 0 && row < a.n;
+            const float scu = (kFp8 && gate) ? __ldg(a.scale + row + 8) : 1.0f;
 #pragma unroll
             for (int c = 0; c < NPAD / 16; ++c) {
                 float d[16];
                 tm_load16(dq + uint32_t(16 * c), d);
                 tm_wait_ld();
-                if (row < a.n) {
+                if (a.act == kActSiluMul) {
+                    float du[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        du[e] = __shfl_down_sync(0xffffffffu, d[e], 8);
+                    if (gate) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            if (16 * c + e < a.m)
+                                a.y[int64_t(16 * c + e) * a.ldy + col] =
+                                    silu_mul_bf16(kFp8 ? sc * d[e] : d[e], kFp8 ? scu * du[e] : du[e]);
+                    }
+                } else if (row < a.n) {
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
                         if (16 * c + e < a.m)
-                            a.y[int64_t(16 * c + e) * a.ldy + row] = to_bf16(kFp8 ? sc * d[e] : d[e]);
+                            a.y[int64_t(16 * c + e) * a.ldy + col] = to_bf16(kFp8 ? sc * d[e] : d[e]);
                 }
             }
         }
@@ -499,37 +551,28 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             const int orow = row0 + rl;
             if (4 * q >= a.m || orow >= a.n)
                 continue;
+            if (a.act == kActSiluMul && (rl & 8))
+                continue; // an up row: added with its gate row (rl - 8)
             const uint32_t off = red_local + uint32_t((rl * kRedPitch + 4 * q) * 4);
-            // all remote loads first (independent), then the sum in split order
-            float4 p[kTcMaxSplits];
-#pragma unroll
-            for (int r = 0; r < kTcMaxSplits; ++r) {
-                p[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (r < a.splits) {
-                    uint32_t remote;
-                    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(off), "r"(r));
-                    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-                                 : "=f"(p[r].x), "=f"(p[r].y), "=f"(p[r].z), "=f"(p[r].w)
-                                 : "r"(remote)
-                                 : "memory");
-                }
-            }
-            float4 v = p[0];
-#pragma unroll
-            for (int r = 1; r < kTcMaxSplits; ++r) {
-                if (r < a.splits) {
-                    v.x += p[r].x;
-                    v.y += p[r].y;
-                    v.z += p[r].z;
-                    v.w += p[r].w;
-                }
-            }
+            const float4 v = cluster_sum4(off, a.splits);
             const float sc = kFp8 ? __ldg(a.scale + orow) : 1.0f;
             const float out[4] = {v.x, v.y, v.z, v.w};
+            const int col = out_col(orow, a.act != kActPlain, a.half);
+            if (a.act != kActSiluMul) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (4 * q + e < a.m)
-                    a.y[int64_t(4 * q + e) * a.ldy + orow] = to_bf16(kFp8 ? sc * out[e] : out[e]);
+                for (int e = 0; e < 4; ++e)
+                    if (4 * q + e < a.m)
+                        a.y[int64_t(4 * q + e) * a.ldy + col] = to_bf16(kFp8 ? sc * out[e] : out[e]);
+            } else {
+                const float4 vu = cluster_sum4(off + uint32_t(8 * kRedPitch * 4), a.splits);
+                const float scu = kFp8 ? __ldg(a.scale + orow + 8) : 1.0f;
+                const float up[4] = {vu.x, vu.y, vu.z, vu.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (4 * q + e < a.m)
+                        a.y[int64_t(4 * q + e) * a.ldy + col] =
+                            silu_mul_bf16(kFp8 ? sc * out[e] : out[e], kFp8 ? scu * up[e] : up[e]);
+            }
         }
         // no CTA leaves while another may still read its tile
         __syncwarp();

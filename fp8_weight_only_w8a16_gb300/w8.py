@@ -6,8 +6,8 @@ into exceptions.  PyTorch provides device memory and streams only.  There is
 no fallback: if libw8.so is missing, importing this module raises.
 
 Names follow the C ABI: ``validate``, ``packed_bytes``, ``bind`` (w8_bind),
-``w8_gemv``, ``bf16_gemv``, ``workspace_bytes``, ``plan_info``,
-``packed_offset``.
+``w8_gemv``, ``bf16_gemv``, ``w8_gemv_silu_mul``, ``workspace_bytes``,
+``plan_info``, ``packed_offset``, ``gate_up_packed_row``.
 """
 from __future__ import annotations
 
@@ -22,8 +22,8 @@ from . import build_lib
 LIB_PATH = build_lib.LIB
 
 DT_E4M3FN, DT_BF16, DT_E4M3FNUZ, DT_E5M2, DT_FP16 = 1, 2, 3, 4, 5
-SRC_ROW_MAJOR = 0
-LAYOUT_MMA_16x32 = 1
+SRC_ROW_MAJOR, SRC_GATE_UP = 0, 1
+LAYOUT_MMA_16x32, LAYOUT_MMA_16x32_GATE_UP = 1, 2
 MAX_M = 64
 
 STATUS = {
@@ -93,7 +93,7 @@ def _load():
     lib.w8_plan_shape.restype = st
     lib.w8_workspace_bytes.argtypes = [vp, i32, i32, ctypes.POINTER(sz)]
     lib.w8_workspace_bytes.restype = st
-    for name in ("w8_gemv", "bf16_gemv"):
+    for name in ("w8_gemv", "bf16_gemv", "w8_gemv_silu_mul"):
         f = getattr(lib, name)
         f.argtypes = [vp, i32, vp, i64, i32, vp, i64, vp, sz, vp]
         f.restype = st
@@ -101,6 +101,8 @@ def _load():
     lib.w8_gemv_noalloc.restype = st
     lib.w8_packed_offset.argtypes = [i32, i64, i64, i64]
     lib.w8_packed_offset.restype = i64
+    lib.w8_gate_up_packed_row.argtypes = [i64, i64]
+    lib.w8_gate_up_packed_row.restype = i64
     lib.w8_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), i32]
     lib.w8_device_status.restype = st
     return lib
@@ -111,8 +113,8 @@ lib = _load()
 # every symbol include/w8.h declares
 EXPORTS = ("w8_status_str", "w8_abi_version", "w8_validate", "w8_packed_bytes", "w8_bind",
            "w8_release", "w8_build_planes", "w8_build_info", "w8_plan_info", "w8_plan_shape",
-           "w8_workspace_bytes", "w8_gemv", "bf16_gemv", "w8_gemv_noalloc", "w8_packed_offset",
-           "w8_device_status")
+           "w8_workspace_bytes", "w8_gemv", "bf16_gemv", "w8_gemv_silu_mul", "w8_gemv_noalloc",
+           "w8_packed_offset", "w8_gate_up_packed_row", "w8_device_status")
 
 
 def _check(status: int):
@@ -143,8 +145,9 @@ class Plane:
 
     @staticmethod
     def from_tensor(w: torch.Tensor, scale: torch.Tensor | None = None, k: int | None = None,
-                    dtype: int | None = None) -> "Plane":
-        """w: 2-D with unit column stride; uint8 -> E4M3FN codes, bfloat16/int16/uint16 -> bf16."""
+                    dtype: int | None = None, layout: int = SRC_ROW_MAJOR) -> "Plane":
+        """w: 2-D with unit column stride; uint8 -> E4M3FN codes, bfloat16/int16/uint16 -> bf16.
+        layout SRC_GATE_UP: a merged [2I, K] projection, gate rows first, then up."""
         assert w.dim() == 2 and w.stride(1) == 1, "plane must be row-major with unit column stride"
         if dtype is None:
             if w.dtype in (torch.uint8, torch.float8_e4m3fn):
@@ -160,7 +163,7 @@ class Plane:
             else:
                 raise TypeError(f"no w8 dtype for {w.dtype}")
         return Plane(w=w, dtype=dtype, n=w.shape[0], k=w.shape[1] if k is None else k,
-                     ldw=w.stride(0), scale=scale)
+                     ldw=w.stride(0), scale=scale, layout=layout)
 
     def desc(self) -> PlaneDesc:
         return PlaneDesc(self.w.data_ptr() if self.w is not None else None, self.dtype,
@@ -277,6 +280,12 @@ def bf16_gemv(build: Build, plane: int, x: torch.Tensor, y: torch.Tensor,
     return _gemv(lib.bf16_gemv, build, plane, x, y, workspace, m, stream)
 
 
+def w8_gemv_silu_mul(build: Build, plane: int, x: torch.Tensor, y: torch.Tensor,
+                     workspace: torch.Tensor | None = None, m: int | None = None, stream=None):
+    """y[:m, :I] = bf16(silu(g) * u) on a gate_up plane of either dtype (one kernel launch)."""
+    return _gemv(lib.w8_gemv_silu_mul, build, plane, x, y, workspace, m, stream)
+
+
 def plan_shape(n: int, k: int, m: int, sm_count: int) -> PlanInfo:
     out = PlanInfo()
     _check(lib.w8_plan_shape(n, k, m, sm_count, ctypes.byref(out)))
@@ -305,3 +314,7 @@ def device_status(reset: bool = False) -> int:
 
 def packed_offset(dtype: int, k_blocks: int, row: int, col: int) -> int:
     return int(lib.w8_packed_offset(dtype, k_blocks, row, col))
+
+
+def gate_up_packed_row(n: int, row: int) -> int:
+    return int(lib.w8_gate_up_packed_row(n, row))

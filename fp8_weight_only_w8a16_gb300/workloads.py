@@ -24,14 +24,20 @@ class Projection:
     dtype: str                  # "e4m3fn" or "bf16"
     ms: tuple                   # decode-token counts exercised
     ldw: int | None = None      # source row stride when the plane is padded
+    act: str = ""               # "silu_mul": a merged gate_up plane (gate rows first)
+                                # whose call returns silu(gate) * up, n / 2 columns
 
     @property
     def weight_bytes(self) -> int:
         return self.n * self.k * (1 if self.dtype == "e4m3fn" else 2)
 
+    @property
+    def out_n(self) -> int:
+        return self.n // 2 if self.act == "silu_mul" else self.n
+
     def algorithmic_bytes(self, m: int) -> int:
         """W + fp32 scales (FP8) + x + y, with the logical K (pad excluded)."""
-        b = self.weight_bytes + 2 * m * self.k + 2 * m * self.n
+        b = self.weight_bytes + 2 * m * self.k + 2 * m * self.out_n
         if self.dtype == "e4m3fn":
             b += 4 * self.n
         return b
@@ -50,6 +56,10 @@ SHARED_GATE_UP = Projection("shared_expert_gate_up", 4096, 6144, "e4m3fn", (8,))
 SHARED_DOWN = Projection("shared_expert_down", 6144, 2048, "e4m3fn", (8,))
 SHARED_GATE_UP_KPAD = Projection("shared_expert_gate_up_kpad", 4096, 6144, "e4m3fn", (8,),
                                  ldw=6144 + 128)
+# The shared expert's gate_up with SiLU-and-multiply in the same kernel: its
+# output h [M, 2048] is the down projection's input.
+SHARED_GATE_UP_SILU = Projection("shared_expert_gate_up_silu", 4096, 6144, "e4m3fn", (8,),
+                                 act="silu_mul")
 Q_B = Projection("q_b_proj", 16384, 2048, "e4m3fn", SWEEP_M)
 KV_B = Projection("kv_b_proj", 28672, 512, "e4m3fn", SWEEP_M)
 WQ_B = Projection("indexer_wq_b", 4096, 2048, "e4m3fn", SWEEP_M)
@@ -62,16 +72,17 @@ LM_HEAD = Projection("lm_head", 154880, 6144, "bf16", (1,))
 WK_WEIGHTS_PROJ = Projection("indexer_wk_weights_proj", 160, 6144, "bf16", SWEEP_M)
 
 ALL = (TINY, FUSED_QKV_A, O_PROJ, O_PROJ_BF16, SHARED_GATE_UP, SHARED_DOWN,
-       SHARED_GATE_UP_KPAD, Q_B, KV_B, WQ_B, WK, WEIGHTS_PROJ, WK_WEIGHTS_PROJ, LM_HEAD)
+       SHARED_GATE_UP_KPAD, SHARED_GATE_UP_SILU, Q_B, KV_B, WQ_B, WK, WEIGHTS_PROJ, WK_WEIGHTS_PROJ, LM_HEAD)
 BY_NAME = {p.name: p for p in ALL}
 
 # The five workload groups, in order: the tiny correctness case, the fused
 # qkv_a projection, o_proj (FP8 and bf16), the shared-expert pair with its
-# K-padded variant, and the full-layer sweep.
+# K-padded variant and its gate_up with SiLU-and-multiply, and the full-layer
+# sweep.
 GROUPS = {
     "tiny": (TINY,),
     "fused_qkv_a_proj": (FUSED_QKV_A,),
     "o_proj": (O_PROJ, O_PROJ_BF16),
-    "shared_expert": (SHARED_GATE_UP, SHARED_DOWN, SHARED_GATE_UP_KPAD),
+    "shared_expert": (SHARED_GATE_UP, SHARED_DOWN, SHARED_GATE_UP_KPAD, SHARED_GATE_UP_SILU),
     "layer_sweep": (Q_B, KV_B, WQ_B, WK, WEIGHTS_PROJ, WK_WEIGHTS_PROJ, LM_HEAD),
 }

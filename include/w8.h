@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define W8_ABI_VERSION 2
+#define W8_ABI_VERSION 3
 
 /* A cudaStream_t: the runtime's stream type is this same pointer type. */
 typedef struct CUstream_st *w8_stream;
@@ -58,9 +58,11 @@ typedef enum {
     W8_ERR_BIAS = 4,      /* a bias pointer was given: the GEMV has no bias */
     W8_ERR_MIXED = 5,     /* bf16 and FP8 planes mixed in one build */
     W8_ERR_SHAPE = 6,     /* N or K < 1 or too large, ldw < K, M outside 0..64,
-                             ldx < K, ldy < N */
+                             ldx < K, ldy < N (< N/2 for w8_gemv_silu_mul), or a
+                             W8_SRC_GATE_UP plane whose N is not a multiple of 16 */
     W8_ERR_SCALE = 7,     /* an FP8 plane without row scales, or a bf16 plane with them */
-    W8_ERR_LAYOUT = 8,    /* unknown source layout */
+    W8_ERR_LAYOUT = 8,    /* unknown source layout, or w8_gemv_silu_mul on a plane not
+                             bound as W8_SRC_GATE_UP */
     W8_ERR_CAPACITY = 9,  /* packed buffer or workspace smaller than required */
     W8_ERR_ALIGN = 10,    /* packed buffer or workspace not 256-byte aligned, x not 16-byte
                              aligned or ldx not a multiple of 8, or y not 2-byte aligned */
@@ -83,8 +85,15 @@ typedef enum {
     W8_DT_FP16 = 5
 } w8_dtype;
 
-/* Source layouts: only plain row-major [n][ldw] planes (K contiguous). */
+/* Source layouts: row-major [n][ldw] planes (K contiguous).
+ * W8_SRC_GATE_UP is a merged MLP projection of n = 2I rows: rows 0..I-1 are
+ * the gate projection and rows I..2I-1 the up projection (ATOM Model Support
+ * Guide: the Llama MLP merges gate and up into one column-parallel
+ * projection, followed by SiLU-and-multiply and the down projection; Adding
+ * a new model, Step 5: gate_proj is shard 0 and up_proj shard 1 of
+ * gate_up_proj).  I must be a multiple of 8 (n a multiple of 16). */
 #define W8_SRC_ROW_MAJOR 0
+#define W8_SRC_GATE_UP 1
 
 /* Packed layout the kernels read (recorded in every build; the PR page,
  * Limitations, notes its own layout "isn't recorded on the tensor"):
@@ -93,13 +102,19 @@ typedef enum {
  * the tensor-core A operand, one 16-byte vector per lane.  The K tail and
  * the row tail are zero-filled. */
 #define W8_LAYOUT_MMA_16x32 1
+/* The same layout for a W8_SRC_GATE_UP plane, with the rows interleaved:
+ * packed 16-row tile t holds gate rows 8t..8t+7, then up rows 8t..8t+7 (the
+ * source rows 8t..8t+7 and I+8t..I+8t+7), so that one tensor-core tile
+ * holds a gate row and its up row eight rows apart.  The scales follow their
+ * rows.  Both gemv calls still write y in source row order. */
+#define W8_LAYOUT_MMA_16x32_GATE_UP 2
 
 /* One source weight plane: W[n][ldw] in device memory, row-major. */
 typedef struct {
     const void *w;        /* device; E4M3 codes (1 byte) or bf16 bits (2 bytes);
                              16-byte aligned */
     int32_t dtype;        /* w8_dtype */
-    int32_t layout;       /* W8_SRC_ROW_MAJOR */
+    int32_t layout;       /* W8_SRC_ROW_MAJOR or W8_SRC_GATE_UP */
     int64_t n;            /* output rows, >= 1 */
     int64_t k;            /* logical reduction columns, >= 1; columns k..ldw-1 are ignored */
     int64_t ldw;          /* row stride in elements, >= k, ldw * element bytes % 16 == 0 */
@@ -110,7 +125,7 @@ typedef struct {
 /* What a build records about one bound plane. */
 typedef struct {
     int32_t dtype;           /* W8_DT_E4M3FN or W8_DT_BF16 */
-    int32_t layout;          /* W8_LAYOUT_MMA_16x32 */
+    int32_t layout;          /* W8_LAYOUT_MMA_16x32 or W8_LAYOUT_MMA_16x32_GATE_UP */
     int64_t n, k;
     int64_t row_tiles;       /* ceil(n / 16) */
     int64_t k_blocks;        /* ceil(k / 32) */
@@ -120,8 +135,10 @@ typedef struct {
 } w8_plane_info;
 
 /* The launch a gemv call makes for one (plane, m); returned for inspection.
- * kernel 0 (m <= 8): the register-ring kernel, 8 warps per CTA.
- * kernel 1 (m >= 9): the tensor-memory kernel, 128 rows x one K range per CTA;
+ * kernel 0 (m <= 16, or a plane of fewer than 48 blocks of 128 rows): the
+ *   register-ring kernel, 8 warps per CTA.
+ * kernel 1 (m >= 17 on a plane of at least 48 blocks of 128 rows): the
+ *   tensor-memory kernel, 128 rows x one K range per CTA;
  *   there n_tiles = tokens rounded up to 16, over 8; row_tiles_per_warp = the
  *   CTA's 8 row tiles; warps_k = 1; depth = the converter warps' ring depth. */
 typedef struct {
@@ -226,6 +243,25 @@ w8_status bf16_gemv(const w8_build *b, int plane, const uint16_t *x, int64_t ldx
                     uint16_t *y, int64_t ldy, void *workspace, size_t workspace_bytes,
                     w8_stream s);
 
+/* The merged gate_up projection followed by SiLU-and-multiply, in one kernel
+ * (ATOM Model Support Guide, Model architecture details, Llama MLP: merged
+ * gate+up, SiLU+mul activation, then down; Model-specific optimizations:
+ * the activation fused into the kernel next to it).  On a plane bound as
+ * W8_SRC_GATE_UP (n = 2I), for 0 <= i < m and 0 <= j < I:
+ *   g = the GEMV's output for source row j (what w8_gemv / bf16_gemv give),
+ *   u = the GEMV's output for source row I + j,
+ *   y[i*ldy + j] = bf16(silu(g) * u),  silu(v) = v / (1 + exp(-v)),
+ * with g and u rounded to bf16 first and the SiLU and the product in fp32
+ * (expf and a correctly rounded division), so the result is what the two
+ * separate steps give.  Either dtype (FP8 with row scales, or bf16).
+ * y: device bf16 [m][ldy], ldy >= I, written for j < I only.  x, m and the
+ * workspace as for w8_gemv (the plan is that of the [2I, K] plane).
+ * Returns W8_ERR_LAYOUT on a plane not bound as W8_SRC_GATE_UP.  One kernel
+ * launch on s. */
+w8_status w8_gemv_silu_mul(const w8_build *b, int plane, const uint16_t *x, int64_t ldx, int m,
+                           uint16_t *y, int64_t ldy, void *workspace, size_t workspace_bytes,
+                           w8_stream s);
+
 /* The FP8 GEMV for callers that cannot allocate device memory.
  *
  * The pages have no counterpart of this entry point; it serves callers that
@@ -255,9 +291,15 @@ w8_status w8_gemv_noalloc(const w8_build *b, int plane, const uint16_t *x, int64
 
 /* Host-side address map of W8_LAYOUT_MMA_16x32: byte offset, inside one
  * plane's packed weights, of element (row, col) of a plane with k_blocks
- * blocks of 32 columns.  dtype is W8_DT_E4M3FN or W8_DT_BF16; returns -1 on a
+ * blocks of 32 columns (row is the packed row: for a gate_up plane, see
+ * w8_gate_up_packed_row).  dtype is W8_DT_E4M3FN or W8_DT_BF16; returns -1 on a
  * bad argument.  The repack kernel places every element at this offset. */
 int64_t w8_packed_offset(int dtype, int64_t k_blocks, int64_t row, int64_t col);
+
+/* The packed row that holds source row `row` of a W8_SRC_GATE_UP plane of n
+ * rows (W8_LAYOUT_MMA_16x32_GATE_UP); -1 on a bad argument (n not a positive
+ * multiple of 16, row outside 0..n-1).  Host-only. */
+int64_t w8_gate_up_packed_row(int64_t n, int64_t row);
 
 #ifdef __cplusplus
 }

@@ -42,7 +42,7 @@ def test_every_declared_function_is_exported():
 
 
 def test_abi_version_and_status_strings():
-    assert w8.lib.w8_abi_version() == 2
+    assert w8.lib.w8_abi_version() == 3
     for code in range(15):
         assert w8.status_str(code)
     assert w8.status_str(99) == "unknown status"
@@ -72,7 +72,13 @@ def _status(*descs):
     ({"dtype": w8.DT_E5M2}, "W8_ERR_DTYPE"),
     ({"dtype": w8.DT_FP16}, "W8_ERR_DTYPE"),
     ({"dtype": 99}, "W8_ERR_DTYPE"),
-    ({"layout": 1}, "W8_ERR_LAYOUT"),
+    ({"layout": 2}, "W8_ERR_LAYOUT"),
+    ({"layout": -1}, "W8_ERR_LAYOUT"),
+    ({"layout": w8.SRC_GATE_UP}, "W8_OK"),                 # n = 64: I = 32
+    ({"layout": w8.SRC_GATE_UP, "n": 48}, "W8_OK"),        # I = 24
+    ({"layout": w8.SRC_GATE_UP, "n": 40}, "W8_ERR_SHAPE"),  # I = 20: not a multiple of 8
+    ({"layout": w8.SRC_GATE_UP, "n": 8}, "W8_ERR_SHAPE"),
+    ({"layout": w8.SRC_GATE_UP, "n": 7}, "W8_ERR_SHAPE"),
     ({"bias": FAKE}, "W8_ERR_BIAS"),
     ({"n": 0}, "W8_ERR_SHAPE"),
     ({"k": 0}, "W8_ERR_SHAPE"),
@@ -108,6 +114,22 @@ def test_packed_bytes_formula():
     assert w8.packed_bytes([_desc(dtype=w8.DT_BF16, scale=None, n=16, k=32, ldw=32)]) == 1024
     two = w8.packed_bytes([_desc(n=100, k=200, ldw=208), _desc(n=16, k=32, ldw=32)])
     assert two == 25088 + 512 + 512 + 256
+
+
+@pytest.mark.parametrize("n", [16, 48, 64, 4096])
+def test_gate_up_packed_row_interleaves_gate_and_up(n):
+    half = n // 2
+    rows = [w8.gate_up_packed_row(n, r) for r in range(n)]
+    assert sorted(rows) == list(range(n))  # a permutation of the packed rows
+    for j in range(half):
+        g, u = rows[j], rows[half + j]
+        # gate row j and up row j share a 16-row tile, eight rows apart
+        assert g // 16 == u // 16 == j // 8
+        assert g % 16 == j % 8 and u == g + 8
+    for bad in (-1, n):
+        assert w8.gate_up_packed_row(n, bad) == -1
+    for bad_n in (0, 8, 24, -16):
+        assert w8.gate_up_packed_row(bad_n, 0) == -1
 
 
 @pytest.mark.parametrize("dtype,elt", [(w8.DT_E4M3FN, 1), (w8.DT_BF16, 2)])

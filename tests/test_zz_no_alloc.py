@@ -73,6 +73,29 @@ def test_noalloc_equals_gemv_with_workspace(w8, n, k, m):
         assert ok, worst
 
 
+def test_noalloc_on_a_gate_up_plane_keeps_source_order(w8):
+    # a merged gate_up plane (gate rows first) whose plan splits K: the
+    # packed rows are interleaved, the output is in source row order
+    n, k, m = 32, 6144, 5
+    rng = np.random.default_rng(11)
+    plane = synth.weight_plane(rng, n, k)
+    x = synth.activations(rng, k, m)
+    w_d, s_d = to_dev(plane.w), to_dev(plane.scale)
+    b = w8.bind([w8.Plane.from_tensor(w_d, s_d, k=k, layout=w8.SRC_GATE_UP)])
+    assert b.plan(0, m).splits > 1
+    xd = to_dev(x)
+    y_ref = torch.zeros((m, n), dtype=torch.int16, device=dev())
+    w8.w8_gemv(b, 0, xd, y_ref, b.new_workspace(0, m))
+    y = torch.full((m, n), 0x7FC1, dtype=torch.int16, device=dev())
+    w8.w8_gemv_noalloc(b, 0, xd, y)
+    torch.cuda.synchronize()
+    got = from_dev(y)
+    assert np.array_equal(got, from_dev(y_ref))
+    y64, mag = oracle.gemv_f64(plane.w, oracle.DT_E4M3FN, plane.scale, x, k=k)
+    ok, worst = oracle.within_tolerance(got, y64, mag)
+    assert ok, worst
+
+
 def test_noalloc_refuses_what_it_cannot_serve(w8):
     # a plan whose split partials exceed the fixed scratch (the first such
     # shape for this GPU's SM count)
