@@ -326,7 +326,8 @@ w8_status w8_plan_info(const w8_build *b, int plane, int m, w8_plan *out)
     if (st == W8_OK && p.dtype == W8_DT_BF16)
     {
         const w8::Plan pl = w8::make_plan(p.n, p.k, m, b->sm_count);
-        out->depth = w8::depth_w(pl.nt, pl.r, false, pl.occ);
+        out->depth = pl.tc ? w8::tc_stages(false, pl.npad).nw * w8::kTcStageBlocks
+                           : w8::depth_w(pl.nt, pl.r, false, pl.occ);
     }
     return st;
 }

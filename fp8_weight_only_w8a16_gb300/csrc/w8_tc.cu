@@ -450,6 +450,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             atomicOr(&g_tc_status, 1);
     } else if (warp == kWarpIssue && lane == 0) {
         // ---- issuer: one thread drives the tensor cores --------------------------
+        // The descriptors of a stage are its slot's base plus compile-time
+        // offsets (the address field holds addr >> 4, and every shared-memory
+        // address stays below 256 KB, so adding never carries out of it); a
+        // full stage is issued unrolled, a partial last stage block by block.
+        const uint64_t bdesc0 = smem_desc(smem_u32(s_b), kLbo, kSbo);
         bool ok = true;
         for (int st = 0; st < nst && ok; ++st) {
             const int sa_ = st % kNA, sb = st % kNB;
@@ -458,17 +463,24 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             if (!ok)
                 break;
             tc_fence_after();
-            const uint32_t stage = smem_u32(s_b + sb * kStageB);
-            for (int j = 0; j < kTcKs; ++j) {
-                const int i = st * kTcKs + j;
-                if (i >= cnb)
-                    break;
+            const uint64_t bd = bdesc0 + uint64_t((sb * kStageB) >> 4);
+            const uint32_t at = tbase + uint32_t(kACol + sa_ * kTcKs * 16);
+            const int nb = cnb - st * kTcKs < kTcKs ? cnb - st * kTcKs : kTcKs;
+            if (nb == kTcKs) {
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const uint32_t a_t = tbase + uint32_t(kACol + (sa_ * kTcKs + j) * 16 + q * 8);
-                    const uint64_t bd = smem_desc(stage + uint32_t(j * kBlockB + q * kStepB), kLbo, kSbo);
-                    umma_ts(tbase, a_t, bd, kIdesc, uint32_t(i | q));
-                }
+                for (int j = 0; j < kTcKs; ++j)
+#pragma unroll
+                    for (int q = 0; q < 2; ++q)
+                        umma_ts(tbase, at + uint32_t(j * 16 + q * 8),
+                                bd + uint64_t((j * kBlockB + q * kStepB) >> 4), kIdesc,
+                                uint32_t(st | j | q));
+            } else {
+                for (int j = 0; j < nb; ++j)
+#pragma unroll
+                    for (int q = 0; q < 2; ++q)
+                        umma_ts(tbase, at + uint32_t(j * 16 + q * 8),
+                                bd + uint64_t((j * kBlockB + q * kStepB) >> 4), kIdesc,
+                                uint32_t(st | j | q));
             }
             umma_commit(&bar_empty_a[sa_]);
             umma_commit(&bar_empty_b[sb]);

@@ -384,6 +384,18 @@ def test_tensor_memory_kernel_clusters_and_graph_replay(w8, n, k, m):
     assert w8.device_status() == 0
 
 
+def test_plan_info_of_a_bf16_tensor_memory_plan(w8):
+    # a bf16 build's plan reports the bf16 ring depth: for the tensor-memory
+    # kernel its weight stages (2 of 4 blocks at 17..32 tokens), not an entry
+    # of the register-ring instance table
+    plane, _x = _case(9, 6144, 256, 1, "bf16")
+    b, _src = bind_plane(w8, plane)
+    p = b.plan(0, 32)
+    assert p.kernel == 1 and p.n_tiles == 4
+    assert p.depth == 2 * 4
+    assert b.plan(0, 8).kernel == 0
+
+
 def test_bind_refusals_on_device(w8):
     n, k = 32, 64
     codes = to_dev(np.zeros((n, k), np.uint8))
