@@ -43,6 +43,8 @@ struct GemvArgs {
     float *partial;         // workspace body: [splits][rt*16][m] fp32 (splits > 1)
     int act;                // kActPlain, kActGateUp or kActSiluMul
     int half;               // gate_up planes: I = n / 2
+    int xg;                 // tc kernel: row blocks of a cluster that share the
+                            // activation tiles (TMA multicast); set by launch_tc
 };
 
 // The output mapping of a plane: gate_up planes (bound with W8_SRC_GATE_UP)

@@ -101,6 +101,7 @@ struct Plan {
     int splits;
     int kbs_max;     // most K blocks one warp streams
     int grid;
+    int xg;          // tc: row blocks per cluster sharing the activation tiles (else 1)
     int smem;        // dynamic shared memory bytes (the K-part reduction)
     size_t ws_counters; // bytes of the counter head of the workspace
     size_t ws_bytes;    // total workspace bytes (0 when splits == 1)
@@ -187,7 +188,8 @@ W8_HD constexpr int tc_smem_bytes(bool fp8, int npad)
     return tc_stages(fp8, npad).nw * 8 * 4 * (fp8 ? kRunFp8 : kRunBf16) +
            tc_stages(fp8, npad).nb * 4 * npad * 64;
 }
-constexpr int kTcMaxSplits = 8;
+constexpr int kTcMaxSplits = 8;  // CTAs per cluster (the portable cluster size)
+constexpr int kTcMaxXg = 2;      // row blocks sharing one activation tile
 
 inline Plan make_tc_plan(int64_t n, int64_t k, int m, int sm_count)
 {
@@ -210,6 +212,14 @@ inline Plan make_tc_plan(int64_t n, int64_t k, int m, int sm_count)
            p.kb / (int64_t(splits) * 2) >= kTcStageBlocks)
         splits *= 2;
     p.splits = splits;
+    // from 48 tokens on, adjacent row blocks of one K range join the cluster
+    // and share each activation tile (as many bytes per CTA as its weights at
+    // 64 tokens): each CTA loads 1/xg of it and multicasts it to the others.
+    // Measured: q_b 64 tokens 18.6 -> 16.7 us; at 32 tokens within +-5 %.
+    int xg = 1;
+    while (p.npad >= 48 && xg < kTcMaxXg && splits * xg * 2 <= kTcMaxSplits && rbs % (xg * 2) == 0)
+        xg *= 2;
+    p.xg = xg;
     p.row_groups = int(rbs);
     p.grid = int(rbs * splits);
     p.kbs_max = int(ceil_div(p.kb, splits));
@@ -253,8 +263,12 @@ inline Plan make_plan(int64_t n, int64_t k, int m, int sm_count)
                 const int64_t waves = ceil_div(ctas, slots);
                 const int64_t resident = ctas < slots ? ctas : slots;
                 const int64_t dw = depth_w(p.nt, r, true, occ);
-                const int64_t inflight = resident * kWarps * (bpw < dw ? bpw : dw) * r * kRunFp8;
-                const int64_t warps = resident * kWarps;
+                // only row tiles that exist are streamed: a plane with fewer
+                // tiles than its CTAs hold leaves the other warps idle
+                const int64_t cta_tiles = int64_t(kWarps / wk) * r;
+                const int64_t tiles = resident * cta_tiles < p.rt ? resident * cta_tiles : p.rt;
+                const int64_t inflight = tiles * wk * (bpw < dw ? bpw : dw) * kRunFp8;
+                const int64_t warps = ceil_div(tiles, r) * wk;
                 bool better;
                 if (!have)
                     better = true;
@@ -294,6 +308,7 @@ inline Plan make_plan(int64_t n, int64_t k, int m, int sm_count)
     p.splits = splits;
     p.row_groups = int(ceil_div(p.rt, int64_t(kWarps / p.wk) * p.r));
     p.grid = p.row_groups * p.splits;
+    p.xg = 1;
     p.kbs_max = int(ceil_div(ceil_div(p.kb, p.splits), p.wk));
     p.smem = kWarps * p.r * p.nt * 4 * 32 * int(sizeof(float));
     if (p.splits > 1) {
