@@ -187,6 +187,7 @@ class GemvBench:
         torch.cuda.synchronize()
         del w_d, s_d, src
         mmax = max(self.ms)
+        assert x_all.shape[0] >= mmax, "the workload draws fewer token rows than the largest M"
         self.x_host = np.ascontiguousarray(x_all[:mmax])
         self.x = torch.from_numpy(self.x_host.view(np.int16)).to(device)
         self.y = {m: torch.zeros((m, proj.out_n), dtype=torch.int16, device=device)
@@ -551,6 +552,7 @@ def run_sweep(args):
                    "us_per_call": round(us, 3), "gbs": round(gbs, 1),
                    "pct_of_8tbs": round(100 * gbs / NOMINAL_HBM_GBS, 1),
                    "frac_of_peak": round(gbs / peak, 4), "peak": f"{peak} ({peak_kind})",
+                   "tflops": round(proj.flops(m) / (us * 1e-6) / 1e12, 1),
                    "alg_bytes": proj.algorithmic_bytes(m), "grid": plan.grid,
                    "splits": plan.splits, "copies": b.copies}
             line = json.dumps(rec)

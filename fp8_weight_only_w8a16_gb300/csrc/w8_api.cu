@@ -140,7 +140,7 @@ const char *w8_status_str(w8_status s)
                                  "multiple of 16 bytes";
     case W8_ERR_BIAS: return "a bias was given; the GEMV has none";
     case W8_ERR_MIXED: return "bf16 and FP8 planes mixed in one build";
-    case W8_ERR_SHAPE: return "bad shape: N, K >= 1, ldw >= K, 0 <= m <= 64, ldx >= K, ldy >= N "
+    case W8_ERR_SHAPE: return "bad shape: N, K >= 1, ldw >= K, 0 <= m <= 256, ldx >= K, ldy >= N "
                               "(N/2 for SiLU-and-multiply); a gate_up plane needs N % 16 == 0";
     case W8_ERR_SCALE: return "FP8 planes need fp32 row scales; bf16 planes take none";
     case W8_ERR_LAYOUT: return "unknown source layout (row-major or gate_up), or SiLU-and-multiply "

@@ -41,7 +41,8 @@ constexpr int kRunFp8 = 512;      // bytes of one (tile, block) run, FP8
 constexpr int kRunBf16 = 1024;    // bytes of one (tile, block) run, bf16
 constexpr int kWarps = 8;         // warps per CTA of the GEMV kernel
 constexpr int kThreads = kWarps * 32;
-constexpr int kMaxM = 64;         // decode tokens per call
+constexpr int kMaxM = 256;        // tokens per call (decode steps, draft rows, prefill chunks)
+constexpr int kMaxRingM = 64;     // the register-ring kernel's limit (8 token groups of 8)
 
 W8_HD int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 W8_HD size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -159,29 +160,44 @@ inline int64_t plan_ctas(int64_t rt, int r, int wk, int splits)
 // K blocks when K allows it.  K is split across CTAs only for planes whose
 // row tiles leave most SMs idle.
 // The tensor-memory kernel (w8_tc.cu): CTAs of 128 rows x a K range, eleven
-// warps, 2 CTAs per SM (256 tensor-memory columns and about 100 KB of shared
-// memory each).  K is split across the CTAs of a cluster (up to 8) until about
-// two CTAs per SM are busy, keeping at least one stage of K blocks per split;
-// the partial sums meet in distributed shared memory, so no workspace.
+// warps.  Up to 64 tokens: 2 CTAs per SM (256 tensor-memory columns and about
+// 100 KB of shared memory each); from 65 to 256 tokens (padded to 96, 128,
+// 192 or 256): 1 CTA per SM (512 columns: the accumulator, then A stages;
+// about 200 KB).  K is split across the CTAs of a cluster (up to 8) until
+// about the resident CTAs are busy, keeping at least one stage of K blocks
+// per split; the partial sums meet in distributed shared memory, so no
+// workspace.
 constexpr int kTcMinM = 17;       // decode tokens from which the tc kernel may run
 constexpr int kTcMinRowBlocks = 48; // ... on planes of at least this many 128-row blocks
 constexpr int kTcStageBlocks = 4; // K blocks per stage of the tc kernel
 constexpr int kTcCtasPerSm = 2;
 constexpr int kTcThreadsPerCta = 352;
 
+// Token paddings of the tensor-memory kernel (its MMA N): steps of 16 up to
+// 64, then 96, 128, 192, 256.
+W8_HD constexpr int tc_npad(int m)
+{
+    return m <= 64 ? int((m + 15) / 16) * 16 : m <= 96 ? 96 : m <= 128 ? 128 : m <= 192 ? 192 : 256;
+}
+W8_HD constexpr int tc_occ(int npad) { return npad <= 64 ? kTcCtasPerSm : 1; }
+
 // Stage slots of the tensor-memory kernel in shared memory: nw weight stages
 // (8 row tiles x 4 K blocks of packed runs, filled by bulk copies) and nb
-// activation stages (4 K blocks x npad tokens), about 100 KB per CTA so that
-// two CTAs share an SM.
+// activation stages (4 K blocks x npad tokens): about 100 KB per CTA up to 64
+// tokens (two CTAs share an SM), about 200 KB above.
 struct TcStages {
     int nw, nb;
 };
 W8_HD constexpr TcStages tc_stages(bool fp8, int npad)
 {
     return fp8 ? (npad <= 16 ? TcStages{5, 6} : npad <= 32 ? TcStages{4, 5}
-                  : npad <= 48 ? TcStages{4, 3} : TcStages{3, 3})
+                  : npad <= 48 ? TcStages{4, 3} : npad <= 64 ? TcStages{3, 3}
+                  : npad <= 96 ? TcStages{5, 5} : npad <= 128 ? TcStages{5, 4}
+                  : npad <= 192 ? TcStages{4, 3} : TcStages{4, 2})
                : (npad <= 16 ? TcStages{3, 2} : npad <= 32 ? TcStages{2, 4}
-                  : npad <= 48 ? TcStages{2, 3} : TcStages{2, 2});
+                  : npad <= 48 ? TcStages{2, 3} : npad <= 64 ? TcStages{2, 2}
+                  : npad <= 96 ? TcStages{3, 4} : npad <= 128 ? TcStages{3, 3}
+                  : npad <= 192 ? TcStages{2, 3} : TcStages{2, 2});
 }
 W8_HD constexpr int tc_smem_bytes(bool fp8, int npad)
 {
@@ -195,18 +211,22 @@ inline Plan make_tc_plan(int64_t n, int64_t k, int m, int sm_count)
 {
     Plan p{};
     p.tc = true;
-    p.npad = int(ceil_div(m, 16) * 16);
+    p.npad = tc_npad(m);
     p.nt = p.npad / 8;
     p.r = 8;  // row tiles per CTA
     p.dw = tc_stages(true, p.npad).nw * kTcStageBlocks; // weight blocks staged ahead (FP8)
-    p.occ = kTcCtasPerSm;
+    p.occ = tc_occ(p.npad);
     p.wk = 1;
     p.rt = ceil_div(n, kTileN);
     p.kb = ceil_div(k, kTileK);
     const int64_t rbs = ceil_div(n, 128);
-    const int64_t target = int64_t(sm_count > 0 ? sm_count : 1) * kTcCtasPerSm;
+    const int64_t target = int64_t(sm_count > 0 ? sm_count : 1) * p.occ;
     // the splits of a row block form one thread-block cluster: a power of two
     // up to 8 (the portable cluster size) that keeps one stage per split
+    // Powers of two until about the resident CTAs are busy.  (Counts of 3 or
+    // 6 that would fill every SM with one CTA each measured slower: o_proj at
+    // 96 tokens 49.5 -> 68.8 us with clusters of 6, the clusters not all
+    // resident at once.)
     int splits = 1;
     while (splits < kTcMaxSplits && rbs * splits * 2 <= target &&
            p.kb / (int64_t(splits) * 2) >= kTcStageBlocks)
@@ -223,7 +243,7 @@ inline Plan make_tc_plan(int64_t n, int64_t k, int m, int sm_count)
     p.row_groups = int(rbs);
     p.grid = int(rbs * splits);
     p.kbs_max = int(ceil_div(p.kb, splits));
-    p.smem = tc_smem_bytes(true, p.npad); // the FP8 instance; bf16 stages are as large
+    p.smem = tc_smem_bytes(true, p.npad); // the FP8 instance (bf16: its own table)
     p.ws_counters = p.ws_bytes = 0; // partial sums stay on chip (cluster exchange)
     return p;
 }
@@ -232,8 +252,12 @@ inline Plan make_tc_plan(int64_t n, int64_t k, int m, int sm_count)
 // the tensor-memory kernel wins from 17 tokens on planes with many row blocks
 // (o_proj, q_b, kv_b), where one activation tile serves 128 rows; the register
 // ring wins below that and on planes with few rows, where the tc kernel's
-// fixed cost per CTA and its cluster reduction dominate.
-inline bool use_tc(int64_t n, int m) { return m >= kTcMinM && ceil_div(n, 128) >= kTcMinRowBlocks; }
+// fixed cost per CTA and its cluster reduction dominate.  Above 64 tokens
+// only the tensor-memory kernel runs.
+inline bool use_tc(int64_t n, int m)
+{
+    return m > kMaxRingM || (m >= kTcMinM && ceil_div(n, 128) >= kTcMinRowBlocks);
+}
 
 inline Plan make_plan(int64_t n, int64_t k, int m, int sm_count)
 {

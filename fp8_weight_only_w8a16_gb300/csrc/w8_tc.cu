@@ -71,13 +71,20 @@ __device__ int g_tc_status;
 namespace {
 
 constexpr int kTcKs = 4;         // K blocks per stage
-constexpr int kTcStages = 3;     // stage slots
+// Tensor memory of one CTA: the accumulator D in columns [0, NPAD) -- 64
+// columns reserved up to 64 tokens -- then A stages of 64 columns (4 K
+// blocks x 16): 3 in 256 columns up to 64 tokens (two CTAs share an SM's 512
+// columns), up to 4 in 512 columns above.
+W8_HD constexpr int tc_tmem_cols(int npad) { return npad <= 64 ? 256 : 512; }
+W8_HD constexpr int tc_acol(int npad) { return npad <= 64 ? 64 : npad; }
+W8_HD constexpr int tc_a_stages(int npad)
+{
+    return (tc_tmem_cols(npad) - tc_acol(npad)) / 64 < 4 ? (tc_tmem_cols(npad) - tc_acol(npad)) / 64 : 4;
+}
 constexpr int kTcThreads = kTcThreadsPerCta; // 8 converters, activations, issuer, weights
 static_assert(kTcThreads == 352, "eleven warps");
 constexpr int kWarpAct = 8, kWarpIssue = 9, kWarpW = 10;
 static_assert(kTcKs == kTcStageBlocks, "the planner's stage size");
-constexpr int kTmemCols = 256;   // D: [0, 64); A stages: [64, 256)
-constexpr int kACol = 64;
 constexpr uint32_t kSpinLimit = 1u << 24;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -314,13 +321,16 @@ __device__ __forceinline__ float4 cluster_sum4(uint32_t off, int splits, int ran
 }
 
 template <bool kFp8, int NPAD>
-__global__ void __launch_bounds__(kTcThreads, 2)
+__global__ void __launch_bounds__(kTcThreads, tc_occ(NPAD))
     tc_gemv_kernel(const GemvArgs a, const __grid_constant__ CUtensorMap tmx)
 {
     constexpr int kRun = kFp8 ? kRunFp8 : kRunBf16;
     constexpr int kNW = tc_stages(kFp8, NPAD).nw; // weight stages (shared memory)
     constexpr int kNB = tc_stages(kFp8, NPAD).nb; // activation stages (shared memory)
-    constexpr int kNA = kTcStages;                // A stages (tensor memory)
+    constexpr int kNA = tc_a_stages(NPAD);        // A stages (tensor memory)
+    constexpr uint32_t kTmemCols = tc_tmem_cols(NPAD);
+    constexpr int kACol = tc_acol(NPAD);
+    static_assert(kNA >= 3 && kACol + kNA * 64 <= int(kTmemCols) && kACol >= NPAD, "tensor memory map");
     constexpr int kTileW = kTcKs * kRun;          // one row tile's runs of a stage
     constexpr int kStageW = 8 * kTileW;
     constexpr int kBlockB = NPAD * 64;            // activation bytes of one K block
@@ -332,8 +342,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     // instruction descriptor: D f32, A and B bf16, both K-major, N = NPAD, M = 128
     constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(NPAD >> 3) << 17) |
                                 (uint32_t(128 >> 4) << 24);
-    static_assert(NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 64, "M = 128 needs N in 16..256, step 16");
-    static_assert(128 * kRedPitch * 4 <= kNW * kStageW, "the exchange tile reuses the weight stages");
+    static_assert(NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 256, "M = 128 needs N in 16..256, step 16");
+    static_assert(128 * kRedPitch * 4 <= tc_smem_bytes(kFp8, NPAD),
+                  "the exchange tile reuses the stages' shared memory");
     static_assert(kNW * kStageW + kNB * kStageB == tc_smem_bytes(kFp8, NPAD), "stage geometry");
 
     extern __shared__ __align__(1024) uint8_t s_dyn[]; // kNW weight stages, then kNB B stages
@@ -583,10 +594,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         }
     } else {
         // Split K across the CTAs of a cluster (rank = split): each CTA parks
-        // its partial tile in its own shared memory (the weight stages are
-        // free: every step has completed), then rank r adds the splits of rows
+        // its partial tile in its own shared memory (the stages are free:
+        // every step has completed and every copy has landed), then rank r adds the splits of rows
         // [r R, (r+1) R) in split order, reading the others' tiles directly.
-        float *red = reinterpret_cast<float *>(s_w);
+        float *red = reinterpret_cast<float *>(s_dyn);
         if (warp < 4) {
             float4 *dst = reinterpret_cast<float4 *>(red + (32 * warp + lane) * kRedPitch);
 #pragma unroll
@@ -602,17 +613,18 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         __syncwarp(); // the cluster barrier is warp-aligned: reconverge first
         asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
         pdl_wait();
-        const int rows_per = 128 / a.splits; // splits divides 128 (a power of two <= 8)
+        const int r_lo = (sp * 128) / a.splits; // split sp adds rows [r_lo, r_lo + rows_per)
+        const int rows_per = ((sp + 1) * 128) / a.splits - r_lo;
         const int items = rows_per * (NPAD / 4);
         const uint32_t red_local = smem_u32(red);
         for (int it = threadIdx.x; it < items; it += kTcThreads) {
             const int q = it / rows_per;           // token quad
-            const int rl = sp * rows_per + (it - q * rows_per);
+            const int rl = r_lo + (it - q * rows_per);
             const int orow = row0 + rl;
             if (4 * q >= a.m || orow >= a.n)
                 continue;
             if (a.act == kActSiluMul && (rl & 8))
-                continue; // an up row: added with its gate row (rl - 8)
+                continue; // an up row: added with its gate row (rl - 8), whichever split has it
             const uint32_t off = red_local + uint32_t((rl * kRedPitch + 4 * q) * 4);
             const float4 v = cluster_sum4(off, a.splits, g * a.splits);
             const float sc = kFp8 ? __ldg(a.scale + orow) : 1.0f;
@@ -662,15 +674,20 @@ void *tc_instance(int npad)
     case 32: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 32>);
     case 48: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 48>);
     case 64: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 64>);
+    case 96: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 96>);
+    case 128: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 128>);
+    case 192: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 192>);
+    case 256: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 256>);
     default: return nullptr;
     }
 }
+constexpr int kTcNpads[] = {16, 32, 48, 64, 96, 128, 192, 256};
 
 } // namespace
 
 cudaError_t prepare_tc_kernels()
 {
-    for (int npad = 16; npad <= 64; npad += 16) {
+    for (int npad : kTcNpads) {
         for (int f = 0; f < 2; ++f) {
             void *fn = f ? tc_instance<true>(npad) : tc_instance<false>(npad);
             cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,

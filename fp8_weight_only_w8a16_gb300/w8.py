@@ -24,7 +24,7 @@ LIB_PATH = build_lib.LIB
 DT_E4M3FN, DT_BF16, DT_E4M3FNUZ, DT_E5M2, DT_FP16 = 1, 2, 3, 4, 5
 SRC_ROW_MAJOR, SRC_GATE_UP = 0, 1
 LAYOUT_MMA_16x32, LAYOUT_MMA_16x32_GATE_UP = 1, 2
-MAX_M = 64
+MAX_M = 256
 
 STATUS = {
     0: "W8_OK", 1: "W8_ERR_NULL", 2: "W8_ERR_DTYPE", 3: "W8_ERR_UNPADDED", 4: "W8_ERR_BIAS",

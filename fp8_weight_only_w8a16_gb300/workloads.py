@@ -71,18 +71,27 @@ LM_HEAD = Projection("lm_head", 154880, 6144, "bf16", (1,))
 # instead of two, rows 0..127 = wk, 128..159 = weights_proj.
 WK_WEIGHTS_PROJ = Projection("indexer_wk_weights_proj", 160, 6144, "bf16", SWEEP_M)
 
+# Above the decode range: draft rows and prefill chunks of 96..256 tokens on
+# the largest attention projections (the tensor-memory kernel only).
+LARGE_M = (96, 128, 192, 256)
+O_PROJ_LARGE_M = Projection("o_proj_large_m", 6144, 16384, "e4m3fn", LARGE_M)
+Q_B_LARGE_M = Projection("q_b_proj_large_m", 16384, 2048, "e4m3fn", LARGE_M)
+KV_B_LARGE_M = Projection("kv_b_proj_large_m", 28672, 512, "e4m3fn", LARGE_M)
+
 ALL = (TINY, FUSED_QKV_A, O_PROJ, O_PROJ_BF16, SHARED_GATE_UP, SHARED_DOWN,
-       SHARED_GATE_UP_KPAD, SHARED_GATE_UP_SILU, Q_B, KV_B, WQ_B, WK, WEIGHTS_PROJ, WK_WEIGHTS_PROJ, LM_HEAD)
+       SHARED_GATE_UP_KPAD, SHARED_GATE_UP_SILU, Q_B, KV_B, WQ_B, WK, WEIGHTS_PROJ, WK_WEIGHTS_PROJ, LM_HEAD,
+       O_PROJ_LARGE_M, Q_B_LARGE_M, KV_B_LARGE_M)
 BY_NAME = {p.name: p for p in ALL}
 
-# The five workload groups, in order: the tiny correctness case, the fused
+# The workload groups, in order: the tiny correctness case, the fused
 # qkv_a projection, o_proj (FP8 and bf16), the shared-expert pair with its
-# K-padded variant and its gate_up with SiLU-and-multiply, and the full-layer
-# sweep.
+# K-padded variant and its gate_up with SiLU-and-multiply, the full-layer
+# sweep, and 96..256 tokens on the large attention projections.
 GROUPS = {
     "tiny": (TINY,),
     "fused_qkv_a_proj": (FUSED_QKV_A,),
     "o_proj": (O_PROJ, O_PROJ_BF16),
     "shared_expert": (SHARED_GATE_UP, SHARED_DOWN, SHARED_GATE_UP_KPAD, SHARED_GATE_UP_SILU),
     "layer_sweep": (Q_B, KV_B, WQ_B, WK, WEIGHTS_PROJ, WK_WEIGHTS_PROJ, LM_HEAD),
+    "large_m": (O_PROJ_LARGE_M, Q_B_LARGE_M, KV_B_LARGE_M),
 }

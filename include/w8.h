@@ -57,7 +57,7 @@ typedef enum {
                              of 16 bytes */
     W8_ERR_BIAS = 4,      /* a bias pointer was given: the GEMV has no bias */
     W8_ERR_MIXED = 5,     /* bf16 and FP8 planes mixed in one build */
-    W8_ERR_SHAPE = 6,     /* N or K < 1 or too large, ldw < K, M outside 0..64,
+    W8_ERR_SHAPE = 6,     /* N or K < 1 or too large, ldw < K, M outside 0..256,
                              ldx < K, ldy < N (< N/2 for w8_gemv_silu_mul), or a
                              W8_SRC_GATE_UP plane whose N is not a multiple of 16 */
     W8_ERR_SCALE = 7,     /* an FP8 plane without row scales, or a bf16 plane with them */
@@ -135,12 +135,13 @@ typedef struct {
 } w8_plane_info;
 
 /* The launch a gemv call makes for one (plane, m); returned for inspection.
- * kernel 0 (m <= 16, or a plane of fewer than 48 blocks of 128 rows): the
- *   register-ring kernel, 8 warps per CTA.
- * kernel 1 (m >= 17 on a plane of at least 48 blocks of 128 rows): the
- *   tensor-memory kernel, 128 rows x one K range per CTA;
- *   there n_tiles = tokens rounded up to 16, over 8; row_tiles_per_warp = the
- *   CTA's 8 row tiles; warps_k = 1; depth = the converter warps' ring depth. */
+ * kernel 0 (m <= 16, or m <= 64 on a plane of fewer than 48 blocks of 128
+ *   rows): the register-ring kernel, 8 warps per CTA.
+ * kernel 1 (m >= 17 on a plane of at least 48 blocks of 128 rows, and every
+ *   m >= 65): the tensor-memory kernel, 128 rows x one K range per CTA;
+ *   there n_tiles = tokens rounded up to 16 (to 96, 128, 192 or 256 above
+ *   64), over 8; row_tiles_per_warp = the CTA's 8 row tiles; warps_k = 1;
+ *   depth = the weight blocks staged ahead. */
 typedef struct {
     int32_t kernel;          /* 0: register ring (mma.sync), 1: tensor memory (tcgen05) */
     int32_t grid;            /* CTAs */
@@ -203,7 +204,7 @@ void w8_release(w8_build *b);
 int w8_build_planes(const w8_build *b);
 w8_status w8_build_info(const w8_build *b, int plane, w8_plane_info *info);
 
-/* The launch plan of a gemv call on this plane with m tokens (1..64). */
+/* The launch plan of a gemv call on this plane with m tokens (1..256). */
 w8_status w8_plan_info(const w8_build *b, int plane, int m, w8_plan *plan);
 
 /* The same plan for a plane of n rows and k columns on a GPU with sm_count
@@ -213,7 +214,7 @@ w8_status w8_plan_shape(int64_t n, int64_t k, int m, int sm_count, w8_plan *plan
 
 /* Workspace bytes a gemv call on `plane` with `m` tokens needs (0 if none).
  * plane = -1 takes the largest over all planes, m = 0 the largest over
- * m = 1..64, so one workspace can serve every call of a build.
+ * m = 1..256, so one workspace can serve every call of a build.
  *
  * Workspace contract: 256-byte aligned device memory, zero-filled once by the
  * caller before its first use (its head holds arrival counters that every
@@ -226,7 +227,8 @@ w8_status w8_workspace_bytes(const w8_build *b, int plane, int m, size_t *bytes)
  * x: device bf16 [m][ldx], ldx >= K, ldx % 8 == 0, 16-byte aligned (every
  *    row is read with 16-byte loads; columns K..ldx-1 are never read);
  * y: device bf16 [m][ldy], ldy >= N, written for n < N only;
- * m: decode tokens, 0..64 (0 is a no-op);
+ * m: tokens, 0..256 (0 is a no-op): decode steps up to 64, draft rows and
+ *    prefill chunks above (the tensor-memory kernel runs every call of 65..256);
  * workspace / workspace_bytes: see w8_workspace_bytes (may be NULL / 0 when
  *    that returns 0).
  * Returns W8_ERR_DTYPE on a bf16 build.  One kernel launch on s. */

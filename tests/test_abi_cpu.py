@@ -172,24 +172,28 @@ SHAPES = [(256, 512), (2624, 6144), (6144, 16384), (4096, 6144), (6144, 2048),
 
 
 @pytest.mark.parametrize("n,k", SHAPES)
-@pytest.mark.parametrize("m", [1, 2, 4, 8, 9, 16, 17, 32, 33, 64])
+@pytest.mark.parametrize("m", [1, 2, 4, 8, 9, 16, 17, 32, 33, 64, 65, 96, 97, 128, 200, 256])
 def test_plan_invariants(n, k, m):
     p = w8.plan_shape(n, k, m, 152)
     kb = -(-k // 32)
     rt = -(-n // 16)
     assert p.grid == p.row_groups * p.splits
-    assert p.kernel == (1 if m >= 17 and -(-n // 128) >= 48 else 0)
+    assert p.kernel == (1 if m > 64 or (m >= 17 and -(-n // 128) >= 48) else 0)
     if p.kernel == 1:
         # the tensor-memory kernel: 128 rows x one K range per CTA, tokens
         # padded to 16, about two CTAs per SM, at least one 4-block stage per split
         assert p.kernel == 1 and p.block == 352
-        assert p.row_groups == -(-n // 128) and p.n_tiles * 8 == -(-m // 16) * 16
+        npad = -(-m // 16) * 16 if m <= 64 else min(x for x in (96, 128, 192, 256) if x >= m)
+        assert p.row_groups == -(-n // 128) and p.n_tiles * 8 == npad
         assert p.splits in (1, 2, 4, 8) and (p.splits == 1 or kb // p.splits >= 4)
         assert p.grid <= 2 * 152 or p.splits == 1
         assert p.k_blocks_per_warp_max == -(-kb // p.splits)
-        npad = p.n_tiles * 8
-        nw, nb = {16: (5, 6), 32: (4, 5), 48: (4, 3), 64: (3, 3)}[npad]  # FP8 stage slots
-        assert p.smem_bytes == nw * 8 * 4 * 512 + nb * 4 * npad * 64 <= 104 * 1024
+        nw, nb = {16: (5, 6), 32: (4, 5), 48: (4, 3), 64: (3, 3), 96: (5, 5), 128: (5, 4),
+                  192: (4, 3), 256: (4, 2)}[npad]  # FP8 stage slots
+        # about 100 KB (two CTAs per SM) up to 64 tokens, about 200 KB (one) above
+        limit = 104 * 1024 if npad <= 64 else 208 * 1024
+        assert p.smem_bytes == nw * 8 * 4 * 512 + nb * 4 * npad * 64 <= limit
+        assert p.grid <= (2 if npad <= 64 else 1) * 152 or p.splits == 1
         assert p.workspace_bytes == 0  # split partials meet on chip
         return
     assert p.block == 256
@@ -224,7 +228,7 @@ def test_plan_does_not_depend_on_anything_but_shape():
 
 
 def test_plan_refuses_bad_shapes():
-    for args in [(0, 32, 1, 152), (16, 0, 1, 152), (16, 32, 0, 152), (16, 32, 65, 152),
+    for args in [(0, 32, 1, 152), (16, 0, 1, 152), (16, 32, 0, 152), (16, 32, 257, 152),
                  (16, 32, 1, 0)]:
         with pytest.raises(w8.W8Error) as e:
             w8.plan_shape(*args)

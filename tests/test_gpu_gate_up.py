@@ -85,7 +85,8 @@ def _case(seed, n, k, m, dtype="e4m3fn"):
 # (2I, K, m): register-ring plans with and without split K, tensor-memory
 # plans (m >= 17 on >= 48 blocks of 128 rows) with and without a cluster
 GATED_SHAPES = [(16, 32, 1), (64, 96, 3), (160, 1000, 8), (32, 6144, 5), (4096, 6144, 8),
-                (512, 3000, 16), (6144, 1024, 32), (6144, 2048, 20), (7168, 512, 64)]
+                (512, 3000, 16), (6144, 1024, 32), (6144, 2048, 20), (7168, 512, 64),
+                (512, 700, 100), (7168, 512, 256)]
 
 
 @pytest.mark.parametrize("dtype", ["e4m3fn", "bf16"])

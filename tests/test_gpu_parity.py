@@ -338,9 +338,9 @@ def test_workspace_reuse_graph_replay_and_errors(w8):
     with pytest.raises(w8.W8Error) as e:
         w8.w8_gemv(b, 1, xd, yd2, ws)
     assert e.value.name == "W8_ERR_PLANE"
-    big = torch.zeros((65, 6144), dtype=torch.int16, device=dev())
+    big = torch.zeros((257, 6144), dtype=torch.int16, device=dev())
     with pytest.raises(w8.W8Error) as e:
-        w8.w8_gemv(b, 0, big, torch.zeros((65, 128), dtype=torch.int16, device=dev()), ws)
+        w8.w8_gemv(b, 0, big, torch.zeros((257, 128), dtype=torch.int16, device=dev()), ws)
     assert e.value.name == "W8_ERR_SHAPE"
     with pytest.raises(w8.W8Error) as e:   # output row stride shorter than N
         w8.w8_gemv(b, 0, xd, torch.zeros((8, 100), dtype=torch.int16, device=dev()), ws)
@@ -483,3 +483,78 @@ def test_lm_head_full_size_sampled(w8):
     rng = np.random.default_rng(2)
     rows = np.unique(np.concatenate([rng.choice(proj.n, 128, replace=False), [0, proj.n - 1]]))
     _check_tol(plane, x, y, rows)
+
+
+# ---------------------------------------------------------------------------
+# 65..256 tokens: draft rows and prefill chunks, tensor-memory kernel only
+# ---------------------------------------------------------------------------
+
+LARGE_M = [(300, 700, 100), (100, 64, 200), (256, 512, 65), (6144, 2048, 128),
+           (6144, 1000, 192), (2624, 6144, 256), (28672, 512, 256)]
+
+
+@pytest.mark.parametrize("dtype", ["e4m3fn", "bf16"])
+@pytest.mark.parametrize("n,k,m", LARGE_M)
+def test_large_token_counts_within_tolerance(w8, dtype, n, k, m):
+    """Above 64 tokens every call runs the tensor-memory kernel with the
+    tokens padded to 96, 128, 192 or 256 (one CTA per SM, 512 TMEM columns),
+    split K in clusters and shared activation tiles where the plan has them;
+    ragged N, K and token counts; sampled rows on the large planes."""
+    plane, x = _case(n + k + m, n, k, m, dtype)
+    b, _src = bind_plane(w8, plane)
+    p = b.plan(0, m)
+    assert p.kernel == 1 and p.workspace_bytes == 0
+    w8.device_status(reset=True)
+    y = run_gemv(w8, b, 0, x, n, fp8=(dtype == "e4m3fn"))
+    rows = None
+    if n >= 2000:
+        rng = np.random.default_rng(5)
+        rows = np.unique(np.concatenate([rng.choice(n, 96, replace=False), [0, 127, 128, n - 1]]))
+    _check_tol(plane, x, y, rows)
+    assert w8.device_status() == 0
+
+
+@pytest.mark.parametrize("n,k,m", [(6144, 256, 128), (6144, 256, 256), (300, 700, 97),
+                                   (2624, 512, 200)])
+def test_large_token_counts_exact_sums_bit_exact(w8, n, k, m):
+    rng = np.random.default_rng(n * 3 + k + m)
+    plane, x = _exact_sum_case(rng, n, k, m)
+    b, _src = bind_plane(w8, plane)
+    y = run_gemv(w8, b, 0, x, n)
+    assert oracle.same_values(y, oracle.gemv(plane.w, DT8, plane.scale, x))
+
+
+@pytest.mark.parametrize("m", [128, 256])
+def test_large_token_counts_unit_scale_fp8_equals_bf16(w8, m):
+    plane, x = _case(77, 6144, 2048, m)
+    unit = synth.Plane("e4m3fn", plane.n, plane.k, plane.ldw, plane.w,
+                       np.ones(plane.n, dtype=np.float32))
+    wide = _widened_bf16_plane(unit)
+    b8, _s8 = bind_plane(w8, unit)
+    b16, _s16 = bind_plane(w8, wide)
+    y8 = run_gemv(w8, b8, 0, x, plane.n)
+    y16 = run_gemv(w8, b16, 0, x, plane.n, fp8=False)
+    assert oracle.same_values(y8, y16)
+
+
+def test_large_token_counts_graph_replay(w8):
+    n, k, m = 6144, 1024, 256
+    plane, x = _case(91, n, k, m)
+    b, _src = bind_plane(w8, plane)
+    w8.device_status(reset=True)
+    y1 = run_gemv(w8, b, 0, x, n)
+    xd = to_dev(x)
+    yd = torch.zeros((m, n), dtype=torch.int16, device=dev())
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        w8.w8_gemv(b, 0, xd, yd, None, stream=s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        w8.w8_gemv(b, 0, xd, yd, None)
+    yd.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(from_dev(yd), y1)
+    assert w8.device_status() == 0

@@ -209,3 +209,15 @@ def test_threads_do_not_change_the_result(orc):
     y1 = orc.gemv(plane.w, DT8, plane.scale, x, threads=1)
     y4 = orc.gemv(plane.w, DT8, plane.scale, x, threads=4)
     assert np.array_equal(y1, y4)
+
+
+def test_workload_inputs_cover_every_token_count():
+    # every workload's activations hold as many rows as its largest M, and
+    # drawing more rows leaves the first ones unchanged
+    from fp8_weight_only_w8a16_gb300 import synth, workloads
+
+    mmax = max(max(p.ms) for p in workloads.ALL)
+    _p, x = synth.workload(16, 64, seed=0)
+    assert x.shape[0] >= mmax
+    _p, x64 = synth.workload(16, 64, seed=0, x_rows=64)
+    assert np.array_equal(x[:64], x64)

@@ -42,7 +42,8 @@ def w8():
 # (n, k, m): register-ring plans that split K across CTAs (and so use the
 # scratch), a tensor-memory plan (its split partials meet on chip: no scratch)
 # and a large plane whose plan does not split
-CASES = [(128, 2048, 16), (32, 6144, 12), (40, 6144, 5), (6144, 1024, 32), (2624, 6144, 4)]
+CASES = [(128, 2048, 16), (32, 6144, 12), (40, 6144, 5), (6144, 1024, 32), (2624, 6144, 4),
+         (256, 512, 100)]
 
 
 @pytest.mark.parametrize("n,k,m", CASES)
