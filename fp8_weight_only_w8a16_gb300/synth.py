@@ -13,7 +13,13 @@ library routines:
   an fp32 scale per row"): scale[n] = amax_n / 448 in fp32 (an all-zero row
   gets scale 1), codes = E4M3(W / scale) clamped to +-448 and rounded through
   ``torch.float8_e4m3fn`` (round to nearest even);
-* bf16 planes: fp32 -> bf16 through torch.
+* bf16 planes: fp32 -> bf16 through torch;
+* MXFP4 planes (w4a16; the OCP microscaling format the Model Support Guide's
+  FP4 GEMMs use): per row and 32-column block, the shared exponent is
+  floor(log2(amax)) - 2 (E2M1's largest exponent), stored as E8M0 (bias 127;
+  an all-zero block gets 127); elements = W / 2^exponent rounded to the
+  nearest E2M1 value (ties to the even code), saturating at +-6; two codes per
+  byte, the even column in the low nibble.
 
 Draw order per workload: the weight plane first, then a [64, K] activation
 block whose first M rows are the M decode tokens, so every M of one workload
@@ -35,12 +41,14 @@ X_ROWS = 256  # largest token count of the workloads (rows are drawn row-major, 
 class Plane:
     """A source weight plane as a checkpoint would hold it (row-major)."""
 
-    dtype: str            # "e4m3fn" or "bf16"
+    dtype: str            # "e4m3fn", "bf16" or "mxfp4"
     n: int
     k: int                # logical columns
     ldw: int              # row stride in elements (>= k); columns k..ldw-1 are zero
-    w: np.ndarray         # [n, ldw] uint8 codes or uint16 bf16 bits
-    scale: np.ndarray | None  # [n] fp32 row scales (FP8 only)
+    w: np.ndarray         # [n, ldw] uint8 codes or uint16 bf16 bits; MXFP4: [n, ldw / 2]
+                          # bytes of two codes (even column in the low nibble)
+    scale: np.ndarray | None  # [n] fp32 row scales (FP8); MXFP4: [n, ceil(k / 32)]
+                              # E8M0 block scales (uint8); None for bf16
 
 
 def _normal(rng: np.random.Generator, shape, std: float) -> np.ndarray:
@@ -66,6 +74,36 @@ def quantize_ptpc_fp8(w: np.ndarray):
     return codes.numpy().copy(), scale.numpy().astype(np.float32)
 
 
+# E2M1 magnitudes by code (sign in bit 3): the values an MXFP4 element takes.
+_E2M1_MAGNITUDES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.float64)
+
+
+def quantize_mxfp4(w: np.ndarray, block: int = 32):
+    """fp32 [n, k] -> (packed codes uint8 [n, ceil(k/2)], E8M0 scales uint8 [n, ceil(k/32)])."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    n, k = w.shape
+    nb = -(-k // block)
+    wp = np.zeros((n, nb * block), dtype=np.float64)
+    wp[:, :k] = w
+    blocks = wp.reshape(n, nb, block)
+    amax = np.abs(blocks).max(axis=2)
+    with np.errstate(divide="ignore"):
+        ex = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 2, 0)
+    ex = np.clip(ex, -127, 127).astype(np.int64)
+    scales = (ex + 127).astype(np.uint8)
+    v = blocks / np.ldexp(1.0, ex)[:, :, None]
+    mag = np.minimum(np.abs(v), 6.0)
+    dist = np.abs(mag[..., None] - _E2M1_MAGNITUDES)
+    # nearest magnitude; on a tie the even code (an exact midpoint sits between
+    # an even and an odd code)
+    best = np.argmin(dist * 4 + (np.arange(8) & 1) * 1e-9, axis=-1)
+    codes = (best | np.where(v < 0, 8, 0)).astype(np.uint8).reshape(n, nb * block)[:, :k]
+    if k % 2:
+        codes = np.concatenate([codes, np.zeros((n, 1), np.uint8)], axis=1)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    return packed, scales
+
+
 def weight_plane(rng: np.random.Generator, n: int, k: int, dtype: str = "e4m3fn",
                  ldw: int | None = None, std: float = 0.02) -> Plane:
     ldw = k if ldw is None else ldw
@@ -80,6 +118,12 @@ def weight_plane(rng: np.random.Generator, n: int, k: int, dtype: str = "e4m3fn"
         w = np.zeros((n, ldw), dtype=np.uint16)
         w[:, :k] = to_bf16_bits(w32)
         return Plane("bf16", n, k, ldw, w, None)
+    if dtype == "mxfp4":
+        assert ldw % 2 == 0
+        packed, scales = quantize_mxfp4(w32)
+        w = np.zeros((n, ldw // 2), dtype=np.uint8)
+        w[:, :packed.shape[1]] = packed
+        return Plane("mxfp4", n, k, ldw, w, scales)
     raise ValueError(dtype)
 
 

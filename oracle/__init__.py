@@ -13,11 +13,12 @@ multiplies each reduced row before the bf16 rounding.  ``brute.py`` is an
 independent numpy fp64 recompute used to pin it.  It also holds the MLP
 activation that follows a merged gate_up projection (ATOM Model Support
 Guide, Model architecture details, Llama MLP): h = silu(g) * u in fp64 with
-one bf16 rounding.
+one bf16 rounding, and the w4a16 GEMV on MXFP4 weights (E2M1 elements, E8M0
+scales per 32 along K).
 
 Every function here is pinned by a ``-m "not gpu"`` test
 (tests/test_oracle_codecs.py, tests/test_oracle_gemv.py,
-tests/test_oracle_silu.py).
+tests/test_oracle_silu.py, tests/test_oracle_mxfp4.py).
 """
 from __future__ import annotations
 
@@ -67,6 +68,16 @@ def _declare(lib):
     lib.orc_f64_to_bf16_rne.restype = ctypes.c_uint16
     lib.orc_silu_mul_f64.argtypes = [vp, vp, c_i64, vp]
     lib.orc_silu_mul_f64.restype = ctypes.c_int
+    lib.orc_e2m1_to_f32.argtypes = [ctypes.c_uint8]
+    lib.orc_e2m1_to_f32.restype = ctypes.c_float
+    lib.orc_e8m0_to_f32.argtypes = [ctypes.c_uint8]
+    lib.orc_e8m0_to_f32.restype = ctypes.c_float
+    lib.orc_gemv_mxfp4.argtypes = [vp, c_i64, c_i64, c_i64, vp, c_i64, vp, c_i64, c_i64, vp,
+                                   c_i64, ctypes.c_int]
+    lib.orc_gemv_mxfp4.restype = ctypes.c_int
+    lib.orc_gemv_mxfp4_f64.argtypes = [vp, c_i64, c_i64, c_i64, vp, c_i64, vp, c_i64, c_i64,
+                                       vp, vp, ctypes.c_int]
+    lib.orc_gemv_mxfp4_f64.restype = ctypes.c_int
     return lib
 
 
@@ -205,6 +216,48 @@ class Oracle:
         y = self.gemv(w, dtype, scale, x, k, threads)
         return self.silu_mul(y[:, : n // 2], y[:, n // 2:])
 
+    # ---- w4a16: MXFP4 weights -------------------------------------------
+    def e2m1_to_f32(self, code: int) -> float:
+        return float(self.lib.orc_e2m1_to_f32(int(code) & 0xF))
+
+    def e8m0_to_f32(self, code: int) -> float:
+        return float(self.lib.orc_e8m0_to_f32(int(code) & 0xFF))
+
+    @staticmethod
+    def _mxfp4_args(w, bs, x, k):
+        assert w.dtype == np.uint8 and w.ndim == 2 and w.strides[1] == 1
+        assert bs.dtype == np.uint8 and bs.ndim == 2 and bs.strides[1] == 1
+        assert x.dtype == np.uint16 and x.ndim == 2 and x.strides[1] == 2
+        n, ldw_bytes = w.shape[0], w.strides[0]
+        k = 2 * w.shape[1] if k is None else k
+        assert k <= 2 * w.shape[1] and bs.shape[0] == n and 32 * bs.shape[1] >= k
+        return n, k, ldw_bytes, bs.strides[0], x.shape[0], x.strides[0] // 2
+
+    def gemv_mxfp4(self, w: np.ndarray, bs: np.ndarray, x: np.ndarray, k: int | None = None,
+                   threads: int = 1) -> np.ndarray:
+        """y = bf16(sum_k e2m1(W) * 2^(bs - 127) * x) in fp32, ascending k; uint16 [m, n].
+
+        ``w``: [n, >=k/2] bytes, two codes each (even column in the low
+        nibble); ``bs``: [n, >=ceil(k/32)] E8M0 block scales; ``x``: [m, >=k].
+        """
+        n, k, ldw, ldb, m, ldx = self._mxfp4_args(w, bs, x, k)
+        y = np.zeros((m, n), dtype=np.uint16)
+        if self.lib.orc_gemv_mxfp4(_ptr(w), n, k, ldw, _ptr(bs), ldb, _ptr(x), ldx, m, _ptr(y), n,
+                                   int(threads)) != 0:
+            raise ValueError("orc_gemv_mxfp4 rejected its arguments")
+        return y
+
+    def gemv_mxfp4_f64(self, w: np.ndarray, bs: np.ndarray, x: np.ndarray, k: int | None = None,
+                       threads: int = 1):
+        """fp64 recompute: (y64 [m,n], mag64 [m,n] = sum|W x|)."""
+        n, k, ldw, ldb, m, ldx = self._mxfp4_args(w, bs, x, k)
+        y64 = np.zeros((m, n), dtype=np.float64)
+        mag = np.zeros((m, n), dtype=np.float64)
+        if self.lib.orc_gemv_mxfp4_f64(_ptr(w), n, k, ldw, _ptr(bs), ldb, _ptr(x), ldx, m,
+                                       _ptr(y64), _ptr(mag), int(threads)) != 0:
+            raise ValueError("orc_gemv_mxfp4_f64 rejected its arguments")
+        return y64, mag
+
     def max_threads(self) -> int:
         return int(self.lib.orc_max_threads())
 
@@ -264,6 +317,22 @@ def max_threads():
 
 def f64_to_bf16_rne(values):
     return _load().f64_to_bf16_rne(values)
+
+
+def e2m1_to_f32(code):
+    return _load().e2m1_to_f32(code)
+
+
+def e8m0_to_f32(code):
+    return _load().e8m0_to_f32(code)
+
+
+def gemv_mxfp4(w, bs, x, k=None, threads=1):
+    return _load().gemv_mxfp4(w, bs, x, k, threads)
+
+
+def gemv_mxfp4_f64(w, bs, x, k=None, threads=1):
+    return _load().gemv_mxfp4_f64(w, bs, x, k, threads)
 
 
 def silu_mul_f64(g, u):
@@ -373,5 +442,5 @@ __all__ = [
     "f32_to_bf16_rne", "f32_to_e4m3_sat", "quantize_rows", "gemv", "gemv_f64",
     "max_threads", "bf16_bits_to_f64", "within_tolerance", "same_values", "build_oracle",
     "f64_to_bf16_rne", "silu_mul_f64", "silu_mul", "gate_up_silu_mul", "SILU_LIPSCHITZ",
-    "silu_mul_within_tolerance",
+    "silu_mul_within_tolerance", "e2m1_to_f32", "e8m0_to_f32", "gemv_mxfp4", "gemv_mxfp4_f64",
 ]

@@ -302,3 +302,108 @@ int orc_silu_mul_f64(const double *g, const double *u, int64_t count, double *h)
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* w4a16: MXFP4 weights (E2M1 elements, E8M0 block scales)             */
+/* ------------------------------------------------------------------ */
+
+/* The ATOM Model Support Guide (Model-specific optimizations, DeepSeek
+ * V2/V3: FP4 support) names MXFP4 GEMMs with 16-bit activations
+ * ("a16wfp4"), and the GLM-5.2 anatomy page's verified deployments serve a
+ * GLM-5.2-MXFP4 checkpoint.  MXFP4 is the OCP
+ * microscaling format: 4-bit E2M1 elements, 32 consecutive elements along K
+ * sharing one 8-bit E8M0 scale.  This file's readings of what the pages leave
+ * open: two elements per byte, column 2i in the low nibble and 2i+1 in the
+ * high nibble; the block scales are a row-major [n][ldb] byte array, block
+ * j covering columns 32j .. 32j+31; no per-row scale on top. */
+
+/* E2M1 code (low 4 bits) -> value: sign bit 3, exponent bits 2..1 (bias 1),
+ * mantissa bit 0; exponent 0 is subnormal (m * 0.5); no infinity or NaN. */
+float orc_e2m1_to_f32(uint8_t c)
+{
+    int s = (c >> 3) & 1;
+    int e = (c >> 1) & 3;
+    int m = c & 1;
+    float v = (e == 0) ? 0.5f * (float)m : ldexpf(1.0f + 0.5f * (float)m, e - 1);
+    return s ? -v : v;
+}
+
+/* E8M0 scale -> value: 2^(e - 127); 255 is NaN. */
+float orc_e8m0_to_f32(uint8_t e)
+{
+    if (e == 255)
+        return NAN;
+    return ldexpf(1.0f, (int)e - 127);
+}
+
+/* Element (r, j) of an MXFP4 plane: code from its nibble times its block's
+ * scale.  The product is exact in fp32 (2 significant bits) unless it
+ * leaves fp32's range. */
+static float mxfp4_value(const uint8_t *w, int64_t ldw_bytes, const uint8_t *bs, int64_t ldb,
+                         int64_t r, int64_t j)
+{
+    uint8_t byte = w[r * ldw_bytes + j / 2];
+    uint8_t code = (j & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+    return orc_e2m1_to_f32(code) * orc_e8m0_to_f32(bs[r * ldb + j / 32]);
+}
+
+/* The w4a16 GEMV as the plain definition: y[i][r] = bf16_rne(sum_j
+ * W[r][j] x[i][j]), W[r][j] = e2m1(code) * e8m0(scale of block j / 32), fp32
+ * accumulation in ascending j.  w: [n][ldw_bytes] packed codes, bs: [n][ldb]
+ * E8M0 bytes (ldb >= ceil(k / 32)).  Returns 0, or -1 on a bad argument. */
+int orc_gemv_mxfp4(const uint8_t *w, int64_t n, int64_t k, int64_t ldw_bytes, const uint8_t *bs,
+                   int64_t ldb, const uint16_t *x, int64_t ldx, int64_t m, uint16_t *y,
+                   int64_t ldy, int threads)
+{
+    if (!w || !bs || !x || !y || n < 0 || k < 0 || m < 0 || 2 * ldw_bytes < k ||
+        32 * ldb < k || ldx < k || ldy < n)
+        return -1;
+#ifdef _OPENMP
+    if (threads < 1)
+        threads = 1;
+#pragma omp parallel for schedule(dynamic, 16) num_threads(threads)
+#endif
+    for (int64_t r = 0; r < n; ++r) {
+        for (int64_t i = 0; i < m; ++i) {
+            float acc = 0.0f;
+            for (int64_t j = 0; j < k; ++j) {
+                float p = mxfp4_value(w, ldw_bytes, bs, ldb, r, j) * orc_bf16_to_f32(x[i * ldx + j]);
+                acc = acc + p;
+            }
+            y[i * ldy + r] = orc_f32_to_bf16_rne(acc);
+        }
+    }
+    (void)threads;
+    return 0;
+}
+
+/* fp64 recompute of the same dequantized inputs for the tolerance checks:
+ * y64[i][r] = sum_j W x, mag64[i][r] = sum_j |W x| (both [m][n]). */
+int orc_gemv_mxfp4_f64(const uint8_t *w, int64_t n, int64_t k, int64_t ldw_bytes,
+                       const uint8_t *bs, int64_t ldb, const uint16_t *x, int64_t ldx, int64_t m,
+                       double *y64, double *mag64, int threads)
+{
+    if (!w || !bs || !x || !y64 || !mag64 || n < 0 || k < 0 || m < 0 || 2 * ldw_bytes < k ||
+        32 * ldb < k || ldx < k)
+        return -1;
+#ifdef _OPENMP
+    if (threads < 1)
+        threads = 1;
+#pragma omp parallel for schedule(dynamic, 16) num_threads(threads)
+#endif
+    for (int64_t r = 0; r < n; ++r) {
+        for (int64_t i = 0; i < m; ++i) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t j = 0; j < k; ++j) {
+                double p = (double)mxfp4_value(w, ldw_bytes, bs, ldb, r, j) *
+                           (double)orc_bf16_to_f32(x[i * ldx + j]);
+                acc += p;
+                mag += fabs(p);
+            }
+            y64[i * n + r] = acc;
+            mag64[i * n + r] = mag;
+        }
+    }
+    (void)threads;
+    return 0;
+}

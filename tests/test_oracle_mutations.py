@@ -19,6 +19,7 @@ from oracle.build import ORACLE_SRC, build_oracle
 
 from . import test_oracle_codecs as codecs
 from . import test_oracle_gemv as gemv_pins
+from . import test_oracle_mxfp4 as mxfp4_pins
 from . import test_oracle_silu as silu_pins
 
 MUTATIONS = {
@@ -44,8 +45,11 @@ MUTATIONS = {
     "rounding_truncates": ("if (dropped > 0x8000u)\n        up = 1;",
                            "if (dropped > 0x8000u)\n        up = 0;"),
     "bf16_widening_shift_wrong": ("(uint32_t)u << 16;", "(uint32_t)u << 15;"),
-    "accumulate_in_bf16": ("acc = acc + p;",
-                           "acc = orc_bf16_to_f32(orc_f32_to_bf16_rne(acc + p));"),
+    "accumulate_in_bf16": ("float p = wv * xv; /* exact: 4 x 8 significant bits */\n                acc = acc + p;",
+                           "float p = wv * xv;\n                acc = orc_bf16_to_f32(orc_f32_to_bf16_rne(acc + p));"),
+    "mxfp4_accumulate_in_bf16": (
+        "* orc_bf16_to_f32(x[i * ldx + j]);\n                acc = acc + p;",
+        "* orc_bf16_to_f32(x[i * ldx + j]);\n                acc = orc_bf16_to_f32(orc_f32_to_bf16_rne(acc + p));"),
     # SiLU-and-multiply and its one-step fp64 -> bf16 rounding
     "silu_exponent_sign": ("double s = g[i] / (1.0 + exp(-g[i]));",
                            "double s = g[i] / (1.0 + exp(g[i]));"),
@@ -57,6 +61,14 @@ MUTATIONS = {
                                   "(float)a));"),
     "f64_rounding_ties_away": ("nearbyint(a / q)", "round(a / q)"),
     "f64_subnormal_spacing": ("if (e < -125)\n        e = -125;", "if (e < -126)\n        e = -126;"),
+    # MXFP4 (w4a16)
+    "e2m1_exponent_bias": ("ldexpf(1.0f + 0.5f * (float)m, e - 1)", "ldexpf(1.0f + 0.5f * (float)m, e - 2)"),
+    "e2m1_mantissa_weight": ("ldexpf(1.0f + 0.5f * (float)m, e - 1)", "ldexpf(1.0f + 0.25f * (float)m, e - 1)"),
+    "e2m1_subnormal_dropped": ("float v = (e == 0) ? 0.5f * (float)m :", "float v = (e == 0) ? 0.0f :"),
+    "e8m0_bias": ("return ldexpf(1.0f, (int)e - 127);", "return ldexpf(1.0f, (int)e - 128);"),
+    "nibble_order_swapped": ("uint8_t code = (j & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);",
+                             "uint8_t code = (j & 1) ? (uint8_t)(byte & 15) : (uint8_t)(byte >> 4);"),
+    "mxfp4_block_of_16": ("orc_e8m0_to_f32(bs[r * ldb + j / 32])", "orc_e8m0_to_f32(bs[r * ldb + j / 16])"),
 }
 
 # pins rerun against each mutated copy (test functions that take the oracle)
@@ -77,6 +89,11 @@ PINS = [
     lambda o: silu_pins.test_silu_closed_forms_and_limits(o),
     lambda o: silu_pins.test_silu_odd_part_identity(o),
     lambda o: silu_pins.test_gate_up_silu_mul_is_nearest_bf16_of_exact_result(o),
+    lambda o: mxfp4_pins.test_e2m1_codes_closed_form(o),
+    lambda o: mxfp4_pins.test_e8m0_scales_closed_form_and_torch(o),
+    lambda o: mxfp4_pins.test_mxfp4_gemv_against_fp64_brute_force(o, 3, 40, 100, 3),
+    lambda o: mxfp4_pins.test_mxfp4_one_hot_codes_scales_and_packing(o),
+    lambda o: mxfp4_pins.test_mxfp4_exact_sum_inputs_match_rational_result(o),
 ]
 
 
