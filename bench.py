@@ -181,8 +181,12 @@ class GemvBench:
         s_d = torch.from_numpy(plane.scale).to(device) if plane.scale is not None else None
         dt = w8.DT_E4M3FN if self.fp8 else w8.DT_BF16
         silu = proj.act == "silu_mul"
-        src = w8.Plane.from_tensor(w_d, s_d, k=proj.k, dtype=dt,
-                                   layout=w8.SRC_GATE_UP if silu else w8.SRC_ROW_MAJOR)
+        mx = proj.dtype == "mxfp4"
+        if mx:
+            src = w8.Plane.mxfp4(w_d, s_d, k=proj.k)
+        else:
+            src = w8.Plane.from_tensor(w_d, s_d, k=proj.k, dtype=dt,
+                                       layout=w8.SRC_GATE_UP if silu else w8.SRC_ROW_MAJOR)
         self.build = w8.bind([src] * copies)
         torch.cuda.synchronize()
         del w_d, s_d, src
@@ -193,7 +197,8 @@ class GemvBench:
         self.y = {m: torch.zeros((m, proj.out_n), dtype=torch.int16, device=device)
                   for m in self.ms}
         self.ws = self.build.new_workspace()
-        self.fn = (w8.w8_gemv_silu_mul if silu else w8.w8_gemv if self.fp8 else w8.bf16_gemv)
+        self.fn = (w8.w8_gemv_silu_mul if silu else w8.mxfp4_gemv if mx
+                   else w8.w8_gemv if self.fp8 else w8.bf16_gemv)
 
     def step_bytes(self):
         return sum(self.proj.algorithmic_bytes(m) for m in self.ms)

@@ -26,11 +26,31 @@ constexpr int64_t kMaxDim = int64_t(1) << 30;
 
 int elem_bytes(int32_t dtype) { return dtype == W8_DT_BF16 ? 2 : 1; }
 
+// Bytes of a row of ldw elements (MXFP4: two elements a byte).
+int64_t row_bytes(int32_t dtype, int64_t ldw)
+{
+    return dtype == W8_DT_MXFP4 ? ldw / 2 : ldw * elem_bytes(dtype);
+}
+
+// The kernels' dtype of a plane dtype.
+int kernel_dt(int32_t dtype)
+{
+    return dtype == W8_DT_E4M3FN ? w8::kDtFp8 : dtype == W8_DT_MXFP4 ? w8::kDtFp4 : w8::kDtBf16;
+}
+
+// The launch plan of a plane's dtype: MXFP4 planes run the register ring only.
+w8::Plan plan_for(int32_t dtype, int64_t n, int64_t k, int m, int sms)
+{
+    return dtype == W8_DT_MXFP4 ? w8::make_ring_plan(n, k, m, sms) : w8::make_plan(n, k, m, sms);
+}
+
+int max_m(int32_t dtype) { return dtype == W8_DT_MXFP4 ? w8::kMaxRingM : w8::kMaxM; }
+
 w8_status check_plane(const w8_plane_desc &d)
 {
     if (!d.w)
         return W8_ERR_NULL;
-    if (d.dtype != W8_DT_E4M3FN && d.dtype != W8_DT_BF16)
+    if (d.dtype != W8_DT_E4M3FN && d.dtype != W8_DT_BF16 && d.dtype != W8_DT_MXFP4)
         return W8_ERR_DTYPE;
     if (d.layout != W8_SRC_ROW_MAJOR && d.layout != W8_SRC_GATE_UP)
         return W8_ERR_LAYOUT;
@@ -43,9 +63,14 @@ w8_status check_plane(const w8_plane_desc &d)
         return W8_ERR_SHAPE; // I = n / 2 gate rows, a multiple of 8
     if (d.dtype == W8_DT_E4M3FN && !d.scale)
         return W8_ERR_SCALE;
-    if (d.dtype == W8_DT_BF16 && d.scale)
+    if (d.dtype != W8_DT_E4M3FN && d.scale)
         return W8_ERR_SCALE;
-    if ((reinterpret_cast<uintptr_t>(d.w) & 15u) != 0 || ((d.ldw * elem_bytes(d.dtype)) & 15) != 0)
+    if (d.dtype == W8_DT_MXFP4 && (!d.block_scale || d.ldb < w8::ceil_div(d.k, 32)))
+        return W8_ERR_SCALE;
+    if (d.dtype != W8_DT_MXFP4 && d.block_scale)
+        return W8_ERR_SCALE;
+    if ((reinterpret_cast<uintptr_t>(d.w) & 15u) != 0 || (d.dtype == W8_DT_MXFP4 && (d.ldw & 1)) ||
+        (row_bytes(d.dtype, d.ldw) & 15) != 0)
         return W8_ERR_UNPADDED;
     return W8_OK;
 }
@@ -53,7 +78,8 @@ w8_status check_plane(const w8_plane_desc &d)
 size_t plane_packed_bytes(int32_t dtype, int64_t n, int64_t k)
 {
     const int64_t rt = w8::ceil_div(n, w8::kTileN), kb = w8::ceil_div(k, w8::kTileK);
-    return size_t(rt) * size_t(kb) * size_t(dtype == W8_DT_BF16 ? w8::kRunBf16 : w8::kRunFp8);
+    return size_t(rt) * size_t(kb) *
+           size_t(dtype == W8_DT_BF16 ? w8::kRunBf16 : dtype == W8_DT_MXFP4 ? w8::kRunFp4 : w8::kRunFp8);
 }
 
 size_t plane_scale_bytes(int32_t dtype, int64_t n)
@@ -77,7 +103,7 @@ w8_status gemv_common(const w8_build *b, int plane, int32_t want_dtype, bool sil
         return W8_ERR_DTYPE;
     if (silu && p.layout != W8_LAYOUT_MMA_16x32_GATE_UP)
         return W8_ERR_LAYOUT;
-    if (m < 0 || m > w8::kMaxM)
+    if (m < 0 || m > max_m(p.dtype))
         return W8_ERR_SHAPE;
     if (m == 0)
         return W8_OK;
@@ -93,7 +119,7 @@ w8_status gemv_common(const w8_build *b, int plane, int32_t want_dtype, bool sil
     if (dev != b->device)
         return W8_ERR_DEVICE;
 
-    const w8::Plan plan = w8::make_plan(p.n, p.k, m, b->sm_count);
+    const w8::Plan plan = plan_for(p.dtype, p.n, p.k, m, b->sm_count);
     w8::GemvArgs a{};
     a.wp = static_cast<const uint8_t *>(p.packed);
     a.scale = p.scale;
@@ -119,7 +145,7 @@ w8_status gemv_common(const w8_build *b, int plane, int32_t want_dtype, bool sil
         a.counters = static_cast<int *>(ws);
         a.partial = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + plan.ws_counters);
     }
-    if (w8::launch_gemv(p.dtype == W8_DT_E4M3FN, plan, a, reinterpret_cast<cudaStream_t>(s)) !=
+    if (w8::launch_gemv(kernel_dt(p.dtype), plan, a, reinterpret_cast<cudaStream_t>(s)) !=
         cudaSuccess)
         return W8_ERR_CUDA;
     return W8_OK;
@@ -134,15 +160,16 @@ const char *w8_status_str(w8_status s)
     switch (s) {
     case W8_OK: return "ok";
     case W8_ERR_NULL: return "a required pointer is NULL";
-    case W8_ERR_DTYPE: return "weight dtype the kernels cannot read (only E4M3FN and BF16), "
-                              "or a gemv call of the other dtype";
+    case W8_ERR_DTYPE: return "weight dtype the kernels cannot read (only E4M3FN, BF16 and "
+                              "MXFP4), or a gemv call of another dtype";
     case W8_ERR_UNPADDED: return "unpadded plane: base not 16-byte aligned or row stride not a "
                                  "multiple of 16 bytes";
     case W8_ERR_BIAS: return "a bias was given; the GEMV has none";
     case W8_ERR_MIXED: return "bf16 and FP8 planes mixed in one build";
     case W8_ERR_SHAPE: return "bad shape: N, K >= 1, ldw >= K, 0 <= m <= 256, ldx >= K, ldy >= N "
                               "(N/2 for SiLU-and-multiply); a gate_up plane needs N % 16 == 0";
-    case W8_ERR_SCALE: return "FP8 planes need fp32 row scales; bf16 planes take none";
+    case W8_ERR_SCALE: return "FP8 planes need fp32 row scales, MXFP4 planes E8M0 block scales "
+                              "(ldb >= ceil(K/32)); no other plane takes either";
     case W8_ERR_LAYOUT: return "unknown source layout (row-major or gate_up), or SiLU-and-multiply "
                                "on a plane not bound as gate_up";
     case W8_ERR_CAPACITY: return "packed buffer or workspace too small";
@@ -252,7 +279,9 @@ w8_status w8_bind(const w8_plane_desc *d, int n_planes, void *dst, size_t dst_by
 
         w8::RepackArgs ra{};
         ra.src = static_cast<const uint8_t *>(pd.w);
-        ra.ld_bytes = pd.ldw * elem_bytes(pd.dtype);
+        ra.ld_bytes = row_bytes(pd.dtype, pd.ldw);
+        ra.bscale_src = pd.block_scale;
+        ra.ldb = pd.ldb;
         ra.n = pd.n;
         ra.k = pd.k;
         ra.kb = info.k_blocks;
@@ -261,7 +290,7 @@ w8_status w8_bind(const w8_plane_desc *d, int n_planes, void *dst, size_t dst_by
         ra.scale_src = pd.scale;
         ra.scale_dst = scale_copy;
         ra.half = gated ? pd.n / 2 : 0;
-        if (w8::launch_repack(pd.dtype == W8_DT_E4M3FN, ra, reinterpret_cast<cudaStream_t>(s)) !=
+        if (w8::launch_repack(kernel_dt(pd.dtype), ra, reinterpret_cast<cudaStream_t>(s)) !=
             cudaSuccess) {
             delete b;
             return W8_ERR_CUDA;
@@ -293,13 +322,8 @@ w8_status w8_build_info(const w8_build *b, int plane, w8_plane_info *info)
     return W8_OK;
 }
 
-w8_status w8_plan_shape(int64_t n, int64_t k, int m, int sm_count, w8_plan *out)
+static void fill_plan(const w8::Plan &pl, w8_plan *out)
 {
-    if (!out)
-        return W8_ERR_NULL;
-    if (n < 1 || k < 1 || n > kMaxDim || k > kMaxDim || m < 1 || m > w8::kMaxM || sm_count < 1)
-        return W8_ERR_SHAPE;
-    const w8::Plan pl = w8::make_plan(n, k, m, sm_count);
     out->kernel = pl.tc ? 1 : 0;
     out->grid = pl.grid;
     out->block = pl.tc ? w8::kTcThreadsPerCta : w8::kThreads;
@@ -312,6 +336,15 @@ w8_status w8_plan_shape(int64_t n, int64_t k, int m, int sm_count, w8_plan *out)
     out->splits = pl.splits;
     out->k_blocks_per_warp_max = pl.kbs_max;
     out->workspace_bytes = pl.ws_bytes;
+}
+
+w8_status w8_plan_shape(int64_t n, int64_t k, int m, int sm_count, w8_plan *out)
+{
+    if (!out)
+        return W8_ERR_NULL;
+    if (n < 1 || k < 1 || n > kMaxDim || k > kMaxDim || m < 1 || m > w8::kMaxM || sm_count < 1)
+        return W8_ERR_SHAPE;
+    fill_plan(w8::make_plan(n, k, m, sm_count), out);
     return W8_OK;
 }
 
@@ -322,14 +355,16 @@ w8_status w8_plan_info(const w8_build *b, int plane, int m, w8_plan *out)
     if (plane < 0 || plane >= int(b->planes.size()))
         return W8_ERR_PLANE;
     const w8_plane_info &p = b->planes[size_t(plane)];
-    const w8_status st = w8_plan_shape(p.n, p.k, m, b->sm_count, out);
-    if (st == W8_OK && p.dtype == W8_DT_BF16)
-    {
-        const w8::Plan pl = w8::make_plan(p.n, p.k, m, b->sm_count);
+    if (m < 1 || m > max_m(p.dtype))
+        return W8_ERR_SHAPE;
+    const w8::Plan pl = plan_for(p.dtype, p.n, p.k, m, b->sm_count);
+    fill_plan(pl, out);
+    if (p.dtype == W8_DT_BF16)
         out->depth = pl.tc ? w8::tc_stages(false, pl.npad).nw * w8::kTcStageBlocks
                            : w8::depth_w(pl.nt, pl.r, false, pl.occ);
-    }
-    return st;
+    if (p.dtype == W8_DT_MXFP4)
+        out->depth = w8::depth_w_dt(pl.nt, pl.r, w8::kDtFp4, pl.occ);
+    return W8_OK;
 }
 
 w8_status w8_workspace_bytes(const w8_build *b, int plane, int m, size_t *bytes)
@@ -345,9 +380,9 @@ w8_status w8_workspace_bytes(const w8_build *b, int plane, int m, size_t *bytes)
     const int p1 = plane < 0 ? int(b->planes.size()) : plane + 1;
     for (int pi = p0; pi < p1; ++pi) {
         const w8_plane_info &p = b->planes[size_t(pi)];
-        const int m0 = m == 0 ? 1 : m, m1 = m == 0 ? w8::kMaxM : m;
-        for (int mm = m0; mm <= m1; ++mm) {
-            const size_t ws = w8::make_plan(p.n, p.k, mm, b->sm_count).ws_bytes;
+        const int m0 = m == 0 ? 1 : m, m1 = m == 0 ? max_m(p.dtype) : m;
+        for (int mm = m0; mm <= m1 && mm <= max_m(p.dtype); ++mm) {
+            const size_t ws = plan_for(p.dtype, p.n, p.k, mm, b->sm_count).ws_bytes;
             if (ws > best)
                 best = ws;
         }
@@ -370,6 +405,13 @@ w8_status bf16_gemv(const w8_build *b, int plane, const uint16_t *x, int64_t ldx
                        workspace_bytes, s);
 }
 
+w8_status mxfp4_gemv(const w8_build *b, int plane, const uint16_t *x, int64_t ldx, int m,
+                     uint16_t *y, int64_t ldy, void *workspace, size_t workspace_bytes, w8_stream s)
+{
+    return gemv_common(b, plane, W8_DT_MXFP4, false, x, ldx, m, y, ldy, workspace,
+                       workspace_bytes, s);
+}
+
 w8_status w8_gemv_silu_mul(const w8_build *b, int plane, const uint16_t *x, int64_t ldx, int m,
                            uint16_t *y, int64_t ldy, void *workspace, size_t workspace_bytes,
                            w8_stream s)
@@ -385,6 +427,8 @@ int64_t w8_packed_offset(int dtype, int64_t k_blocks, int64_t row, int64_t col)
         return w8::packed_offset_fp8(k_blocks, row, col);
     if (dtype == W8_DT_BF16)
         return w8::packed_offset_bf16(k_blocks, row, col);
+    if (dtype == W8_DT_MXFP4)
+        return w8::packed_nibble_fp4(k_blocks, row, col);
     return -1;
 }
 

@@ -122,23 +122,16 @@ __device__ __forceinline__ float ld_cg_f32(const float *p)
     return v;
 }
 
-// Weight operand of one (row tile, K block) for one lane.
-template <bool kFp8> struct WFrag;
-template <> struct WFrag<true> { uint4 v; };
-template <> struct WFrag<false> { uint4 v[2]; };
+// Weight operand of one (row tile, K block) for one lane: 16 bytes of E4M3
+// codes, 32 bytes of bf16, or 8 bytes of MXFP4 codes plus the word of its
+// rows' block scales (bf16 of row g, bf16 of row g+8).
+template <int kDt> struct WFrag;
+template <> struct WFrag<kDtFp8> { uint4 v; };
+template <> struct WFrag<kDtBf16> { uint4 v[2]; };
+template <> struct WFrag<kDtFp4> { uint2 v; uint32_t s; };
 
-template <bool kFp8>
-__device__ __forceinline__ void load_w(WFrag<kFp8> &f, const uint8_t *p)
-{
-    if constexpr (kFp8) {
-        f.v = ld_stream(p);
-    } else {
-        f.v[0] = ld_stream(p);
-        f.v[1] = ld_stream(p + 512);
-    }
-}
-
-// Predicated weight load: fills f only when ok (f keeps its value otherwise).
+// Predicated streaming loads: fill the destination only when ok (it keeps
+// its value otherwise).
 __device__ __forceinline__ void ld_stream_pred(uint4 &v, const uint8_t *p, uint32_t ok)
 {
     asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %5, 0;\n\t"
@@ -146,33 +139,77 @@ __device__ __forceinline__ void ld_stream_pred(uint4 &v, const uint8_t *p, uint3
                  : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
                  : "l"(p), "r"(ok));
 }
-
-template <bool kFp8>
-__device__ __forceinline__ void load_w_pred(WFrag<kFp8> &f, const uint8_t *p, uint32_t ok)
+__device__ __forceinline__ void ld_stream8_pred(uint2 &v, const uint8_t *p, uint32_t ok)
 {
-    if constexpr (kFp8) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %3, 0;\n\t"
+                 "@q ld.global.nc.L1::no_allocate.L2::256B.v2.u32 {%0,%1}, [%2];\n\t}"
+                 : "+r"(v.x), "+r"(v.y)
+                 : "l"(p), "r"(ok));
+}
+__device__ __forceinline__ void ld_stream4_pred(uint32_t &v, const uint8_t *p, uint32_t ok)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t"
+                 "@q ld.global.nc.L1::no_allocate.L2::256B.u32 %0, [%1];\n\t}"
+                 : "+r"(v)
+                 : "l"(p), "r"(ok));
+}
+
+// Load the lane's fragment of the run at p (p already includes the lane's
+// offset into the run; soff is the offset from p to the lane's scale word,
+// MXFP4 only), predicated on ok.
+template <int kDt>
+__device__ __forceinline__ void load_w_pred(WFrag<kDt> &f, const uint8_t *p, int soff, uint32_t ok)
+{
+    if constexpr (kDt == kDtFp8) {
         ld_stream_pred(f.v, p, ok);
-    } else {
+    } else if constexpr (kDt == kDtBf16) {
         ld_stream_pred(f.v[0], p, ok);
         ld_stream_pred(f.v[1], p + 512, ok);
+    } else {
+        ld_stream8_pred(f.v, p, ok);
+        ld_stream4_pred(f.s, p + soff, ok);
     }
 }
-
-template <bool kFp8>
-__device__ __forceinline__ void zero_w(WFrag<kFp8> &f)
+template <int kDt>
+__device__ __forceinline__ void load_w(WFrag<kDt> &f, const uint8_t *p, int soff)
 {
-    if constexpr (kFp8) {
+    load_w_pred<kDt>(f, p, soff, 1u);
+}
+
+template <int kDt>
+__device__ __forceinline__ void zero_w(WFrag<kDt> &f)
+{
+    if constexpr (kDt == kDtFp8) {
         f.v = make_uint4(0, 0, 0, 0);
-    } else {
+    } else if constexpr (kDt == kDtBf16) {
         f.v[0] = make_uint4(0, 0, 0, 0);
         f.v[1] = make_uint4(0, 0, 0, 0);
+    } else {
+        f.v = make_uint2(0, 0);
+        f.s = 0;
     }
 }
 
-template <bool kFp8>
-__device__ __forceinline__ void a_operands(uint32_t (&a)[8], const WFrag<kFp8> &f)
+// Two E2M1 codes (nibbles 0 and 4 of x) -> the bf16x2 bit patterns of their
+// values times 2^-126, exactly: the sign goes to bit 15, the two exponent bits
+// and the mantissa bit to bits 8..6, so a normal code e >= 1 reads as
+// (1 + m/2) 2^(e - 127) and a subnormal one (e = 0) as m/2 2^-126.
+__device__ __forceinline__ uint32_t e2m1x2_bits(uint32_t x)
 {
-    if constexpr (kFp8) {
+    return ((x & 0x00070007u) << 6) | ((x & 0x00080008u) << 12);
+}
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// The eight A registers of one lane for one block (two m16n8k16 steps).
+template <int kDt>
+__device__ __forceinline__ void a_operands(uint32_t (&a)[8], const WFrag<kDt> &f)
+{
+    if constexpr (kDt == kDtFp8) {
         a[0] = widen_e4m3x2<kSelRowG>(f.v.x);
         a[1] = widen_e4m3x2<kSelRowG8>(f.v.x);
         a[2] = widen_e4m3x2<kSelRowG>(f.v.y);
@@ -181,9 +218,25 @@ __device__ __forceinline__ void a_operands(uint32_t (&a)[8], const WFrag<kFp8> &
         a[5] = widen_e4m3x2<kSelRowG8>(f.v.z);
         a[6] = widen_e4m3x2<kSelRowG>(f.v.w);
         a[7] = widen_e4m3x2<kSelRowG8>(f.v.w);
-    } else {
+    } else if constexpr (kDt == kDtBf16) {
         a[0] = f.v[0].x; a[1] = f.v[0].y; a[2] = f.v[0].z; a[3] = f.v[0].w;
         a[4] = f.v[1].x; a[5] = f.v[1].y; a[6] = f.v[1].z; a[7] = f.v[1].w;
+    } else {
+        // E2M1 x 2^-126 (exact) x 2^126 (exact) x the block scale 2^(e-127)
+        // (exact: the value keeps 2 significant bits within bf16's range; a
+        // NaN scale gives NaN, a product past bf16's range gives inf)
+        uint32_t sg, sg8;
+        asm("prmt.b32 %0, %1, 0, 0x1010;" : "=r"(sg) : "r"(f.s));  // (row g, row g)
+        asm("prmt.b32 %0, %1, 0, 0x3232;" : "=r"(sg8) : "r"(f.s)); // (row g+8, row g+8)
+        constexpr uint32_t k2p126 = 0x7E807E80u;                  // 2^126, 2^126
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const uint32_t w = q ? f.v.y : f.v.x;
+            a[4 * q + 0] = mul_bf16x2(mul_bf16x2(e2m1x2_bits(w), k2p126), sg);
+            a[4 * q + 1] = mul_bf16x2(mul_bf16x2(e2m1x2_bits(w >> 4), k2p126), sg8);
+            a[4 * q + 2] = mul_bf16x2(mul_bf16x2(e2m1x2_bits(w >> 8), k2p126), sg);
+            a[4 * q + 3] = mul_bf16x2(mul_bf16x2(e2m1x2_bits(w >> 12), k2p126), sg8);
+        }
     }
 }
 

@@ -75,14 +75,14 @@ __device__ __forceinline__ uint4 load_x_tail(const uint16_t *p, bool ok, int64_t
 
 // One K block: widen the R weight fragments and run the two tensor-core steps
 // of every (row tile, 8 tokens) into its accumulator.
-template <bool kFp8, int NT, int R>
-__device__ __forceinline__ void block_step(float (&acc)[R][NT][4], const WFrag<kFp8> (&w)[R],
+template <int kDt, int NT, int R>
+__device__ __forceinline__ void block_step(float (&acc)[R][NT][4], const WFrag<kDt> (&w)[R],
                                            const uint4 (&x)[NT])
 {
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         uint32_t aop[8];
-        a_operands<kFp8>(aop, w[r]);
+        a_operands<kDt>(aop, w[r]);
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
             mma_bf16(acc[r][j], aop[0], aop[1], aop[2], aop[3], x[j].x, x[j].y);
@@ -94,12 +94,14 @@ __device__ __forceinline__ void block_step(float (&acc)[R][NT][4], const WFrag<k
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <bool kFp8, int NT, int R, int DW, int DX, int kMinBlocks>
+template <int kDt, int NT, int R, int DW, int DX, int kMinBlocks>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvArgs a)
 {
     static_assert(DW % DX == 0, "the activation ring depth divides the weight ring depth");
     extern __shared__ __align__(16) float red[]; // [warp][R][NT][4][32]
-    constexpr int kRun = kFp8 ? kRunFp8 : kRunBf16;
+    constexpr bool kFp8 = kDt == kDtFp8; // row scales in the epilogue
+    constexpr int kRun = kDt == kDtFp8 ? kRunFp8 : kDt == kDtFp4 ? kRunFp4 : kRunBf16;
+    constexpr int kLaneBytes = kDt == kDtFp4 ? 8 : 16; // a lane's part of a run (bf16: twice)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -126,13 +128,15 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
     nmain = nmain < 0 ? 0 : (nmain > nkb ? nkb : nmain);
     const bool has_tail = nkb > nmain;
 
-    const uint8_t *wptr[R]; // this lane's 16 bytes of the warp's first run of each tile
+    const uint8_t *wptr[R]; // this lane's part of the warp's first run of each tile
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const int tile = rg * (wt * R) + r * wt + tg;
         const int64_t t64 = tile < a.rt ? tile : 0; // idle slots re-read tile 0
-        wptr[r] = a.wp + (t64 * a.kb + kb0) * kRun + lane * 16;
+        wptr[r] = a.wp + (t64 * a.kb + kb0) * kRun + lane * kLaneBytes;
     }
+    // MXFP4: from the lane's codes to its rows' scale word (g) after the codes
+    const int soff = kDt == kDtFp4 ? kRunFp4Codes - kLaneBytes * lane + 4 * g : 0;
     const uint16_t *xptr[NT];
     uint32_t tok_ok[NT];
 #pragma unroll
@@ -145,12 +149,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
     // Weights first: the packed plane is written only by w8_bind, which
     // finishes before any GEMV can be launched, so these loads may overlap the
     // tail of the previous kernel on the stream.  The ring holds blocks
-    // [0, DW); for FP8 planes, blocks up to kPf go to L2 now, and every ring
-    // group sends the kPf-distant group after it (bulk prefetches: no
-    // registers, no waits).  bf16 planes skip it: twice the bytes ahead
-    // crowded L2 on the largest planes (lm_head, o_proj bf16) and cost time.
-    // Lane 0 issues them, so its wptr is the start of the warp's runs.
-    constexpr int kPf = kFp8 ? (DW > 16 ? DW : 16) : DW;
+    // [0, DW); for FP8 and MXFP4 planes, blocks up to kPf go to L2 now, and
+    // every ring group sends the kPf-distant group after it (bulk
+    // prefetches: no registers, no waits).  bf16 planes skip it: twice the
+    // bytes ahead crowded L2 on the largest planes (lm_head, o_proj bf16) and
+    // cost time.  Lane 0 issues them, so its wptr is the start of the warp's
+    // runs.
+    constexpr int kPf = kDt != kDtBf16 ? (DW > 16 ? DW : 16) : DW;
     if (kPf > DW && lane == 0 && nmain > DW) {
         const int hi = nmain < kPf ? nmain : kPf;
         if (hi > DW)
@@ -158,15 +163,15 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
             for (int r = 0; r < R; ++r)
                 prefetch_l2(wptr[r] + DW * kRun, uint32_t(hi - DW) * kRun);
     }
-    WFrag<kFp8> wring[DW][R];
+    WFrag<kDt> wring[DW][R];
     uint4 xring[DX][NT];
 #pragma unroll
     for (int i = 0; i < DW; ++i)
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            zero_w<kFp8>(wring[i][r]);
+            zero_w<kDt>(wring[i][r]);
             if (i < nmain)
-                load_w<kFp8>(wring[i][r], wptr[r] + i * kRun);
+                load_w<kDt>(wring[i][r], wptr[r] + i * kRun, soff);
         }
     // the CTA's row scales (bind-time data too) into shared memory
     __shared__ float s_scale[kWarps * 2 * kTileN];
@@ -211,11 +216,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
         }
 #pragma unroll
         for (int i = 0; i < DW; ++i) {
-            block_step<kFp8, NT, R>(acc, wring[i], xring[i % DX]);
+            block_step<kDt, NT, R>(acc, wring[i], xring[i % DX]);
             const uint32_t more_w = (b + DW + i) < nmain;
 #pragma unroll
             for (int r = 0; r < R; ++r)
-                load_w_pred<kFp8>(wring[i][r], wptr[r] + (b + DW + i) * kRun, more_w);
+                load_w_pred<kDt>(wring[i][r], wptr[r] + (b + DW + i) * kRun, soff, more_w);
             const uint32_t more_x = (b + DX + i) < nmain;
 #pragma unroll
             for (int j = 0; j < NT; ++j)
@@ -227,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
 #pragma unroll
     for (int i = 0; i < DW - 1; ++i) {
         if (b + i < nmain) {
-            block_step<kFp8, NT, R>(acc, wring[i], xring[i % DX]);
+            block_step<kDt, NT, R>(acc, wring[i], xring[i % DX]);
             const uint32_t more_x = (b + DX + i) < nmain;
 #pragma unroll
             for (int j = 0; j < NT; ++j)
@@ -238,16 +243,16 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
     if (has_tail) {
         // the partial last block: zero activations past K (its weights past K
         // are zero-filled by the repack)
-        WFrag<kFp8> tw[R];
+        WFrag<kDt> tw[R];
         uint4 tx[NT];
 #pragma unroll
         for (int r = 0; r < R; ++r)
-            load_w<kFp8>(tw[r], wptr[r] + nmain * kRun);
+            load_w<kDt>(tw[r], wptr[r] + nmain * kRun, soff);
         const int64_t col = int64_t(kb0 + nmain) * kTileK + 8 * t;
 #pragma unroll
         for (int j = 0; j < NT; ++j)
             tx[j] = load_x_tail(xptr[j] + nmain * kTileK, tok_ok[j] != 0, col, a.k);
-        block_step<kFp8, NT, R>(acc, tw, tx);
+        block_step<kDt, NT, R>(acc, tw, tx);
     }
 
     // ---- K parts meet in shared memory ---------------------------------------
@@ -362,34 +367,41 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
 // instance table: one kernel per (dtype, NT, R, occupancy) with the depths of
 // w8_layout.h
 // ---------------------------------------------------------------------------
-template <bool kFp8, int NT, int R, int OCC>
+template <int kDt, int NT, int R, int OCC>
 void *inst()
 {
-    return reinterpret_cast<void *>(&gemv_kernel<kFp8, NT, R, depth_w(NT, R, kFp8, OCC),
-                                                 depth_x(NT, R, kFp8, OCC), OCC>);
+    return reinterpret_cast<void *>(&gemv_kernel<kDt, NT, R, depth_w_dt(NT, R, kDt, OCC),
+                                                 depth_x_dt(NT, R, kDt, OCC), OCC>);
 }
 
-template <bool kFp8, int I>
+template <int kDt, int I>
 void *inst_at()
 {
-    return inst<kFp8, kInst[I].nt, kInst[I].r, kInst[I].occ>();
+    return inst<kDt, kInst[I].nt, kInst[I].r, kInst[I].occ>();
 }
 
-template <bool kFp8, int... Is>
+template <int kDt, int... Is>
 void *pick_from(int idx, std::integer_sequence<int, Is...>)
 {
     void *fn = nullptr;
-    ((fn = (idx == Is ? inst_at<kFp8, Is>() : fn)), ...);
+    ((fn = (idx == Is ? inst_at<kDt, Is>() : fn)), ...);
     return fn;
 }
 
-template <bool kFp8>
+template <int kDt>
 void *pick(int nt, int r, int occ)
 {
     const int idx = inst_index(nt, r, occ);
     if (idx < 0)
         return nullptr;
-    return pick_from<kFp8>(idx, std::make_integer_sequence<int, kNumInst>{});
+    return pick_from<kDt>(idx, std::make_integer_sequence<int, kNumInst>{});
+}
+
+void *pick_dt(int dt, int nt, int r, int occ)
+{
+    return dt == kDtFp8 ? pick<kDtFp8>(nt, r, occ)
+           : dt == kDtFp4 ? pick<kDtFp4>(nt, r, occ)
+                          : pick<kDtBf16>(nt, r, occ);
 }
 
 } // namespace
@@ -398,9 +410,8 @@ cudaError_t prepare_gemv_kernels()
 {
     // the K-part reduction buffer: 8 warps x R x NT x 128 floats, at most 64 KB
     for (int i = 0; i < kNumInst; ++i) {
-        for (int f = 0; f < 2; ++f) {
-            void *fn = f ? pick<true>(kInst[i].nt, kInst[i].r, kInst[i].occ)
-                         : pick<false>(kInst[i].nt, kInst[i].r, kInst[i].occ);
+        for (int dt : {kDtBf16, kDtFp8, kDtFp4}) {
+            void *fn = pick_dt(dt, kInst[i].nt, kInst[i].r, kInst[i].occ);
             cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  64 * 1024);
             if (e != cudaSuccess)
@@ -410,11 +421,11 @@ cudaError_t prepare_gemv_kernels()
     return prepare_tc_kernels();
 }
 
-cudaError_t launch_gemv(bool fp8, const Plan &plan, const GemvArgs &a, cudaStream_t s)
+cudaError_t launch_gemv(int dt, const Plan &plan, const GemvArgs &a, cudaStream_t s)
 {
     if (plan.tc)
-        return launch_tc(fp8, plan, a, s);
-    void *fn = fp8 ? pick<true>(plan.nt, plan.r, plan.occ) : pick<false>(plan.nt, plan.r, plan.occ);
+        return dt == kDtFp4 ? cudaErrorInvalidValue : launch_tc(dt == kDtFp8, plan, a, s);
+    void *fn = pick_dt(dt, plan.nt, plan.r, plan.occ);
     if (!fn)
         return cudaErrorInvalidValue;
     void *args[] = {const_cast<GemvArgs *>(&a)};

@@ -56,8 +56,10 @@ inline void set_output_map(GemvArgs &a, const w8_plane_info &p, bool silu)
     a.half = gated ? int(p.n / 2) : 0;
 }
 
-// One launch of the GEMV kernel chosen by the plan (FP8 or bf16 weights).
-cudaError_t launch_gemv(bool fp8, const Plan &plan, const GemvArgs &a, cudaStream_t s);
+// One launch of the GEMV kernel chosen by the plan; dt is the weight dtype
+// (kDtBf16, kDtFp8 or kDtFp4 of w8_device.cuh; MXFP4 plans are register-ring
+// plans).
+cudaError_t launch_gemv(int dt, const Plan &plan, const GemvArgs &a, cudaStream_t s);
 
 // Raise the dynamic shared-memory limit of every GEMV kernel instance on the
 // current device (called once per device before the first launch).
@@ -80,8 +82,11 @@ struct RepackArgs {
     int64_t half;           // 0, or I for a gate_up plane (n = 2I, I % 8 == 0):
                             // packed row 16t+i reads source row 8t+i (i < 8)
                             // or I + 8t + i - 8 (i >= 8)
+    const uint8_t *bscale_src; // MXFP4: caller's E8M0 block scales [n][ldb] (device)
+    int64_t ldb;
 };
 
-cudaError_t launch_repack(bool fp8, const RepackArgs &a, cudaStream_t s);
+// The repack of one plane (dt: kDtBf16, kDtFp8 or kDtFp4).
+cudaError_t launch_repack(int dt, const RepackArgs &a, cudaStream_t s);
 
 } // namespace w8

@@ -41,6 +41,9 @@ constexpr int kRunFp8 = 512;      // bytes of one (tile, block) run, FP8
 constexpr int kRunBf16 = 1024;    // bytes of one (tile, block) run, bf16
 constexpr int kWarps = 8;         // warps per CTA of the GEMV kernel
 constexpr int kThreads = kWarps * 32;
+// Weight dtypes of the kernels (the register ring reads all three; the
+// tensor-memory kernel bf16 and FP8).
+constexpr int kDtBf16 = 0, kDtFp8 = 1, kDtFp4 = 2;
 constexpr int kMaxM = 256;        // tokens per call (decode steps, draft rows, prefill chunks)
 constexpr int kMaxRingM = 64;     // the register-ring kernel's limit (8 token groups of 8)
 
@@ -58,6 +61,27 @@ W8_HD int64_t packed_offset_fp8(int64_t k_blocks, int64_t row, int64_t col)
     const int word = q * 2 + (jj >> 1);
     const int byte = word * 4 + hi + ((jj & 1) << 1);
     return ((rt * k_blocks + kb) * 32 + lane) * 16 + byte;
+}
+
+// MXFP4 (w4a16): a (tile, block) run is 256 bytes of codes -- lane (g, t)
+// holds 8 bytes, one 32-bit word per tensor-core step q, whose nibbles 0/4,
+// 1/5, 2/6 and 3/7 are the (low, high) halves of the A registers (row g,
+// cols 8t+4q, +1), (row g+8, same), (row g, cols 8t+4q+2, +3), (row g+8,
+// same) -- then 8 words of block scales, word g = bf16 scale of row g | bf16
+// scale of row g+8 << 16.
+constexpr int kRunFp4 = 288;
+constexpr int kRunFp4Codes = 256;
+
+// Nibble offset of element (row, col)'s code in an MXFP4 plane's packed runs.
+W8_HD int64_t packed_nibble_fp4(int64_t k_blocks, int64_t row, int64_t col)
+{
+    const int64_t rt = row >> 4, kb = col >> 5;
+    const int r = int(row & 15), c = int(col & 31);
+    const int g = r & 7, hi = r >> 3, t = c >> 3, j = c & 7;
+    const int lane = g * 4 + t;
+    const int q = j >> 2, jj = j & 3;
+    const int p = ((jj & 1) << 2) + ((jj >> 1) << 1) + hi;
+    return ((rt * k_blocks + kb) * kRunFp4 + lane * 8) * 2 + q * 8 + p;
 }
 
 W8_HD int64_t packed_offset_bf16(int64_t k_blocks, int64_t row, int64_t col)
@@ -123,14 +147,16 @@ W8_HD int nt_for_m(int m) { return m <= 8 ? 1 : m <= 16 ? 2 : m <= 32 ? 4 : 8; }
 // (measured: depths 16/8 -> 12/6 took fused_qkv_a_proj from 5.8 to 5.4 us).
 struct Inst {
     int nt, r, occ;
-    int dw_fp8, dx_fp8, dw_bf16, dx_bf16;
+    int dw_fp8, dx_fp8, dw_bf16, dx_bf16, dw_fp4, dx_fp4;
 };
+// (MXFP4 fragments hold 12 bytes a block against FP8's 16 but widen through
+// more temporaries: the FP8 depths, except where they spill.)
 constexpr int kNumInst = 10;
 constexpr Inst kInst[kNumInst] = {
-    {1, 1, 2, 12, 6, 8, 4}, {1, 2, 2, 6, 6, 4, 2}, {1, 1, 3, 6, 6, 4, 2}, {1, 2, 3, 4, 4, 2, 2},
-    {2, 1, 2, 10, 5, 6, 3}, {2, 2, 2, 6, 3, 2, 2},
-    {4, 1, 2, 6, 2, 4, 2},  {4, 2, 1, 8, 4, 4, 2},
-    {8, 1, 1, 6, 2, 4, 2},  {8, 2, 1, 6, 2, 4, 2},
+    {1, 1, 2, 12, 6, 8, 4, 12, 6}, {1, 2, 2, 6, 6, 4, 2, 6, 6}, {1, 1, 3, 6, 6, 4, 2, 6, 6},
+    {1, 2, 3, 4, 4, 2, 2, 4, 4},   {2, 1, 2, 10, 5, 6, 3, 8, 4}, {2, 2, 2, 6, 3, 2, 2, 6, 3},
+    {4, 1, 2, 6, 2, 4, 2, 6, 2},   {4, 2, 1, 8, 4, 4, 2, 8, 4},
+    {8, 1, 1, 6, 2, 4, 2, 6, 2},   {8, 2, 1, 6, 2, 4, 2, 6, 2},
 };
 constexpr int inst_index(int nt, int r, int occ)
 {
@@ -146,6 +172,15 @@ constexpr int depth_w(int nt, int r, bool fp8, int occ)
 constexpr int depth_x(int nt, int r, bool fp8, int occ)
 {
     return fp8 ? kInst[inst_index(nt, r, occ)].dx_fp8 : kInst[inst_index(nt, r, occ)].dx_bf16;
+}
+// The depths of one kernel dtype (kDtBf16, kDtFp8, kDtFp4).
+constexpr int depth_w_dt(int nt, int r, int dt, int occ)
+{
+    return dt == kDtFp4 ? kInst[inst_index(nt, r, occ)].dw_fp4 : depth_w(nt, r, dt == kDtFp8, occ);
+}
+constexpr int depth_x_dt(int nt, int r, int dt, int occ)
+{
+    return dt == kDtFp4 ? kInst[inst_index(nt, r, occ)].dx_fp4 : depth_x(nt, r, dt == kDtFp8, occ);
 }
 
 inline int64_t plan_ctas(int64_t rt, int r, int wk, int splits)
@@ -259,10 +294,10 @@ inline bool use_tc(int64_t n, int m)
     return m > kMaxRingM || (m >= kTcMinM && ceil_div(n, 128) >= kTcMinRowBlocks);
 }
 
-inline Plan make_plan(int64_t n, int64_t k, int m, int sm_count)
+// The register-ring plan (1..64 tokens), for every dtype; MXFP4 planes run
+// only this kernel.
+inline Plan make_ring_plan(int64_t n, int64_t k, int m, int sm_count)
 {
-    if (use_tc(n, m))
-        return make_tc_plan(n, k, m, sm_count);
     Plan p{};
     p.nt = nt_for_m(m);
     p.rt = ceil_div(n, kTileN);
@@ -344,6 +379,11 @@ inline Plan make_plan(int64_t n, int64_t k, int m, int sm_count)
         p.ws_bytes = 0;
     }
     return p;
+}
+
+inline Plan make_plan(int64_t n, int64_t k, int m, int sm_count)
+{
+    return use_tc(n, m) ? make_tc_plan(n, k, m, sm_count) : make_ring_plan(n, k, m, sm_count);
 }
 
 } // namespace w8

@@ -112,7 +112,7 @@ extern "C" w8_status w8_gemv_noalloc(const w8_build *b, int plane, const uint16_
         a.counters = static_cast<int *>(ws);
         a.partial = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + plan.ws_counters);
     }
-    if (w8::launch_gemv(true, plan, a, reinterpret_cast<cudaStream_t>(s)) != cudaSuccess)
+    if (w8::launch_gemv(w8::kDtFp8, plan, a, reinterpret_cast<cudaStream_t>(s)) != cudaSuccess)
         return W8_ERR_CUDA;
     return W8_OK;
 }

@@ -10,6 +10,8 @@
 // A gate_up plane (a merged [2I, K] MLP projection) is read with its gate and
 // up rows interleaved eight at a time, so that a tile's rows g and g+8 are a
 // gate row and its up row.
+// MXFP4 planes pack two codes a byte into 288-byte runs whose last 32 bytes
+// carry the rows' block scales as bf16 pairs.
 // FP8 also writes the build's copy of the row scales; a row that holds a NaN
 // code (0x7F or 0xFF) gets a NaN scale, so its outputs are NaN as the
 // definition gives, while the GEMV's widening stays a fixed exact map.
@@ -148,14 +150,77 @@ __global__ void __launch_bounds__(256) repack_bf16_kernel(const RepackArgs a)
     }
 }
 
+// 8 codes (columns col .. col+7) of one MXFP4 source row as a 32-bit word,
+// nibble j = column col + j (zero past K).  col is a multiple of 8, so the
+// 4 bytes are 4-byte aligned (source rows are 16-byte aligned).
+__device__ __forceinline__ uint32_t load8_fp4(const uint8_t *row, int64_t col, int64_t k)
+{
+    if (col + 8 <= k)
+        return *reinterpret_cast<const uint32_t *>(row + col / 2);
+    uint32_t v = 0;
+    for (int j = 0; j < 8; ++j)
+        if (col + j < k)
+            v |= uint32_t((row[(col + j) / 2] >> (4 * ((col + j) & 1))) & 15u) << (4 * j);
+    return v;
+}
+
+// E8M0 scale -> bf16 bits of 2^(e - 127): the exponent field, except e = 0
+// (2^-127, a bf16 subnormal) and e = 255 (NaN).
+__device__ __forceinline__ uint32_t e8m0_to_bf16(uint32_t e)
+{
+    return e == 0 ? 0x0040u : e == 255 ? 0x7FC0u : (e << 7);
+}
+
+__global__ void __launch_bounds__(256) repack_fp4_kernel(const RepackArgs a)
+{
+    const int64_t rt = blockIdx.x;
+    const int64_t items = a.kb * 32;
+    for (int64_t it = threadIdx.x; it < items; it += blockDim.x) {
+        const int64_t kb = it >> 5;
+        const int lane = int(it & 31);
+        const int g = lane >> 2, t = lane & 3;
+        const int64_t col = kb * kTileK + 8 * t;
+        uint32_t lo = 0, hi = 0, slo = 0, shi = 0;
+        const int64_t n0 = rt * kTileN + g, n1 = n0 + 8;
+        if (n0 < a.n) {
+            lo = load8_fp4(a.src + src_row(a, n0) * a.ld_bytes, col, a.k);
+            slo = e8m0_to_bf16(a.bscale_src[src_row(a, n0) * a.ldb + kb]);
+        }
+        if (n1 < a.n) {
+            hi = load8_fp4(a.src + src_row(a, n1) * a.ld_bytes, col, a.k);
+            shi = e8m0_to_bf16(a.bscale_src[src_row(a, n1) * a.ldb + kb]);
+        }
+        // word q, nibble p: column c = 4q + (p & 4 ? 1 : 0) + (p & 2 ? 2 : 0) of
+        // the lane's 8, from row g (p even) or row g+8 (p odd)
+        uint32_t out[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            uint32_t wv = 0;
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                const int c = 4 * q + ((p >> 2) & 1) + (p & 2);
+                const uint32_t src = (p & 1) ? hi : lo;
+                wv |= ((src >> (4 * c)) & 15u) << (4 * p);
+            }
+            out[q] = wv;
+        }
+        uint8_t *run = a.dst + (rt * a.kb + kb) * kRunFp4;
+        *reinterpret_cast<uint2 *>(run + lane * 8) = make_uint2(out[0], out[1]);
+        if (t == 0)
+            *reinterpret_cast<uint32_t *>(run + kRunFp4Codes + 4 * g) = slo | (shi << 16);
+    }
+}
+
 } // namespace
 
-cudaError_t launch_repack(bool fp8, const RepackArgs &a, cudaStream_t s)
+cudaError_t launch_repack(int dt, const RepackArgs &a, cudaStream_t s)
 {
     if (a.rt <= 0)
         return cudaSuccess;
-    if (fp8)
+    if (dt == kDtFp8)
         repack_fp8_kernel<<<dim3(unsigned(a.rt)), 256, 0, s>>>(a);
+    else if (dt == kDtFp4)
+        repack_fp4_kernel<<<dim3(unsigned(a.rt)), 256, 0, s>>>(a);
     else
         repack_bf16_kernel<<<dim3(unsigned(a.rt)), 256, 0, s>>>(a);
     return cudaGetLastError();

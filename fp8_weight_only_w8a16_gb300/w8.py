@@ -6,7 +6,7 @@ into exceptions.  PyTorch provides device memory and streams only.  There is
 no fallback: if libw8.so is missing, importing this module raises.
 
 Names follow the C ABI: ``validate``, ``packed_bytes``, ``bind`` (w8_bind),
-``w8_gemv``, ``bf16_gemv``, ``w8_gemv_silu_mul``, ``workspace_bytes``,
+``w8_gemv``, ``bf16_gemv``, ``mxfp4_gemv``, ``w8_gemv_silu_mul``, ``workspace_bytes``,
 ``plan_info``, ``packed_offset``, ``gate_up_packed_row``.
 """
 from __future__ import annotations
@@ -21,7 +21,7 @@ from . import build_lib
 
 LIB_PATH = build_lib.LIB
 
-DT_E4M3FN, DT_BF16, DT_E4M3FNUZ, DT_E5M2, DT_FP16 = 1, 2, 3, 4, 5
+DT_E4M3FN, DT_BF16, DT_E4M3FNUZ, DT_E5M2, DT_FP16, DT_MXFP4 = 1, 2, 3, 4, 5, 6
 SRC_ROW_MAJOR, SRC_GATE_UP = 0, 1
 LAYOUT_MMA_16x32, LAYOUT_MMA_16x32_GATE_UP = 1, 2
 MAX_M = 256
@@ -44,7 +44,8 @@ class W8Error(RuntimeError):
 class PlaneDesc(ctypes.Structure):
     _fields_ = [("w", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("layout", ctypes.c_int32),
                 ("n", ctypes.c_int64), ("k", ctypes.c_int64), ("ldw", ctypes.c_int64),
-                ("scale", ctypes.c_void_p), ("bias", ctypes.c_void_p)]
+                ("scale", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+                ("block_scale", ctypes.c_void_p), ("ldb", ctypes.c_int64)]
 
 
 class PlaneInfo(ctypes.Structure):
@@ -93,7 +94,7 @@ def _load():
     lib.w8_plan_shape.restype = st
     lib.w8_workspace_bytes.argtypes = [vp, i32, i32, ctypes.POINTER(sz)]
     lib.w8_workspace_bytes.restype = st
-    for name in ("w8_gemv", "bf16_gemv", "w8_gemv_silu_mul"):
+    for name in ("w8_gemv", "bf16_gemv", "w8_gemv_silu_mul", "mxfp4_gemv"):
         f = getattr(lib, name)
         f.argtypes = [vp, i32, vp, i64, i32, vp, i64, vp, sz, vp]
         f.restype = st
@@ -113,7 +114,8 @@ lib = _load()
 # every symbol include/w8.h declares
 EXPORTS = ("w8_status_str", "w8_abi_version", "w8_validate", "w8_packed_bytes", "w8_bind",
            "w8_release", "w8_build_planes", "w8_build_info", "w8_plan_info", "w8_plan_shape",
-           "w8_workspace_bytes", "w8_gemv", "bf16_gemv", "w8_gemv_silu_mul", "w8_gemv_noalloc",
+           "w8_workspace_bytes", "w8_gemv", "bf16_gemv", "w8_gemv_silu_mul", "mxfp4_gemv",
+           "w8_gemv_noalloc",
            "w8_packed_offset", "w8_gate_up_packed_row", "w8_device_status")
 
 
@@ -142,6 +144,7 @@ class Plane:
     scale: torch.Tensor | None = None
     bias: torch.Tensor | None = None
     layout: int = SRC_ROW_MAJOR
+    block_scale: torch.Tensor | None = None  # MXFP4: [n, ldb] uint8 E8M0 scales
 
     @staticmethod
     def from_tensor(w: torch.Tensor, scale: torch.Tensor | None = None, k: int | None = None,
@@ -165,11 +168,25 @@ class Plane:
         return Plane(w=w, dtype=dtype, n=w.shape[0], k=w.shape[1] if k is None else k,
                      ldw=w.stride(0), scale=scale, layout=layout)
 
+    @staticmethod
+    def mxfp4(w: torch.Tensor, block_scale: torch.Tensor, k: int | None = None,
+              layout: int = SRC_ROW_MAJOR) -> "Plane":
+        """An MXFP4 plane: w [n, ldw/2] uint8 (two codes a byte, the even
+        column in the low nibble), block_scale [n, ldb] uint8 E8M0."""
+        assert w.dim() == 2 and w.stride(1) == 1 and w.element_size() == 1
+        assert block_scale.dim() == 2 and block_scale.stride(1) == 1
+        ldw = 2 * w.stride(0)
+        return Plane(w=w, dtype=DT_MXFP4, n=w.shape[0], k=2 * w.shape[1] if k is None else k,
+                     ldw=ldw, layout=layout, block_scale=block_scale)
+
     def desc(self) -> PlaneDesc:
+        bs = self.block_scale
         return PlaneDesc(self.w.data_ptr() if self.w is not None else None, self.dtype,
                          self.layout, self.n, self.k, self.ldw,
                          self.scale.data_ptr() if self.scale is not None else None,
-                         self.bias.data_ptr() if self.bias is not None else None)
+                         self.bias.data_ptr() if self.bias is not None else None,
+                         bs.data_ptr() if bs is not None else None,
+                         bs.stride(0) if bs is not None else 0)
 
 
 def _descs(planes):
@@ -278,6 +295,12 @@ def bf16_gemv(build: Build, plane: int, x: torch.Tensor, y: torch.Tensor,
               workspace: torch.Tensor | None = None, m: int | None = None, stream=None):
     """y[:m, :N] = bf16(W x^T)^T on a BF16 build (one kernel launch)."""
     return _gemv(lib.bf16_gemv, build, plane, x, y, workspace, m, stream)
+
+
+def mxfp4_gemv(build: Build, plane: int, x: torch.Tensor, y: torch.Tensor,
+               workspace: torch.Tensor | None = None, m: int | None = None, stream=None):
+    """y[:m, :N] = bf16(dequant(W) x^T)^T on an MXFP4 build (one kernel launch)."""
+    return _gemv(lib.mxfp4_gemv, build, plane, x, y, workspace, m, stream)
 
 
 def w8_gemv_silu_mul(build: Build, plane: int, x: torch.Tensor, y: torch.Tensor,

@@ -29,6 +29,8 @@ class Projection:
 
     @property
     def weight_bytes(self) -> int:
+        if self.dtype == "mxfp4":  # codes, half a byte each, and one E8M0 byte per 32
+            return self.n * self.k // 2 + self.n * -(-self.k // 32)
         return self.n * self.k * (1 if self.dtype == "e4m3fn" else 2)
 
     @property
@@ -78,15 +80,21 @@ O_PROJ_LARGE_M = Projection("o_proj_large_m", 6144, 16384, "e4m3fn", LARGE_M)
 Q_B_LARGE_M = Projection("q_b_proj_large_m", 16384, 2048, "e4m3fn", LARGE_M)
 KV_B_LARGE_M = Projection("kv_b_proj_large_m", 28672, 512, "e4m3fn", LARGE_M)
 
+# w4a16: the same projections as MXFP4 planes (the GLM-5.2 anatomy page's
+# deployments serve a GLM-5.2-MXFP4 checkpoint), on the register ring.
+O_PROJ_MXFP4 = Projection("o_proj_mxfp4", 6144, 16384, "mxfp4", (1, 2, 8, 32))
+Q_B_MXFP4 = Projection("q_b_proj_mxfp4", 16384, 2048, "mxfp4", (1, 8, 64))
+FUSED_QKV_A_MXFP4 = Projection("fused_qkv_a_proj_mxfp4", 2624, 6144, "mxfp4", (1, 4, 16))
+
 ALL = (TINY, FUSED_QKV_A, O_PROJ, O_PROJ_BF16, SHARED_GATE_UP, SHARED_DOWN,
        SHARED_GATE_UP_KPAD, SHARED_GATE_UP_SILU, Q_B, KV_B, WQ_B, WK, WEIGHTS_PROJ, WK_WEIGHTS_PROJ, LM_HEAD,
-       O_PROJ_LARGE_M, Q_B_LARGE_M, KV_B_LARGE_M)
+       O_PROJ_LARGE_M, Q_B_LARGE_M, KV_B_LARGE_M, O_PROJ_MXFP4, Q_B_MXFP4, FUSED_QKV_A_MXFP4)
 BY_NAME = {p.name: p for p in ALL}
 
 # The workload groups, in order: the tiny correctness case, the fused
 # qkv_a projection, o_proj (FP8 and bf16), the shared-expert pair with its
 # K-padded variant and its gate_up with SiLU-and-multiply, the full-layer
-# sweep, and 96..256 tokens on the large attention projections.
+# sweep, 96..256 tokens on the large attention projections, and MXFP4 planes.
 GROUPS = {
     "tiny": (TINY,),
     "fused_qkv_a_proj": (FUSED_QKV_A,),
@@ -94,4 +102,5 @@ GROUPS = {
     "shared_expert": (SHARED_GATE_UP, SHARED_DOWN, SHARED_GATE_UP_KPAD, SHARED_GATE_UP_SILU),
     "layer_sweep": (Q_B, KV_B, WQ_B, WK, WEIGHTS_PROJ, WK_WEIGHTS_PROJ, LM_HEAD),
     "large_m": (O_PROJ_LARGE_M, Q_B_LARGE_M, KV_B_LARGE_M),
+    "mxfp4": (O_PROJ_MXFP4, Q_B_MXFP4, FUSED_QKV_A_MXFP4),
 }

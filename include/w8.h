@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define W8_ABI_VERSION 3
+#define W8_ABI_VERSION 4
 
 /* A cudaStream_t: the runtime's stream type is this same pointer type. */
 typedef struct CUstream_st *w8_stream;
@@ -60,7 +60,9 @@ typedef enum {
     W8_ERR_SHAPE = 6,     /* N or K < 1 or too large, ldw < K, M outside 0..256,
                              ldx < K, ldy < N (< N/2 for w8_gemv_silu_mul), or a
                              W8_SRC_GATE_UP plane whose N is not a multiple of 16 */
-    W8_ERR_SCALE = 7,     /* an FP8 plane without row scales, or a bf16 plane with them */
+    W8_ERR_SCALE = 7,     /* an FP8 plane without row scales, a bf16 or MXFP4 plane with
+                             them, an MXFP4 plane without block scales or ldb too short,
+                             or another plane with block scales */
     W8_ERR_LAYOUT = 8,    /* unknown source layout, or w8_gemv_silu_mul on a plane not
                              bound as W8_SRC_GATE_UP */
     W8_ERR_CAPACITY = 9,  /* packed buffer or workspace smaller than required */
@@ -82,7 +84,14 @@ typedef enum {
     W8_DT_BF16 = 2,
     W8_DT_E4M3FNUZ = 3,
     W8_DT_E5M2 = 4,
-    W8_DT_FP16 = 5
+    W8_DT_FP16 = 5,
+    /* w4a16: MXFP4 weights (ATOM Model Support Guide, Model-specific
+     * optimizations, DeepSeek V2/V3: FP4 support names MXFP4 GEMMs with
+     * 16-bit activations; the GLM-5.2 anatomy page deploys a GLM-5.2-MXFP4
+     * checkpoint).  The OCP microscaling format: E2M1 elements, two per
+     * byte (the even column in the low nibble), 32 consecutive elements
+     * along K sharing one E8M0 scale 2^(e - 127) (255 = NaN). */
+    W8_DT_MXFP4 = 6
 } w8_dtype;
 
 /* Source layouts: row-major [n][ldw] planes (K contiguous).
@@ -100,7 +109,10 @@ typedef enum {
  * rows in tiles of 16, K in blocks of 32, each (tile, block) a 512-byte
  * (FP8) or 1024-byte (bf16) run holding the 16x32 weights in the order of
  * the tensor-core A operand, one 16-byte vector per lane.  The K tail and
- * the row tail are zero-filled. */
+ * the row tail are zero-filled.  MXFP4: 288-byte runs, 256 bytes of codes
+ * (lane (g, t): 8 bytes, one 32-bit word per tensor-core step) then 8 words
+ * of block scales, word g = bf16 scale of row g | bf16 scale of row g+8 << 16
+ * (E8M0 0 -> bf16 2^-127, 255 -> NaN). */
 #define W8_LAYOUT_MMA_16x32 1
 /* The same layout for a W8_SRC_GATE_UP plane, with the rows interleaved:
  * packed 16-row tile t holds gate rows 8t..8t+7, then up rows 8t..8t+7 (the
@@ -111,27 +123,31 @@ typedef enum {
 
 /* One source weight plane: W[n][ldw] in device memory, row-major. */
 typedef struct {
-    const void *w;        /* device; E4M3 codes (1 byte) or bf16 bits (2 bytes);
-                             16-byte aligned */
+    const void *w;        /* device; E4M3 codes (1 byte), bf16 bits (2 bytes) or MXFP4
+                             codes (two per byte); 16-byte aligned */
     int32_t dtype;        /* w8_dtype */
     int32_t layout;       /* W8_SRC_ROW_MAJOR or W8_SRC_GATE_UP */
     int64_t n;            /* output rows, >= 1 */
     int64_t k;            /* logical reduction columns, >= 1; columns k..ldw-1 are ignored */
-    int64_t ldw;          /* row stride in elements, >= k, ldw * element bytes % 16 == 0 */
-    const float *scale;   /* device, [n] fp32 row scales: required for E4M3FN, NULL for BF16 */
+    int64_t ldw;          /* row stride in elements, >= k, ldw * element bytes % 16 == 0
+                             (MXFP4: ldw % 32 == 0) */
+    const float *scale;   /* device, [n] fp32 row scales: required for E4M3FN, NULL otherwise */
     const void *bias;     /* must be NULL */
+    const uint8_t *block_scale; /* device, MXFP4 only: [n][ldb] E8M0 scales, block j covering
+                             columns 32j .. 32j+31; NULL for the other dtypes */
+    int64_t ldb;          /* MXFP4: row stride of block_scale in bytes, >= ceil(k / 32) */
 } w8_plane_desc;
 
 /* What a build records about one bound plane. */
 typedef struct {
-    int32_t dtype;           /* W8_DT_E4M3FN or W8_DT_BF16 */
+    int32_t dtype;           /* W8_DT_E4M3FN, W8_DT_BF16 or W8_DT_MXFP4 */
     int32_t layout;          /* W8_LAYOUT_MMA_16x32 or W8_LAYOUT_MMA_16x32_GATE_UP */
     int64_t n, k;
     int64_t row_tiles;       /* ceil(n / 16) */
     int64_t k_blocks;        /* ceil(k / 32) */
     const void *packed;      /* device, inside the caller's packed buffer */
     const float *scale;      /* device, the build's copy of the row scales (FP8), else NULL */
-    size_t packed_bytes;     /* bytes of the packed weights */
+    size_t packed_bytes;     /* bytes of the packed weights (MXFP4: with the block scales) */
 } w8_plane_info;
 
 /* The launch a gemv call makes for one (plane, m); returned for inspection.
@@ -264,6 +280,19 @@ w8_status w8_gemv_silu_mul(const w8_build *b, int plane, const uint16_t *x, int6
                            uint16_t *y, int64_t ldy, void *workspace, size_t workspace_bytes,
                            w8_stream s);
 
+/* The w4a16 GEMV on an MXFP4 build: the same call with each weight dequantized
+ * as its E2M1 value times its block's E8M0 scale (exact in bf16),
+ *   y[i*ldy + n] = bf16(sum_k e2m1(W[n,k]) * 2^(bs[n, k/32] - 127) * x[i*ldx + k]),
+ * fp32 accumulation.  m: 0..64 (the register-ring kernel); W8_ERR_SHAPE above.
+ * A row holding a NaN scale, or a weight past fp32's range, gives NaN (the
+ * plain definition: NaN or inf times a zero token).  The same summation order
+ * as bf16_gemv for the same (N, K, m): with every scale 1 the result equals
+ * the bf16 plane of the dequantized weights bit for bit.
+ * Returns W8_ERR_DTYPE on another build.  One kernel launch on s. */
+w8_status mxfp4_gemv(const w8_build *b, int plane, const uint16_t *x, int64_t ldx, int m,
+                     uint16_t *y, int64_t ldy, void *workspace, size_t workspace_bytes,
+                     w8_stream s);
+
 /* The FP8 GEMV for callers that cannot allocate device memory.
  *
  * The pages have no counterpart of this entry point; it serves callers that
@@ -294,8 +323,10 @@ w8_status w8_gemv_noalloc(const w8_build *b, int plane, const uint16_t *x, int64
 /* Host-side address map of W8_LAYOUT_MMA_16x32: byte offset, inside one
  * plane's packed weights, of element (row, col) of a plane with k_blocks
  * blocks of 32 columns (row is the packed row: for a gate_up plane, see
- * w8_gate_up_packed_row).  dtype is W8_DT_E4M3FN or W8_DT_BF16; returns -1 on a
- * bad argument.  The repack kernel places every element at this offset. */
+ * w8_gate_up_packed_row).  dtype is W8_DT_E4M3FN, W8_DT_BF16 or W8_DT_MXFP4
+ * (for MXFP4 the NIBBLE offset: twice the byte offset, plus 1 for a high
+ * nibble); returns -1 on a bad argument.  The repack kernel places every
+ * element at this offset. */
 int64_t w8_packed_offset(int dtype, int64_t k_blocks, int64_t row, int64_t col);
 
 /* The packed row that holds source row `row` of a W8_SRC_GATE_UP plane of n

@@ -42,7 +42,7 @@ def test_every_declared_function_is_exported():
 
 
 def test_abi_version_and_status_strings():
-    assert w8.lib.w8_abi_version() == 3
+    assert w8.lib.w8_abi_version() == 4
     for code in range(15):
         assert w8.status_str(code)
     assert w8.status_str(99) == "unknown status"
@@ -53,10 +53,13 @@ FAKE = 0x10000  # a 16-byte aligned address; validate never dereferences it
 
 def _desc(**kw):
     d = dict(w=FAKE, dtype=w8.DT_E4M3FN, layout=0, n=64, k=128, ldw=128, scale=FAKE + 4096,
-             bias=None)
+             bias=None, block_scale=None, ldb=0)
     d.update(kw)
     return w8.PlaneDesc(d["w"], d["dtype"], d["layout"], d["n"], d["k"], d["ldw"], d["scale"],
-                        d["bias"])
+                        d["bias"], d["block_scale"], d["ldb"])
+
+
+MX = dict(dtype=w8.DT_MXFP4, scale=None, block_scale=FAKE + 8192, ldb=4)
 
 
 def _status(*descs):
@@ -92,6 +95,16 @@ def _status(*descs):
     ({"k": 130, "ldw": 144}, "W8_OK"),
     ({"dtype": w8.DT_BF16, "scale": None, "ldw": 132}, "W8_ERR_UNPADDED"),
     ({"dtype": w8.DT_BF16, "scale": None, "ldw": 136}, "W8_OK"),
+    # MXFP4: E8M0 block scales instead of row scales; rows of a multiple of 16 bytes
+    (dict(MX), "W8_OK"),
+    (dict(MX, k=100, ldw=128), "W8_OK"),
+    (dict(MX, block_scale=None), "W8_ERR_SCALE"),
+    (dict(MX, scale=FAKE + 4096), "W8_ERR_SCALE"),
+    (dict(MX, ldb=3), "W8_ERR_SCALE"),           # 128 columns need 4 blocks
+    (dict(MX, ldw=144), "W8_ERR_UNPADDED"),      # 72 bytes a row
+    (dict(MX, ldw=129, k=100), "W8_ERR_UNPADDED"),
+    (dict(MX, ldw=160), "W8_OK"),                # 80 bytes a row
+    ({"block_scale": FAKE + 8192, "ldb": 4}, "W8_ERR_SCALE"),  # FP8 plane with block scales
 ])
 def test_validate_refusal_matrix(kw, want):
     assert w8.STATUS[_status(_desc(**kw))] == want
@@ -105,6 +118,29 @@ def test_mixed_build_refused_and_empty_list():
     assert w8.STATUS[w8.lib.w8_validate(None, 0)] == "W8_ERR_NULL"
     # a bad plane anywhere in the list is reported before the mix check
     assert w8.STATUS[_status(_desc(), _desc(bias=FAKE))] == "W8_ERR_BIAS"
+
+
+def test_packed_bytes_mxfp4():
+    # [100, 200]: 7 tiles x 7 blocks x 288 B (codes and the rows' bf16 block scales)
+    assert w8.packed_bytes([_desc(n=100, k=200, ldw=224, **{k: v for k, v in MX.items()
+                                                          if k != "ldb"}, ldb=7)]) == \
+        -(-7 * 7 * 288 // 256) * 256
+
+
+def test_packed_nibble_map_is_a_bijection():
+    rt, kb = 3, 4
+    offs = [w8.packed_offset(w8.DT_MXFP4, kb, r, c) for r in range(rt * 16) for c in range(kb * 32)]
+    # every code nibble of every run exactly once; the last 64 nibbles of a
+    # 576-nibble run hold the block scales
+    runs = [(o // 576, o % 576) for o in offs]
+    assert all(within < 512 for _, within in runs)
+    assert sorted(o for o in offs) == sorted(run * 576 + w for run in range(rt * kb)
+                                             for w in range(512))
+    # lane (g, t) holds rows g, g+8 and columns 8t..8t+7 of its 8 bytes
+    for r in (0, 5, 8, 13):
+        for c in (0, 7, 8, 31):
+            o = w8.packed_offset(w8.DT_MXFP4, 1, r, c)
+            assert (o // 2) // 8 == 4 * (r % 8) + c // 8
 
 
 def test_packed_bytes_formula():

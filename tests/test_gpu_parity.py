@@ -454,8 +454,9 @@ def test_multi_plane_build(w8):
 # full-size workloads, sampled rows
 # ---------------------------------------------------------------------------
 
-# (gate_up planes with SiLU-and-multiply: tests/test_gpu_gate_up.py)
-FULL = [p for p in workloads.ALL if p.name != "lm_head" and not p.act]
+# (gate_up planes with SiLU-and-multiply: tests/test_gpu_gate_up.py; MXFP4
+# planes: tests/test_gpu_mxfp4.py)
+FULL = [p for p in workloads.ALL if p.name != "lm_head" and not p.act and p.dtype != "mxfp4"]
 
 
 @pytest.mark.parametrize("proj", FULL, ids=[p.name for p in FULL])
