@@ -427,9 +427,20 @@ int64_t w8_packed_offset(int dtype, int64_t k_blocks, int64_t row, int64_t col)
         return w8::packed_offset_fp8(k_blocks, row, col);
     if (dtype == W8_DT_BF16)
         return w8::packed_offset_bf16(k_blocks, row, col);
-    if (dtype == W8_DT_MXFP4)
-        return w8::packed_nibble_fp4(k_blocks, row, col);
-    return -1;
+    return -1; // MXFP4: w8_mxfp4_code_bits
+}
+
+w8_status w8_mxfp4_code_bits(int64_t k_blocks, int64_t row, int64_t col, int64_t *bits)
+{
+    if (!bits)
+        return W8_ERR_NULL;
+    if (k_blocks < 1 || row < 0 || col < 0 || col >= k_blocks * w8::kTileK)
+        return W8_ERR_SHAPE;
+    int64_t b[4];
+    w8::mxfp4_code_bits(k_blocks, row, col, b);
+    for (int i = 0; i < 4; ++i)
+        bits[i] = b[i];
+    return W8_OK;
 }
 
 int64_t w8_gate_up_packed_row(int64_t n, int64_t row)

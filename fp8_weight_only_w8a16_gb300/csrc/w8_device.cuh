@@ -190,13 +190,22 @@ __device__ __forceinline__ void zero_w(WFrag<kDt> &f)
     }
 }
 
-// Two E2M1 codes (nibbles 0 and 4 of x) -> the bf16x2 bit patterns of their
-// values times 2^-126, exactly: the sign goes to bit 15, the two exponent bits
-// and the mantissa bit to bits 8..6, so a normal code e >= 1 reads as
-// (1 + m/2) 2^(e - 127) and a subnormal one (e = 0) as m/2 2^-126.
-__device__ __forceinline__ uint32_t e2m1x2_bits(uint32_t x)
+// MXFP4 A registers from a packed code word (the bit places of w8_layout.h):
+// the bf16x2 bit patterns of two E2M1 values times 2^-126, exactly -- sign to
+// bit 15, exponent bits to 8..7, mantissa bit to 6, so a normal code e >= 1
+// reads as (1 + m/2) 2^(e - 127) and the subnormal one (e = 0) as m/2 2^-126.
+constexpr uint32_t kFp4Mask = 0x81C081C0u; // magnitudes at 6..8, 22..24, signs at 15, 31
+template <int kReg>
+__device__ __forceinline__ uint32_t e2m1x2_bits(uint32_t w)
 {
-    return ((x & 0x00070007u) << 6) | ((x & 0x00080008u) << 12);
+    if constexpr (kReg == 0)
+        return (w << 6) & kFp4Mask;
+    else if constexpr (kReg == 1)
+        return (w << 3) & kFp4Mask;
+    else if constexpr (kReg == 2)
+        return w & kFp4Mask;
+    else // bits 10, 11 -> 6, 7; 13 -> 8; 14 -> 15 (and the same 16 higher)
+        return ((w >> 4) & 0x00C000C0u) | ((w >> 5) & 0x01000100u) | ((w << 1) & 0x80008000u);
 }
 __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b)
 {
@@ -232,10 +241,10 @@ __device__ __forceinline__ void a_operands(uint32_t (&a)[8], const WFrag<kDt> &f
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const uint32_t w = q ? f.v.y : f.v.x;
-            a[4 * q + 0] = mul_bf16x2(mul_bf16x2(e2m1x2_bits(w), k2p126), sg);
-            a[4 * q + 1] = mul_bf16x2(mul_bf16x2(e2m1x2_bits(w >> 4), k2p126), sg8);
-            a[4 * q + 2] = mul_bf16x2(mul_bf16x2(e2m1x2_bits(w >> 8), k2p126), sg);
-            a[4 * q + 3] = mul_bf16x2(mul_bf16x2(e2m1x2_bits(w >> 12), k2p126), sg8);
+            a[4 * q + 0] = mul_bf16x2(mul_bf16x2(e2m1x2_bits<0>(w), k2p126), sg);
+            a[4 * q + 1] = mul_bf16x2(mul_bf16x2(e2m1x2_bits<1>(w), k2p126), sg8);
+            a[4 * q + 2] = mul_bf16x2(mul_bf16x2(e2m1x2_bits<2>(w), k2p126), sg);
+            a[4 * q + 3] = mul_bf16x2(mul_bf16x2(e2m1x2_bits<3>(w), k2p126), sg8);
         }
     }
 }

@@ -63,25 +63,44 @@ W8_HD int64_t packed_offset_fp8(int64_t k_blocks, int64_t row, int64_t col)
     return ((rt * k_blocks + kb) * 32 + lane) * 16 + byte;
 }
 
-// MXFP4 (w4a16): a (tile, block) run is 256 bytes of codes -- lane (g, t)
-// holds 8 bytes, one 32-bit word per tensor-core step q, whose nibbles 0/4,
-// 1/5, 2/6 and 3/7 are the (low, high) halves of the A registers (row g,
-// cols 8t+4q, +1), (row g+8, same), (row g, cols 8t+4q+2, +3), (row g+8,
-// same) -- then 8 words of block scales, word g = bf16 scale of row g | bf16
-// scale of row g+8 << 16.
+// MXFP4 (w4a16): a (tile, block) run is 256 bytes of codes, then 8 words of
+// block scales (word g = bf16 scale of row g | bf16 scale of row g+8 << 16).
+// Lane (g, t) holds 8 bytes: word q for tensor-core step q, whose four A
+// registers (row g, cols 8t+4q, +1), (row g+8, same), (row g, cols 8t+4q+2,
+// +3), (row g+8, same) each take 8 bits -- the (low, high) elements'
+// magnitude bits (mantissa, exponent low, exponent high) and sign bits -- at
+// places that one shift and one mask carry to their bf16 positions (6..8 and
+// 15 for the low element, 22..24 and 31 for the high one): registers 0, 1, 2
+// at bit o = 0, 3, 6 (magnitude at o..o+2 and o+16..o+18, signs at o+9 and
+// o+25), register 3 in the remaining bits 10, 11, 13 (magnitude), 14 (sign)
+// and 26, 27, 29, 30.
 constexpr int kRunFp4 = 288;
 constexpr int kRunFp4Codes = 256;
 
-// Nibble offset of element (row, col)'s code in an MXFP4 plane's packed runs.
-W8_HD int64_t packed_nibble_fp4(int64_t k_blocks, int64_t row, int64_t col)
+// Bit offsets, inside a plane's packed MXFP4 runs, of element (row, col)'s
+// mantissa, exponent-low, exponent-high and sign bits.
+W8_HD void mxfp4_code_bits(int64_t k_blocks, int64_t row, int64_t col, int64_t (&bits)[4])
 {
     const int64_t rt = row >> 4, kb = col >> 5;
     const int r = int(row & 15), c = int(col & 31);
     const int g = r & 7, hi = r >> 3, t = c >> 3, j = c & 7;
     const int lane = g * 4 + t;
     const int q = j >> 2, jj = j & 3;
-    const int p = ((jj & 1) << 2) + ((jj >> 1) << 1) + hi;
-    return ((rt * k_blocks + kb) * kRunFp4 + lane * 8) * 2 + q * 8 + p;
+    const int reg = (jj >> 1) * 2 + hi, half = jj & 1;
+    const int64_t base = ((rt * k_blocks + kb) * kRunFp4 + lane * 8 + q * 4) * 8;
+    if (reg < 3) {
+        const int o = 3 * reg + 16 * half;
+        bits[0] = base + o;
+        bits[1] = base + o + 1;
+        bits[2] = base + o + 2;
+        bits[3] = base + o + 9;
+    } else {
+        const int o = 16 * half;
+        bits[0] = base + o + 10;
+        bits[1] = base + o + 11;
+        bits[2] = base + o + 13;
+        bits[3] = base + o + 14;
+    }
 }
 
 W8_HD int64_t packed_offset_bf16(int64_t k_blocks, int64_t row, int64_t col)

@@ -10,8 +10,9 @@
 // A gate_up plane (a merged [2I, K] MLP projection) is read with its gate and
 // up rows interleaved eight at a time, so that a tile's rows g and g+8 are a
 // gate row and its up row.
-// MXFP4 planes pack two codes a byte into 288-byte runs whose last 32 bytes
-// carry the rows' block scales as bf16 pairs.
+// MXFP4 planes pack their codes into 288-byte runs (each code's four bits at
+// the places the kernel's widening reads) whose last 32 bytes carry the rows'
+// block scales as bf16 pairs.
 // FP8 also writes the build's copy of the row scales; a row that holds a NaN
 // code (0x7F or 0xFF) gets a NaN scale, so its outputs are NaN as the
 // definition gives, while the GEMV's widening stays a fixed exact map.
@@ -190,20 +191,25 @@ __global__ void __launch_bounds__(256) repack_fp4_kernel(const RepackArgs a)
             hi = load8_fp4(a.src + src_row(a, n1) * a.ld_bytes, col, a.k);
             shi = e8m0_to_bf16(a.bscale_src[src_row(a, n1) * a.ldb + kb]);
         }
-        // word q, nibble p: column c = 4q + (p & 4 ? 1 : 0) + (p & 2 ? 2 : 0) of
-        // the lane's 8, from row g (p even) or row g+8 (p odd)
-        uint32_t out[2];
+        // word q holds A registers reg = 0..3 of step q: (row g, cols 4q, +1),
+        // (row g+8, same), (row g, cols 4q+2, +3), (row g+8, same) of the lane's
+        // 8 columns, each element's mantissa, exponent-low, exponent-high and
+        // sign bits at the places of mxfp4_code_bits (w8_layout.h)
+        uint32_t out[2] = {0u, 0u};
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            uint32_t wv = 0;
+        for (int q = 0; q < 2; ++q)
 #pragma unroll
-            for (int p = 0; p < 8; ++p) {
-                const int c = 4 * q + ((p >> 2) & 1) + (p & 2);
-                const uint32_t src = (p & 1) ? hi : lo;
-                wv |= ((src >> (4 * c)) & 15u) << (4 * p);
-            }
-            out[q] = wv;
-        }
+            for (int reg = 0; reg < 4; ++reg)
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int c = 4 * q + 2 * (reg >> 1) + half;
+                    const uint32_t code = (((reg & 1) ? hi : lo) >> (4 * c)) & 15u;
+                    const int o = reg < 3 ? 3 * reg + 16 * half : 16 * half;
+                    const int om = reg < 3 ? o : o + 10, oe0 = reg < 3 ? o + 1 : o + 11;
+                    const int oe1 = reg < 3 ? o + 2 : o + 13, os = reg < 3 ? o + 9 : o + 14;
+                    out[q] |= ((code & 1u) << om) | (((code >> 1) & 1u) << oe0) |
+                              (((code >> 2) & 1u) << oe1) | (((code >> 3) & 1u) << os);
+                }
         uint8_t *run = a.dst + (rt * a.kb + kb) * kRunFp4;
         *reinterpret_cast<uint2 *>(run + lane * 8) = make_uint2(out[0], out[1]);
         if (t == 0)

@@ -102,6 +102,8 @@ def _load():
     lib.w8_gemv_noalloc.restype = st
     lib.w8_packed_offset.argtypes = [i32, i64, i64, i64]
     lib.w8_packed_offset.restype = i64
+    lib.w8_mxfp4_code_bits.argtypes = [i64, i64, i64, ctypes.POINTER(i64)]
+    lib.w8_mxfp4_code_bits.restype = st
     lib.w8_gate_up_packed_row.argtypes = [i64, i64]
     lib.w8_gate_up_packed_row.restype = i64
     lib.w8_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), i32]
@@ -116,7 +118,7 @@ EXPORTS = ("w8_status_str", "w8_abi_version", "w8_validate", "w8_packed_bytes", 
            "w8_release", "w8_build_planes", "w8_build_info", "w8_plan_info", "w8_plan_shape",
            "w8_workspace_bytes", "w8_gemv", "bf16_gemv", "w8_gemv_silu_mul", "mxfp4_gemv",
            "w8_gemv_noalloc",
-           "w8_packed_offset", "w8_gate_up_packed_row", "w8_device_status")
+           "w8_packed_offset", "w8_mxfp4_code_bits", "w8_gate_up_packed_row", "w8_device_status")
 
 
 def _check(status: int):
@@ -337,6 +339,14 @@ def device_status(reset: bool = False) -> int:
 
 def packed_offset(dtype: int, k_blocks: int, row: int, col: int) -> int:
     return int(lib.w8_packed_offset(dtype, k_blocks, row, col))
+
+
+def mxfp4_code_bits(k_blocks: int, row: int, col: int) -> tuple:
+    """Bit offsets of an MXFP4 element's (mantissa, exponent low, exponent
+    high, sign) bits in the packed runs."""
+    out = (ctypes.c_int64 * 4)()
+    _check(lib.w8_mxfp4_code_bits(k_blocks, row, col, out))
+    return tuple(out)
 
 
 def gate_up_packed_row(n: int, row: int) -> int:

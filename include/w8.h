@@ -110,9 +110,9 @@ typedef enum {
  * (FP8) or 1024-byte (bf16) run holding the 16x32 weights in the order of
  * the tensor-core A operand, one 16-byte vector per lane.  The K tail and
  * the row tail are zero-filled.  MXFP4: 288-byte runs, 256 bytes of codes
- * (lane (g, t): 8 bytes, one 32-bit word per tensor-core step) then 8 words
- * of block scales, word g = bf16 scale of row g | bf16 scale of row g+8 << 16
- * (E8M0 0 -> bf16 2^-127, 255 -> NaN). */
+ * (lane (g, t): 8 bytes, one 32-bit word per tensor-core step, bit places of
+ * w8_mxfp4_code_bits) then 8 words of block scales, word g = bf16 scale of
+ * row g | bf16 scale of row g+8 << 16 (E8M0 0 -> bf16 2^-127, 255 -> NaN). */
 #define W8_LAYOUT_MMA_16x32 1
 /* The same layout for a W8_SRC_GATE_UP plane, with the rows interleaved:
  * packed 16-row tile t holds gate rows 8t..8t+7, then up rows 8t..8t+7 (the
@@ -323,11 +323,19 @@ w8_status w8_gemv_noalloc(const w8_build *b, int plane, const uint16_t *x, int64
 /* Host-side address map of W8_LAYOUT_MMA_16x32: byte offset, inside one
  * plane's packed weights, of element (row, col) of a plane with k_blocks
  * blocks of 32 columns (row is the packed row: for a gate_up plane, see
- * w8_gate_up_packed_row).  dtype is W8_DT_E4M3FN, W8_DT_BF16 or W8_DT_MXFP4
- * (for MXFP4 the NIBBLE offset: twice the byte offset, plus 1 for a high
- * nibble); returns -1 on a bad argument.  The repack kernel places every
- * element at this offset. */
+ * w8_gate_up_packed_row).  dtype is W8_DT_E4M3FN or W8_DT_BF16 (MXFP4 codes
+ * are not byte-addressable: see w8_mxfp4_code_bits); returns -1 on a bad
+ * argument.  The repack kernel places every element at this offset. */
 int64_t w8_packed_offset(int dtype, int64_t k_blocks, int64_t row, int64_t col);
+
+/* Host-side address map of an MXFP4 plane's packed runs: the BIT offsets of
+ * element (row, col)'s mantissa, exponent-low, exponent-high and sign bits
+ * (bits[0..3]; bit b is bit b % 8 of byte b / 8).  In each 16 x 32 run,
+ * lane (g, t)'s 8 bytes hold one 32-bit word per tensor-core step whose four
+ * A registers each keep their two elements' bits where one shift and one
+ * mask put them at bf16 bits 6..8 / 15 and 22..24 / 31.  W8_ERR_SHAPE on a
+ * bad argument.  Host-only. */
+w8_status w8_mxfp4_code_bits(int64_t k_blocks, int64_t row, int64_t col, int64_t *bits);
 
 /* The packed row that holds source row `row` of a W8_SRC_GATE_UP plane of n
  * rows (W8_LAYOUT_MMA_16x32_GATE_UP); -1 on a bad argument (n not a positive

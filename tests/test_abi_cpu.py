@@ -127,20 +127,25 @@ def test_packed_bytes_mxfp4():
         -(-7 * 7 * 288 // 256) * 256
 
 
-def test_packed_nibble_map_is_a_bijection():
+def test_mxfp4_bit_map_is_a_bijection_onto_the_code_bits():
     rt, kb = 3, 4
-    offs = [w8.packed_offset(w8.DT_MXFP4, kb, r, c) for r in range(rt * 16) for c in range(kb * 32)]
-    # every code nibble of every run exactly once; the last 64 nibbles of a
-    # 576-nibble run hold the block scales
-    runs = [(o // 576, o % 576) for o in offs]
-    assert all(within < 512 for _, within in runs)
-    assert sorted(o for o in offs) == sorted(run * 576 + w for run in range(rt * kb)
-                                             for w in range(512))
-    # lane (g, t) holds rows g, g+8 and columns 8t..8t+7 of its 8 bytes
+    bits = [b for r in range(rt * 16) for c in range(kb * 32)
+            for b in w8.mxfp4_code_bits(kb, r, c)]
+    # every code bit of every 288-byte run exactly once; its last 256 bits
+    # hold the block scales
+    assert sorted(bits) == [run * 2304 + b for run in range(rt * kb) for b in range(2048)]
+    assert w8.packed_offset(w8.DT_MXFP4, kb, 0, 0) == -1
     for r in (0, 5, 8, 13):
         for c in (0, 7, 8, 31):
-            o = w8.packed_offset(w8.DT_MXFP4, 1, r, c)
-            assert (o // 2) // 8 == 4 * (r % 8) + c // 8
+            m, e0, e1, sg = w8.mxfp4_code_bits(1, r, c)
+            # lane (g, t) owns bytes 8 (4g + t) .. + 7 of the run
+            assert all(b // 64 == 4 * (r % 8) + c // 8 for b in (m, e0, e1, sg))
+            # one shift carries the magnitude to bf16 bits 6..8 and the sign to
+            # 15 (low element) or 22..24 and 31 (high element) of its word:
+            # consecutive magnitude bits except in the spare register (13)
+            assert e0 == m + 1 and (e1 == m + 2 or e1 == m + 3)
+    with pytest.raises(w8.W8Error):
+        w8.mxfp4_code_bits(1, 0, 32)
 
 
 def test_packed_bytes_formula():

@@ -7,7 +7,7 @@ scale per 32 columns.  mxfp4_gemv computes y = bf16(sum_k e2m1(W) 2^(e-127)
 x) with fp32 accumulation on the register-ring kernel (1..64 tokens).
 Checked against the oracle:
 
-* the repack places every code where the host nibble map says and writes
+* the repack places every code bit where the host bit map says and writes
   each run's bf16 block-scale words;
 * random seeded inputs over ragged N and K, every token-group count and
   split K, within the GEMV tolerance of the oracle's fp64 recompute;
@@ -68,7 +68,7 @@ def _run(w8, b, x, n, fn=None):
 
 
 @pytest.mark.parametrize("n,k", [(37, 77), (16, 32), (100, 300), (5, 1)])
-def test_repack_matches_host_nibble_map(w8, n, k):
+def test_repack_matches_host_bit_map(w8, n, k):
     plane, _ = _case(1, n, k, 1)
     b, _src = _bind(w8, plane)
     info = b.info(0)
@@ -80,9 +80,9 @@ def test_repack_matches_host_nibble_map(w8, n, k):
     want = np.zeros(info.packed_bytes, dtype=np.uint8)
     for r in range(rt * 16):
         for c in range(kb * 32):
-            o = w8.packed_offset(w8.DT_MXFP4, kb, r, c)
-            code = (plane.w[r, c // 2] >> (4 * (c & 1))) & 15 if (r < n and c < k) else 0
-            want[o // 2] |= np.uint8(code << (4 * (o & 1)))
+            code = int(plane.w[r, c // 2] >> (4 * (c & 1))) & 15 if (r < n and c < k) else 0
+            for i, b in enumerate(w8.mxfp4_code_bits(kb, r, c)):
+                want[b // 8] |= np.uint8(((code >> i) & 1) << (b % 8))
     # the scale words: bf16 of 2^(e - 127) for rows g and g+8 of each run
     def bf16_of(e):
         return 0x0040 if e == 0 else 0x7FC0 if e == 255 else (int(e) << 7)
