@@ -1,7 +1,7 @@
 // w8_device.cuh -- device helpers shared by the GEMV kernels of libw8:
-// streaming weight loads, the exact E4M3 -> bf16 widening, the weight operand
-// fragments of the packed layout (w8_layout.h), rounding, asynchronous copies
-// and programmatic-dependent-launch controls.
+// streaming weight loads, the exact E4M3 -> bf16 and MXFP4 -> bf16
+// widenings, the weight operand fragments of the packed layout (w8_layout.h),
+// rounding, asynchronous copies and programmatic-dependent-launch controls.
 #pragma once
 
 #include <cuda_runtime.h>

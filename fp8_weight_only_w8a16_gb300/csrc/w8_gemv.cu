@@ -1,4 +1,4 @@
-// w8_gemv.cu -- the w8a16 / bf16 decode GEMV for sm_103a.
+// w8_gemv.cu -- the w8a16 / bf16 / w4a16 decode GEMV for sm_103a.
 //
 // Computes, per output row n and decode token m (ATOM PR #2980, Summary and
 // Changes),
@@ -6,7 +6,10 @@
 // with fp32 accumulation.  The E4M3 codes widen exactly to bf16 in registers,
 // feed bf16 tensor-core steps (mma.sync m16n8k16, fp32 accumulators) with the
 // decode tokens as the instruction's N = 8 dimension, and the fp32 row scale
-// multiplies the reduced row right before the single bf16 rounding.
+// multiplies the reduced row right before the single bf16 rounding.  bf16
+// planes skip the widening and the scale; MXFP4 planes (the ATOM Model
+// Support Guide's FP4 GEMMs with 16-bit activations) widen each code times
+// its E8M0 block scale exactly to bf16 instead, with no row scale.
 //
 // Why tensor cores for a GEMV: at M = 8 every weight byte costs 8 multiply-adds;
 // at the HBM rate that is ~5e13 FMA/s, more than the fp32 pipes sustain once

@@ -230,16 +230,6 @@ __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *
                  : "memory");
 }
 
-// A operand of one 32-column block for 16 rows, registers in the order of
-// tcgen05.st 16x256b.x2: (row g, step 0 cols 2t, 2t+1), (row g+8, same),
-// (row g, step 1), (row g+8, step 1).
-__device__ __forceinline__ void tm_store_a(uint32_t taddr, const uint32_t (&r)[8])
-{
-    asm volatile("tcgen05.st.sync.aligned.16x256b.x2.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
-                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-                 : "memory");
-}
-
 // The A operand of a whole stage (4 blocks = 64 columns) for 16 rows:
 // tcgen05.st 16x256b.x8, registers 8j..8j+7 = block j in tm_store_a's order.
 __device__ __forceinline__ void tm_store_stage(uint32_t taddr, const uint32_t (&r)[32])
