@@ -585,12 +585,17 @@ def run_one(args):
     s_d = torch.from_numpy(plane.scale).to(device) if plane.scale is not None else None
     dt = w8.DT_E4M3FN if proj.dtype == "e4m3fn" else w8.DT_BF16
     silu = proj.act == "silu_mul"
-    b = w8.bind([w8.Plane.from_tensor(w_d, s_d, k=proj.k, dtype=dt,
-                                      layout=w8.SRC_GATE_UP if silu else w8.SRC_ROW_MAJOR)])
+    mx = proj.dtype == "mxfp4"
+    if mx:
+        b = w8.bind([w8.Plane.mxfp4(w_d, s_d, k=proj.k)])
+    else:
+        b = w8.bind([w8.Plane.from_tensor(w_d, s_d, k=proj.k, dtype=dt,
+                                          layout=w8.SRC_GATE_UP if silu else w8.SRC_ROW_MAJOR)])
     ws = b.new_workspace()
     x = torch.from_numpy(np.ascontiguousarray(x_all[:m]).view(np.int16)).to(device)
     y = torch.zeros((m, proj.out_n), dtype=torch.int16, device=device)
-    fn = (w8.w8_gemv_silu_mul if silu else w8.w8_gemv if dt == w8.DT_E4M3FN else w8.bf16_gemv)
+    fn = (w8.w8_gemv_silu_mul if silu else w8.mxfp4_gemv if mx
+          else w8.w8_gemv if dt == w8.DT_E4M3FN else w8.bf16_gemv)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # 2 x L2
     for _ in range(args.calls):
         flush.zero_()
