@@ -24,7 +24,8 @@
  *  - Every function returns a w8_status.  Arguments are checked on the host
  *    before anything is enqueued; nothing traps on the device and no function
  *    exits the process.  A failed launch or CUDA call returns W8_ERR_CUDA.
- *  - w8_gemv and bf16_gemv are asynchronous on the caller's stream, never
+ *  - The gemv calls (w8_gemv, bf16_gemv, mxfp4_gemv, w8_gemv_silu_mul,
+ *    w8_gemv_noalloc) are asynchronous on the caller's stream, never
  *    synchronise and launch exactly one kernel, with programmatic dependent
  *    launch: the kernel may begin streaming weights while the previous kernel
  *    of the stream drains, and reads activations and writes outputs only
