@@ -1,13 +1,13 @@
 // w8_api.cu -- the C ABI of libw8 (declared and documented in include/w8.h).
 //
-// Host-side validation and binding follow the bind/refuse rules of ATOM PR
-// #2980 (Changes: "binds FP8 planes in place and refuses what the kernels
-// can't read, such as a non-E4M3fn or unpadded plane, a bias, or bf16 and
-// FP8 mixed in one build"; Limitations: e4m3fnuz and every other format are
-// refused at bind).  The gemv entry points take the same arguments for both
-// weight dtypes; the FP8 row scales travel with the build and reach the
-// kernel as its trailing data (Changes: "passes the row scales as the last
-// kernel arguments, so bf16 builds keep their argument layout").
+// Host-side validation and binding follow the refusals of ATOM PR #2980
+// (Changes and Limitations): a plane in any 8-bit format other than E4M3fn,
+// a row stride or base that is not 16-byte aligned, a bias, and a build that
+// mixes bf16 with FP8 are turned away at bind.  The gemv entry points take
+// the same arguments for every weight dtype; the FP8 row scales travel with
+// the build and reach the kernel after the other arguments, so the bf16
+// call's arguments are those of the FP8 one without them (the PR appends the
+// scales in the same way).
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>

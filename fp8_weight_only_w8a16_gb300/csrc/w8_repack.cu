@@ -1,7 +1,7 @@
 // w8_repack.cu -- bind-time repack of a row-major plane into W8_LAYOUT_MMA_16x32.
 //
-// The PR page (Changes) binds FP8 planes "in place" in AITER's (16, 16)
-// preshuffle; here bind instead copies each plane once into the caller's
+// The PR page (Changes) keeps each FP8 plane where it lies, in the (16, 16)
+// preshuffle that AITER uses; here bind instead copies each plane once into the caller's
 // packed buffer, in the order the GEMV's tensor-core A operand wants (see
 // w8_layout.h).  One CTA per 16-row tile.  Each thread produces one lane's
 // 16-byte vector of one K block: it reads 8 consecutive columns of rows g and

@@ -9,8 +9,8 @@ library routines:
 * draws: numpy PCG64 (``default_rng(seed)``), standard normal in fp32; the
   weights are N(0, 0.02) and the activations N(0, 1);
 * activations: fp32 -> bf16 through ``torch.Tensor.to(torch.bfloat16)``;
-* FP8 planes: the ptpc_fp8 weight format of ATOM PR #2980 (Summary: "E4M3 ...,
-  an fp32 scale per row"): scale[n] = amax_n / 448 in fp32 (an all-zero row
+* FP8 planes: the ptpc_fp8 weight format of ATOM PR #2980 (Summary: E4M3
+  codes with one fp32 factor for each row): scale[n] = amax_n / 448 in fp32 (an all-zero row
   gets scale 1), codes = E4M3(W / scale) clamped to +-448 and rounded through
   ``torch.float8_e4m3fn`` (round to nearest even);
 * bf16 planes: fp32 -> bf16 through torch;
@@ -21,7 +21,7 @@ library routines:
   nearest E2M1 value (ties to the even code), saturating at +-6; two codes per
   byte, the even column in the low nibble.
 
-Draw order per workload: the weight plane first, then a [64, K] activation
+Draw order per workload: the weight plane first, then a [256, K] activation
 block whose first M rows are the M decode tokens, so every M of one workload
 sees the same prefix of tokens.
 """

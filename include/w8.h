@@ -8,12 +8,11 @@
  *
  *     y[m, n] = bf16_rne( scale[n] * sum_k bf16(W[n, k]) * x[m, k] )
  *
- * W is an E4M3fn plane with one fp32 scale per output row ("E4M3 ..., an fp32
- * scale per row"); every E4M3fn code widens exactly to bf16 ("FP8 widens
- * exactly to bf16"); accumulation is fp32 and the scale multiplies each fully
- * reduced row before the single bf16 rounding ("scales each reduced row before
- * the bf16 rounding").  A bf16 plane runs through the same computation with no
- * scale ("bf16 planes run as before").
+ * W is an E4M3fn plane carrying a single fp32 factor for every output row;
+ * each of its codes converts to a bf16 value with no rounding; the products
+ * are summed in fp32, and the row's factor is applied to that finished sum
+ * just before the one conversion to bf16.  A bf16 plane takes the same path
+ * with no factor at all (the PR keeps bf16 weights on their existing path).
  *
  * Conventions for every function below:
  *  - Pointers named "device" point into CUDA device memory of the device that
@@ -76,10 +75,9 @@ typedef enum {
                              library's fixed W8_NOALLOC_SCRATCH_BYTES */
 } w8_status;
 
-/* Source element types.  Only E4M3FN and BF16 are readable (PR page, Changes
- * and Limitations: "refuses what the kernels can't read, such as a
- * non-E4M3fn ... plane"; "anything else, including e4m3fnuz ..., is refused
- * at bind"). */
+/* Source element types.  Bind accepts E4M3FN, BF16 and (w4a16) MXFP4 and
+ * refuses every other format, e4m3fnuz among them (the PR page, Changes and
+ * Limitations: bind turns away planes its kernels cannot decode). */
 typedef enum {
     W8_DT_E4M3FN = 1,
     W8_DT_BF16 = 2,
@@ -106,7 +104,7 @@ typedef enum {
 #define W8_SRC_GATE_UP 1
 
 /* Packed layout the kernels read (recorded in every build; the PR page,
- * Limitations, notes its own layout "isn't recorded on the tensor"):
+ * Limitations, says its own tensors do not carry their layout):
  * rows in tiles of 16, K in blocks of 32, each (tile, block) a 512-byte
  * (FP8) or 1024-byte (bf16) run holding the 16x32 weights in the order of
  * the tensor-core A operand, one 16-byte vector per lane.  The K tail and
@@ -263,9 +261,10 @@ w8_status bf16_gemv(const w8_build *b, int plane, const uint16_t *x, int64_t ldx
                     w8_stream s);
 
 /* The merged gate_up projection followed by SiLU-and-multiply, in one kernel
- * (ATOM Model Support Guide, Model architecture details, Llama MLP: merged
- * gate+up, SiLU+mul activation, then down; Model-specific optimizations:
- * the activation fused into the kernel next to it).  On a plane bound as
+ * (ATOM Model Support Guide, Model architecture details, Llama MLP: one
+ * merged projection for gate and up, the SiLU-and-multiply activation, then
+ * the down projection; Model-specific optimizations: the activation fused
+ * into a neighbouring kernel).  On a plane bound as
  * W8_SRC_GATE_UP (n = 2I), for 0 <= i < m and 0 <= j < I:
  *   g = the GEMV's output for source row j (what w8_gemv / bf16_gemv give),
  *   u = the GEMV's output for source row I + j,

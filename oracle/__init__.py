@@ -8,8 +8,8 @@ legs of ``bench.py`` use it.
 The arithmetic lives in ``w8_oracle.c`` (plain C, fp32 ascending-k
 accumulation, one fp32 scale multiply, one bf16 round to nearest even), which
 follows ATOM pull request #2980, sections Summary and
-Changes: the E4M3 plane widens exactly to bf16 and the fp32 row scale
-multiplies each reduced row before the bf16 rounding.  ``brute.py`` is an
+Changes: every E4M3 code has an exact bf16 value, and the fp32 row factor is
+applied to the finished row sum, ahead of the one conversion to bf16.  ``brute.py`` is an
 independent numpy fp64 recompute used to pin it.  It also holds the MLP
 activation that follows a merged gate_up projection (ATOM Model Support
 Guide, Model architecture details, Llama MLP): h = silu(g) * u in fp64 with

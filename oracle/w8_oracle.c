@@ -11,12 +11,11 @@
  *
  *     y[m,n] = bf16_rne( scale[n] * sum_k widen(W[n,k]) * x[m,k] )
  *
- * with W an E4M3fn plane (one fp32 scale per row; the scale multiplies the
- * fully reduced row, before the single bf16 rounding), x bf16 activations and
+ * with W an E4M3fn plane (one fp32 factor for each output row, applied once
+ * the row's sum is complete and ahead of the one bf16 rounding), x bf16 activations and
  * fp32 accumulation.  A bf16 plane runs through the same computation with no
- * scale ("bf16 planes run as before").  The FP8 codes widen exactly to bf16
- * ("FP8 widens exactly to bf16"), so the widening is the exact value of the
- * code.
+ * scale (the PR leaves bf16 weights on their existing path).  Each E4M3 code
+ * has an exact bf16 value, so the widening is the exact value of the code.
  *
  * Everything here is the plain definition: scalar loops, ascending k, fp32
  * accumulation, one fp32 multiply by the scale, one round-to-nearest-even to

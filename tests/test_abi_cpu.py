@@ -1,7 +1,8 @@
 """Host-side tests of the C ABI (no GPU): the library loads and exports every
-symbol include/w8.h declares; w8_validate refuses what the PR page says bind
-refuses (Changes: "a non-E4M3fn or unpadded plane, a bias, or bf16 and FP8
-mixed in one build"; Limitations: e4m3fnuz and every other format); the
+symbol include/w8.h declares; w8_validate refuses the planes the PR page's
+bind step turns away (Changes: any FP8 format other than E4M3fn, a plane
+without padding, a bias term, a build that mixes bf16 and FP8 planes;
+Limitations: e4m3fnuz and the remaining formats); the
 packed address map is a bijection that keeps each lane's 16-byte vector
 inside one (row tile, K block); the launch planner covers K exactly and does
 not depend on the weight dtype.  No compute call is made here.

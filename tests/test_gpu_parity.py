@@ -1,9 +1,9 @@
 """GPU parity of the w8a16 / bf16 GEMV against the CPU oracle, through the C ABI.
 
-What is checked (ATOM PR #2980, Testing: the kernels "equal the dequantized
-product bit for bit at 1, 5 and 16 tokens and read all 254 finite E4M3 codes
-exactly"; served checks "within worst-case fp32 rounding of an fp64
-recompute"):
+What is checked (ATOM PR #2980, Testing: the PR compares its kernels with the
+dequantized product, bit-identical for token counts 1, 5 and 16, and checks that
+every finite E4M3 code is read without error; its served outputs are held to
+the fp32 rounding bound against an fp64 recomputation):
 
 * random seeded inputs, many shapes with ragged N and K tails and every
   token-count regime, within |y - y64| <= 2^-7 |y64| + 2^-12 sum|scale W x|

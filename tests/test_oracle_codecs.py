@@ -3,9 +3,9 @@
 Each check holds the C oracle to something other than itself: closed-form
 values of the E4M3fn format (tests/golden/e4m3_special_codes.txt), torch's own
 float8_e4m3fn and bfloat16 conversions, and structural invariants of the
-format (ordering, uniform spacing within a binade).  The method relies on
-"FP8 widens exactly to bf16" (ATOM PR #2980, Summary) and the GPU tests read
-"all 254 finite E4M3 codes" (same page, Testing).
+format (ordering, uniform spacing within a binade).  The method depends on
+every E4M3 code having an exact bf16 value (ATOM PR #2980, Summary), and the
+GPU tests cover each of the format's finite codes (same page, Testing).
 """
 from __future__ import annotations
 

@@ -1,10 +1,10 @@
 """Pins for the oracle's GEMV (CPU only).
 
 The oracle computes y[m,n] = bf16_rne(scale[n] * sum_k W[n,k] x[m,k]) with
-fp32 accumulation in ascending k (ATOM PR #2980, Summary and Changes: FP8
-widens exactly to bf16, the fp32 row scale multiplies each reduced row before
-the bf16 rounding).  These tests pin it to things it cannot agree with by
-construction:
+fp32 accumulation in ascending k (ATOM PR #2980, Summary and Changes: each
+E4M3 code has an exact bf16 value, and the fp32 row factor is applied to the
+finished row sum ahead of the one conversion to bf16).  These tests pin it to
+things it cannot agree with by construction:
 
 * an independent fp64 brute force (torch dtypes + numpy matmul) on tiny
   inputs, within the stated tolerance, and the oracle's own fp64 recompute
@@ -137,8 +137,8 @@ def test_exact_sum_inputs_match_rational_result(orc):
 def test_scale_multiplies_the_reduced_row_once(orc):
     """Exact-sum rows with arbitrary fp32 scales: the result must be
     bf16(fp32(scale * acc)) with acc the exact row sum -- one fp32 multiply of
-    the reduced row, then one bf16 rounding (PR page, Changes: "scales each
-    reduced row before the bf16 rounding").  Scaling each product, or rounding
+    the reduced row, then one bf16 rounding (PR page, Changes: the factor is
+    applied to the finished row sum, ahead of the conversion).  Scaling each product, or rounding
     acc to bf16 before scaling, gives other bits on many of these rows."""
     rng = np.random.default_rng(14)
     n, k, m = 32, 48, 4

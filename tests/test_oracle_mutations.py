@@ -4,8 +4,9 @@ Each case plants one plausible mistake in a copy of oracle/w8_oracle.c,
 compiles the copy to a temporary library and reruns the pins against it: at
 least one pin must fail.  This is how the pins show they would catch a
 dropped term, a wrong sign, index or exponent, a misplaced scale or a wrong
-rounding in the oracle (the PR page, Testing, asks the same of its kernel
-tests: "breaking the row scale or the dword order fails them").  The
+rounding in the oracle (the PR page, Testing, makes the same demand of its
+kernel tests: a broken row factor or a wrong dword order must make them
+fail).  The
 committed oracle is never modified; mistakes are planted only on the CPU.
 """
 from __future__ import annotations
