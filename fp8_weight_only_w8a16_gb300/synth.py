@@ -13,6 +13,10 @@ library routines:
   codes with one fp32 factor for each row): scale[n] = amax_n / 448 in fp32 (an all-zero row
   gets scale 1), codes = E4M3(W / scale) clamped to +-448 and rounded through
   ``torch.float8_e4m3fn`` (round to nearest even);
+* block-scaled FP8 planes (the blockscale GEMM's weights; a checkpoint's
+  weight_scale_inv): one fp32 factor per 128 x 128 block, amax_block / 448
+  (an all-zero block gets 1), codes = E4M3(W / factor) clamped to +-448 and
+  rounded through ``torch.float8_e4m3fn``;
 * bf16 planes: fp32 -> bf16 through torch;
 * MXFP4 planes (w4a16; the OCP microscaling format the Model Support Guide's
   FP4 GEMMs use): per row and 32-column block, the shared exponent is
@@ -41,14 +45,15 @@ X_ROWS = 256  # largest token count of the workloads (rows are drawn row-major, 
 class Plane:
     """A source weight plane as a checkpoint would hold it (row-major)."""
 
-    dtype: str            # "e4m3fn", "bf16" or "mxfp4"
+    dtype: str            # "e4m3fn", "e4m3fn_b128", "bf16" or "mxfp4"
     n: int
     k: int                # logical columns
     ldw: int              # row stride in elements (>= k); columns k..ldw-1 are zero
     w: np.ndarray         # [n, ldw] uint8 codes or uint16 bf16 bits; MXFP4: [n, ldw / 2]
                           # bytes of two codes (even column in the low nibble)
     scale: np.ndarray | None  # [n] fp32 row scales (FP8); MXFP4: [n, ceil(k / 32)]
-                              # E8M0 block scales (uint8); None for bf16
+                              # E8M0 block scales (uint8); block-scaled FP8:
+                              # [ceil(n / 128), ceil(k / 128)] fp32; None for bf16
 
 
 def _normal(rng: np.random.Generator, shape, std: float) -> np.ndarray:
@@ -72,6 +77,22 @@ def quantize_ptpc_fp8(w: np.ndarray):
     q = (t / scale[:, None]).clamp_(-E4M3_MAX, E4M3_MAX)
     codes = q.to(torch.float8_e4m3fn).view(torch.uint8)
     return codes.numpy().copy(), scale.numpy().astype(np.float32)
+
+
+def quantize_fp8_b128(w: np.ndarray, block: int = 128):
+    """fp32 [n, k] -> (E4M3fn codes uint8 [n, k], fp32 factors [ceil(n/128), ceil(k/128)])."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    n, k = w.shape
+    nbr, nbc = -(-n // block), -(-k // block)
+    t = torch.zeros((nbr * block, nbc * block), dtype=torch.float32)
+    t[:n, :k] = torch.from_numpy(w)
+    blocks = t.view(nbr, block, nbc, block)
+    amax = blocks.abs().amax(dim=(1, 3))
+    factor = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    q = (blocks / factor[:, None, :, None]).clamp_(-E4M3_MAX, E4M3_MAX)
+    codes = q.reshape(nbr * block, nbc * block)[:n, :k].contiguous()
+    codes = codes.to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes.numpy().copy(), factor.numpy().astype(np.float32)
 
 
 # E2M1 magnitudes by code (sign in bit 3): the values an MXFP4 element takes.
@@ -114,6 +135,11 @@ def weight_plane(rng: np.random.Generator, n: int, k: int, dtype: str = "e4m3fn"
         w = np.zeros((n, ldw), dtype=np.uint8)
         w[:, :k] = codes
         return Plane("e4m3fn", n, k, ldw, w, scale)
+    if dtype == "e4m3fn_b128":
+        codes, factor = quantize_fp8_b128(w32)
+        w = np.zeros((n, ldw), dtype=np.uint8)
+        w[:, :k] = codes
+        return Plane("e4m3fn_b128", n, k, ldw, w, factor)
     if dtype == "bf16":
         w = np.zeros((n, ldw), dtype=np.uint16)
         w[:, :k] = to_bf16_bits(w32)

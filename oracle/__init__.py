@@ -13,12 +13,14 @@ applied to the finished row sum, ahead of the one conversion to bf16.  ``brute.p
 independent numpy fp64 recompute used to pin it.  It also holds the MLP
 activation that follows a merged gate_up projection (ATOM Model Support
 Guide, Model architecture details, Llama MLP): h = silu(g) * u in fp64 with
-one bf16 rounding, and the w4a16 GEMV on MXFP4 weights (E2M1 elements, E8M0
-scales per 32 along K).
+one bf16 rounding, the w4a16 GEMV on MXFP4 weights (E2M1 elements, E8M0
+scales per 32 along K), and the GEMV on block-scaled FP8 planes (one fp32
+factor per 128 x 128 block, applied to each block's finished partial sum).
 
 Every function here is pinned by a ``-m "not gpu"`` test
 (tests/test_oracle_codecs.py, tests/test_oracle_gemv.py,
-tests/test_oracle_silu.py, tests/test_oracle_mxfp4.py).
+tests/test_oracle_silu.py, tests/test_oracle_mxfp4.py,
+tests/test_oracle_b128.py).
 """
 from __future__ import annotations
 
@@ -78,6 +80,12 @@ def _declare(lib):
     lib.orc_gemv_mxfp4_f64.argtypes = [vp, c_i64, c_i64, c_i64, vp, c_i64, vp, c_i64, c_i64,
                                        vp, vp, ctypes.c_int]
     lib.orc_gemv_mxfp4_f64.restype = ctypes.c_int
+    lib.orc_gemv_e4m3_b128.argtypes = [vp, c_i64, c_i64, c_i64, vp, c_i64, vp, c_i64, c_i64,
+                                       vp, c_i64, ctypes.c_int]
+    lib.orc_gemv_e4m3_b128.restype = ctypes.c_int
+    lib.orc_gemv_e4m3_b128_f64.argtypes = [vp, c_i64, c_i64, c_i64, vp, c_i64, vp, c_i64,
+                                           c_i64, vp, vp, ctypes.c_int]
+    lib.orc_gemv_e4m3_b128_f64.restype = ctypes.c_int
     return lib
 
 
@@ -258,6 +266,42 @@ class Oracle:
             raise ValueError("orc_gemv_mxfp4_f64 rejected its arguments")
         return y64, mag
 
+    # ---- block-scaled FP8: one fp32 factor per 128 x 128 block -----------
+    @staticmethod
+    def _b128_args(w, bs, x, k):
+        assert w.dtype == np.uint8 and w.ndim == 2 and w.strides[1] == 1
+        assert bs.dtype == np.float32 and bs.ndim == 2 and bs.strides[1] == 4
+        assert x.dtype == np.uint16 and x.ndim == 2 and x.strides[1] == 2
+        n, ldw = w.shape[0], w.strides[0]
+        k = w.shape[1] if k is None else k
+        assert k <= w.shape[1] and bs.shape[0] == -(-n // 128) and 128 * bs.shape[1] >= k
+        return n, k, ldw, bs.strides[0] // 4, x.shape[0], x.strides[0] // 2
+
+    def gemv_b128(self, w: np.ndarray, bs: np.ndarray, x: np.ndarray, k: int | None = None,
+                  threads: int = 1) -> np.ndarray:
+        """y = bf16(sum over 128-column blocks of bs * (sum_k W x)) in fp32; uint16 [m, n].
+
+        ``w``: [n, >=k] E4M3 codes; ``bs``: [ceil(n/128), >=ceil(k/128)] fp32
+        block factors; ``x``: [m, >=k] bf16 bits.
+        """
+        n, k, ldw, ldb, m, ldx = self._b128_args(w, bs, x, k)
+        y = np.zeros((m, n), dtype=np.uint16)
+        if self.lib.orc_gemv_e4m3_b128(_ptr(w), n, k, ldw, _ptr(bs), ldb, _ptr(x), ldx, m,
+                                       _ptr(y), n, int(threads)) != 0:
+            raise ValueError("orc_gemv_e4m3_b128 rejected its arguments")
+        return y
+
+    def gemv_b128_f64(self, w: np.ndarray, bs: np.ndarray, x: np.ndarray,
+                      k: int | None = None, threads: int = 1):
+        """fp64 recompute: (y64 [m,n], mag64 [m,n] = sum|bs * W * x|)."""
+        n, k, ldw, ldb, m, ldx = self._b128_args(w, bs, x, k)
+        y64 = np.zeros((m, n), dtype=np.float64)
+        mag = np.zeros((m, n), dtype=np.float64)
+        if self.lib.orc_gemv_e4m3_b128_f64(_ptr(w), n, k, ldw, _ptr(bs), ldb, _ptr(x), ldx, m,
+                                           _ptr(y64), _ptr(mag), int(threads)) != 0:
+            raise ValueError("orc_gemv_e4m3_b128_f64 rejected its arguments")
+        return y64, mag
+
     def max_threads(self) -> int:
         return int(self.lib.orc_max_threads())
 
@@ -333,6 +377,14 @@ def gemv_mxfp4(w, bs, x, k=None, threads=1):
 
 def gemv_mxfp4_f64(w, bs, x, k=None, threads=1):
     return _load().gemv_mxfp4_f64(w, bs, x, k, threads)
+
+
+def gemv_b128(w, bs, x, k=None, threads=1):
+    return _load().gemv_b128(w, bs, x, k, threads)
+
+
+def gemv_b128_f64(w, bs, x, k=None, threads=1):
+    return _load().gemv_b128_f64(w, bs, x, k, threads)
 
 
 def silu_mul_f64(g, u):
@@ -443,4 +495,5 @@ __all__ = [
     "max_threads", "bf16_bits_to_f64", "within_tolerance", "same_values", "build_oracle",
     "f64_to_bf16_rne", "silu_mul_f64", "silu_mul", "gate_up_silu_mul", "SILU_LIPSCHITZ",
     "silu_mul_within_tolerance", "e2m1_to_f32", "e8m0_to_f32", "gemv_mxfp4", "gemv_mxfp4_f64",
+    "gemv_b128", "gemv_b128_f64",
 ]

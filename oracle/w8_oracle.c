@@ -30,7 +30,10 @@
  * exact rational results, and power-of-two scale invariance; the SiLU-and-
  * multiply against torch's float64 silu, the odd-part identity
  * silu(v) - silu(-v) = v and its limits, and the one-step fp64 -> bf16
- * rounding against the fp32 rounding and on exact bf16 midpoints.
+ * rounding against the fp32 rounding and on exact bf16 midpoints; the
+ * block-scaled GEMV against an fp64 brute force, one-hot tokens over
+ * distinct block factors, Fraction sums, and its one-column-block case
+ * against the row-scaled GEMV.
  */
 #include <math.h>
 #include <stdint.h>
@@ -395,6 +398,100 @@ int orc_gemv_mxfp4_f64(const uint8_t *w, int64_t n, int64_t k, int64_t ldw_bytes
             double acc = 0.0, mag = 0.0;
             for (int64_t j = 0; j < k; ++j) {
                 double p = (double)mxfp4_value(w, ldw_bytes, bs, ldb, r, j) *
+                           (double)orc_bf16_to_f32(x[i * ldx + j]);
+                acc += p;
+                mag += fabs(p);
+            }
+            y64[i * n + r] = acc;
+            mag64[i * n + r] = mag;
+        }
+    }
+    (void)threads;
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Block-scaled FP8: one fp32 factor per 128 x 128 block of weights    */
+/* ------------------------------------------------------------------ */
+
+/* The GLM-5.2 anatomy page (fused_qkv_a_proj) has that projection run
+ * AITER's preshuffle blockscale GEMM, and the ATOM Model Support Guide
+ * (Weight loading, Loading flow) loads a checkpoint's weight_scale_inv
+ * tensors as the layer's weight scales.  The pages give neither the block
+ * shape nor where the factor enters the sum; the readings taken here:
+ *   - a factor covers 128 rows x 128 columns of W, so bs is
+ *     [ceil(n / 128)][ldb] fp32 with ldb >= ceil(k / 128);
+ *   - as the PR applies its row factor to a finished sum, a block's factor
+ *     multiplies the finished sum of that block's 128 columns: per row and
+ *     token, each block's partial sum p (fp32, ascending k) is multiplied by
+ *     its factor (one fp32 multiply) and added to the row's fp32 total (one
+ *     fp32 add), blocks in ascending order; the total is rounded to bf16
+ *     once.  There is no row factor. */
+#define ORC_BLOCK 128
+
+static int b128_args_ok(const uint8_t *w, int64_t n, int64_t k, int64_t ldw, const float *bs,
+                        int64_t ldb, const uint16_t *x, int64_t ldx, int64_t m)
+{
+    return w && bs && x && n >= 0 && k >= 0 && m >= 0 && ldw >= k && ldx >= k &&
+           ldb * ORC_BLOCK >= k;
+}
+
+int orc_gemv_e4m3_b128(const uint8_t *w, int64_t n, int64_t k, int64_t ldw, const float *bs,
+                       int64_t ldb, const uint16_t *x, int64_t ldx, int64_t m, uint16_t *y,
+                       int64_t ldy, int threads)
+{
+    if (!b128_args_ok(w, n, k, ldw, bs, ldb, x, ldx, m) || !y || ldy < n)
+        return -1;
+#ifdef _OPENMP
+    if (threads < 1)
+        threads = 1;
+#pragma omp parallel for schedule(dynamic, 16) num_threads(threads)
+#endif
+    for (int64_t r = 0; r < n; ++r) {
+        const float *row_factors = bs + (r / ORC_BLOCK) * ldb;
+        for (int64_t i = 0; i < m; ++i) {
+            float acc = 0.0f;
+            for (int64_t j0 = 0; j0 < k; j0 += ORC_BLOCK) {
+                const int64_t j1 = j0 + ORC_BLOCK < k ? j0 + ORC_BLOCK : k;
+                float part = 0.0f;
+                for (int64_t j = j0; j < j1; ++j) {
+                    float wv = orc_e4m3_to_f32(w[r * ldw + j]);
+                    float xv = orc_bf16_to_f32(x[i * ldx + j]);
+                    float p = wv * xv; /* exact */
+                    part = part + p;
+                }
+                float scaled = row_factors[j0 / ORC_BLOCK] * part;
+                acc = acc + scaled;
+            }
+            y[i * ldy + r] = orc_f32_to_bf16_rne(acc);
+        }
+    }
+    (void)threads;
+    return 0;
+}
+
+/* fp64 recompute of the same inputs for the tolerance checks:
+ *   y64[i][r]   = sum_j bs[r/128][j/128] * W[r,j] * x[i,j]      (double)
+ *   mag64[i][r] = sum_j |bs[r/128][j/128] * W[r,j] * x[i,j]|    (double)
+ * Both arrays are [m][n]. */
+int orc_gemv_e4m3_b128_f64(const uint8_t *w, int64_t n, int64_t k, int64_t ldw,
+                           const float *bs, int64_t ldb, const uint16_t *x, int64_t ldx,
+                           int64_t m, double *y64, double *mag64, int threads)
+{
+    if (!b128_args_ok(w, n, k, ldw, bs, ldb, x, ldx, m) || !y64 || !mag64)
+        return -1;
+#ifdef _OPENMP
+    if (threads < 1)
+        threads = 1;
+#pragma omp parallel for schedule(dynamic, 16) num_threads(threads)
+#endif
+    for (int64_t r = 0; r < n; ++r) {
+        const float *row_factors = bs + (r / ORC_BLOCK) * ldb;
+        for (int64_t i = 0; i < m; ++i) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t j = 0; j < k; ++j) {
+                double p = (double)row_factors[j / ORC_BLOCK] *
+                           (double)orc_e4m3_to_f32(w[r * ldw + j]) *
                            (double)orc_bf16_to_f32(x[i * ldx + j]);
                 acc += p;
                 mag += fabs(p);

@@ -18,6 +18,7 @@ import pytest
 import oracle
 from oracle.build import ORACLE_SRC, build_oracle
 
+from . import test_oracle_b128 as b128_pins
 from . import test_oracle_codecs as codecs
 from . import test_oracle_gemv as gemv_pins
 from . import test_oracle_mxfp4 as mxfp4_pins
@@ -70,6 +71,20 @@ MUTATIONS = {
     "nibble_order_swapped": ("uint8_t code = (j & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);",
                              "uint8_t code = (j & 1) ? (uint8_t)(byte & 15) : (uint8_t)(byte >> 4);"),
     "mxfp4_block_of_16": ("orc_e8m0_to_f32(bs[r * ldb + j / 32])", "orc_e8m0_to_f32(bs[r * ldb + j / 16])"),
+    # block-scaled FP8 (indexes kept in bounds so that a mutant reads no stray memory)
+    "b128_factor_dropped": ("float scaled = row_factors[j0 / ORC_BLOCK] * part;",
+                            "float scaled = part;"),
+    "b128_block_index_transposed": (
+        "float scaled = row_factors[j0 / ORC_BLOCK] * part;",
+        "float scaled = bs[((j0 / ORC_BLOCK) % ((n + ORC_BLOCK - 1) / ORC_BLOCK)) * ldb +"
+        " (r / ORC_BLOCK) % ldb] * part;"),
+    "b128_row_blocks_of_64": (
+        "const float *row_factors = bs + (r / ORC_BLOCK) * ldb;\n        for (int64_t i = 0; i < m; ++i) {\n            float acc = 0.0f;",
+        "const float *row_factors = bs + ((r / 64) % ((n + ORC_BLOCK - 1) / ORC_BLOCK)) * ldb;\n        for (int64_t i = 0; i < m; ++i) {\n            float acc = 0.0f;"),
+    "b128_first_block_dropped": ("for (int64_t j0 = 0; j0 < k; j0 += ORC_BLOCK) {",
+                                 "for (int64_t j0 = ORC_BLOCK; j0 < k; j0 += ORC_BLOCK) {"),
+    "b128_total_in_bf16": ("acc = acc + scaled;",
+                           "acc = orc_bf16_to_f32(orc_f32_to_bf16_rne(acc + scaled));"),
 }
 
 # pins rerun against each mutated copy (test functions that take the oracle)
@@ -95,6 +110,10 @@ PINS = [
     lambda o: mxfp4_pins.test_mxfp4_gemv_against_fp64_brute_force(o, 3, 40, 100, 3),
     lambda o: mxfp4_pins.test_mxfp4_one_hot_codes_scales_and_packing(o),
     lambda o: mxfp4_pins.test_mxfp4_exact_sum_inputs_match_rational_result(o),
+    lambda o: b128_pins.test_b128_gemv_against_fp64_brute_force(o, 1, 130, 300, 4),
+    lambda o: b128_pins.test_b128_one_hot_picks_each_blocks_factor(o),
+    lambda o: b128_pins.test_b128_exact_sum_inputs_match_rational_result(o),
+    lambda o: b128_pins.test_b128_one_column_block_is_the_row_scaled_gemv(o),
 ]
 
 
