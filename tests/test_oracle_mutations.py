@@ -34,8 +34,8 @@ MUTATIONS = {
         "orc_f32_to_bf16_rne(acc)) : acc;"),
     "first_term_dropped": ("for (int64_t j = 0; j < k; ++j) {\n                float wv",
                            "for (int64_t j = 1; j < k; ++j) {\n                float wv"),
-    "x_index_reversed": ("float xv = orc_bf16_to_f32(x[i * ldx + j]);",
-                         "float xv = orc_bf16_to_f32(x[i * ldx + (k - 1 - j)]);"),
+    "x_index_reversed": ("float xv = orc_bf16_to_f32(x[i * ldx + j]);\n                float p = wv * xv; /* exact: 4",
+                         "float xv = orc_bf16_to_f32(x[i * ldx + (k - 1 - j)]);\n                float p = wv * xv; /* exact: 4"),
     "sign_ignored": ("        v = ldexpf(1.0f + (float)m / 8.0f, e - 7); /* 1.m * 2^(e-7) */\n"
                      "    return s ? -v : v;",
                      "        v = ldexpf(1.0f + (float)m / 8.0f, e - 7); /* 1.m * 2^(e-7) */\n"
