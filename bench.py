@@ -159,6 +159,19 @@ class ClockSampler:
 # the GPU arm
 # ---------------------------------------------------------------------------
 
+def source_plane(w8, proj, w_d, s_d):
+    """The w8.Plane of a workload's source tensors and the gemv call it takes."""
+    if proj.dtype == "mxfp4":
+        return w8.Plane.mxfp4(w_d, s_d, k=proj.k), w8.mxfp4_gemv
+    if proj.dtype == "e4m3fn_b128":
+        return w8.Plane.e4m3_b128(w_d, s_d, k=proj.k), w8.w8_gemv
+    silu = proj.act == "silu_mul"
+    fp8 = proj.dtype == "e4m3fn"
+    src = w8.Plane.from_tensor(w_d, s_d, k=proj.k, dtype=w8.DT_E4M3FN if fp8 else w8.DT_BF16,
+                               layout=w8.SRC_GATE_UP if silu else w8.SRC_ROW_MAJOR)
+    return src, (w8.w8_gemv_silu_mul if silu else w8.w8_gemv if fp8 else w8.bf16_gemv)
+
+
 class GemvBench:
     """Bound copies of one workload plane, activations, outputs, workspace."""
 
@@ -166,7 +179,6 @@ class GemvBench:
         self.proj, self.ms, self.w8, self.torch, self.device = proj, tuple(ms), w8, torch, device
         plane, x_all = synth.workload(proj.n, proj.k, proj.dtype, seed=0, ldw=proj.ldw)
         self.plane = plane
-        self.fp8 = proj.dtype == "e4m3fn"
         props = torch.cuda.get_device_properties(device)
         l2 = getattr(props, "L2_cache_size", 0) or getattr(props, "l2_cache_size", 0) or (128 << 20)
         self.l2 = l2
@@ -179,14 +191,7 @@ class GemvBench:
         self.copies = copies
         w_d = torch.from_numpy(plane.w).to(device)
         s_d = torch.from_numpy(plane.scale).to(device) if plane.scale is not None else None
-        dt = w8.DT_E4M3FN if self.fp8 else w8.DT_BF16
-        silu = proj.act == "silu_mul"
-        mx = proj.dtype == "mxfp4"
-        if mx:
-            src = w8.Plane.mxfp4(w_d, s_d, k=proj.k)
-        else:
-            src = w8.Plane.from_tensor(w_d, s_d, k=proj.k, dtype=dt,
-                                       layout=w8.SRC_GATE_UP if silu else w8.SRC_ROW_MAJOR)
+        src, self.fn = source_plane(w8, proj, w_d, s_d)
         self.build = w8.bind([src] * copies)
         torch.cuda.synchronize()
         del w_d, s_d, src
@@ -197,8 +202,6 @@ class GemvBench:
         self.y = {m: torch.zeros((m, proj.out_n), dtype=torch.int16, device=device)
                   for m in self.ms}
         self.ws = self.build.new_workspace()
-        self.fn = (w8.w8_gemv_silu_mul if silu else w8.mxfp4_gemv if mx
-                   else w8.w8_gemv if self.fp8 else w8.bf16_gemv)
 
     def step_bytes(self):
         return sum(self.proj.algorithmic_bytes(m) for m in self.ms)
@@ -583,19 +586,11 @@ def run_one(args):
     plane, x_all = synth.workload(proj.n, proj.k, proj.dtype, seed=0, ldw=proj.ldw)
     w_d = torch.from_numpy(plane.w).to(device)
     s_d = torch.from_numpy(plane.scale).to(device) if plane.scale is not None else None
-    dt = w8.DT_E4M3FN if proj.dtype == "e4m3fn" else w8.DT_BF16
-    silu = proj.act == "silu_mul"
-    mx = proj.dtype == "mxfp4"
-    if mx:
-        b = w8.bind([w8.Plane.mxfp4(w_d, s_d, k=proj.k)])
-    else:
-        b = w8.bind([w8.Plane.from_tensor(w_d, s_d, k=proj.k, dtype=dt,
-                                          layout=w8.SRC_GATE_UP if silu else w8.SRC_ROW_MAJOR)])
+    src, fn = source_plane(w8, proj, w_d, s_d)
+    b = w8.bind([src])
     ws = b.new_workspace()
     x = torch.from_numpy(np.ascontiguousarray(x_all[:m]).view(np.int16)).to(device)
     y = torch.zeros((m, proj.out_n), dtype=torch.int16, device=device)
-    fn = (w8.w8_gemv_silu_mul if silu else w8.mxfp4_gemv if mx
-          else w8.w8_gemv if dt == w8.DT_E4M3FN else w8.bf16_gemv)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # 2 x L2
     for _ in range(args.calls):
         flush.zero_()

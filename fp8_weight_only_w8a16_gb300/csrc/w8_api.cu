@@ -35,25 +35,40 @@ int64_t row_bytes(int32_t dtype, int64_t ldw)
 // The kernels' dtype of a plane dtype.
 int kernel_dt(int32_t dtype)
 {
-    return dtype == W8_DT_E4M3FN ? w8::kDtFp8 : dtype == W8_DT_MXFP4 ? w8::kDtFp4 : w8::kDtBf16;
+    return dtype == W8_DT_E4M3FN        ? w8::kDtFp8
+           : dtype == W8_DT_MXFP4       ? w8::kDtFp4
+           : dtype == W8_DT_E4M3FN_B128 ? w8::kDtFp8B
+                                        : w8::kDtBf16;
 }
 
-// The launch plan of a plane's dtype: MXFP4 planes run the register ring only.
+// Planes whose factors vary along K (MXFP4, block-scaled FP8) run the
+// register ring only.
+bool ring_only(int32_t dtype) { return dtype == W8_DT_MXFP4 || dtype == W8_DT_E4M3FN_B128; }
+
+// The launch plan of a plane's dtype.
 w8::Plan plan_for(int32_t dtype, int64_t n, int64_t k, int m, int sms)
 {
-    return dtype == W8_DT_MXFP4 ? w8::make_ring_plan(n, k, m, sms) : w8::make_plan(n, k, m, sms);
+    return ring_only(dtype) ? w8::make_ring_plan(n, k, m, sms, dtype == W8_DT_E4M3FN_B128)
+                            : w8::make_plan(n, k, m, sms);
 }
 
-int max_m(int32_t dtype) { return dtype == W8_DT_MXFP4 ? w8::kMaxRingM : w8::kMaxM; }
+int max_m(int32_t dtype) { return ring_only(dtype) ? w8::kMaxRingM : w8::kMaxM; }
+
+// FP8 planes with row scales (E4M3FN) or block factors (E4M3FN_B128): both
+// carry fp32 factors in `scale` and run through w8_gemv.
+bool fp8_codes(int32_t dtype) { return dtype == W8_DT_E4M3FN || dtype == W8_DT_E4M3FN_B128; }
 
 w8_status check_plane(const w8_plane_desc &d)
 {
     if (!d.w)
         return W8_ERR_NULL;
-    if (d.dtype != W8_DT_E4M3FN && d.dtype != W8_DT_BF16 && d.dtype != W8_DT_MXFP4)
+    if (d.dtype != W8_DT_E4M3FN && d.dtype != W8_DT_BF16 && d.dtype != W8_DT_MXFP4 &&
+        d.dtype != W8_DT_E4M3FN_B128)
         return W8_ERR_DTYPE;
     if (d.layout != W8_SRC_ROW_MAJOR && d.layout != W8_SRC_GATE_UP)
         return W8_ERR_LAYOUT;
+    if (d.layout == W8_SRC_GATE_UP && d.dtype == W8_DT_E4M3FN_B128)
+        return W8_ERR_LAYOUT; // a tile would hold gate and up rows of two row blocks
     if (d.bias)
         return W8_ERR_BIAS;
     if (d.n < 1 || d.k < 1 || d.n > kMaxDim || d.k > kMaxDim || d.ldw < d.k ||
@@ -61,9 +76,11 @@ w8_status check_plane(const w8_plane_desc &d)
         return W8_ERR_SHAPE;
     if (d.layout == W8_SRC_GATE_UP && d.n % (2 * 8) != 0)
         return W8_ERR_SHAPE; // I = n / 2 gate rows, a multiple of 8
-    if (d.dtype == W8_DT_E4M3FN && !d.scale)
+    if (fp8_codes(d.dtype) && !d.scale)
         return W8_ERR_SCALE;
-    if (d.dtype != W8_DT_E4M3FN && d.scale)
+    if (!fp8_codes(d.dtype) && d.scale)
+        return W8_ERR_SCALE;
+    if (d.dtype == W8_DT_E4M3FN_B128 && d.ldb < w8::ceil_div(d.k, w8::kBlockB))
         return W8_ERR_SCALE;
     if (d.dtype == W8_DT_MXFP4 && (!d.block_scale || d.ldb < w8::ceil_div(d.k, 32)))
         return W8_ERR_SCALE;
@@ -84,9 +101,18 @@ size_t plane_packed_bytes(int32_t dtype, int64_t n, int64_t k)
 
 size_t plane_scale_bytes(int32_t dtype, int64_t n)
 {
-    if (dtype != W8_DT_E4M3FN)
+    if (!fp8_codes(dtype))
         return 0;
     return size_t(w8::ceil_div(n, w8::kTileN)) * w8::kTileN * sizeof(float);
+}
+
+// The build's copy of a block-scaled plane's factors: [ceil(n/128)][ceil(k/128)].
+size_t plane_factor_bytes(int32_t dtype, int64_t n, int64_t k)
+{
+    if (dtype != W8_DT_E4M3FN_B128)
+        return 0;
+    return size_t(w8::ceil_div(n, w8::kBlockB)) * size_t(w8::ceil_div(k, w8::kBlockB)) *
+           sizeof(float);
 }
 
 // want_dtype 0: either dtype (SiLU-and-multiply serves both).
@@ -99,7 +125,8 @@ w8_status gemv_common(const w8_build *b, int plane, int32_t want_dtype, bool sil
     if (plane < 0 || plane >= int(b->planes.size()))
         return W8_ERR_PLANE;
     const w8_plane_info &p = b->planes[size_t(plane)];
-    if (want_dtype != 0 && p.dtype != want_dtype)
+    if (want_dtype != 0 && p.dtype != want_dtype &&
+        !(want_dtype == W8_DT_E4M3FN && p.dtype == W8_DT_E4M3FN_B128))
         return W8_ERR_DTYPE;
     if (silu && p.layout != W8_LAYOUT_MMA_16x32_GATE_UP)
         return W8_ERR_LAYOUT;
@@ -134,6 +161,8 @@ w8_status gemv_common(const w8_build *b, int plane, int32_t want_dtype, bool sil
     a.rt = int(plan.rt);
     a.splits = plan.splits;
     a.wk = plan.wk;
+    a.bfac = p.block_factors;
+    a.nbf = int(w8::ceil_div(p.k, w8::kBlockB));
     w8::set_output_map(a, p, silu);
     if (plan.ws_bytes > 0) { // register-ring split-K plans (tensor-memory plans need none)
         if (!ws)
@@ -160,18 +189,20 @@ const char *w8_status_str(w8_status s)
     switch (s) {
     case W8_OK: return "ok";
     case W8_ERR_NULL: return "a required pointer is NULL";
-    case W8_ERR_DTYPE: return "weight dtype the kernels cannot read (only E4M3FN, BF16 and "
-                              "MXFP4), or a gemv call of another dtype";
+    case W8_ERR_DTYPE: return "weight dtype the kernels cannot read (only E4M3FN, E4M3FN_B128, "
+                              "BF16 and MXFP4), or a gemv call of another dtype";
     case W8_ERR_UNPADDED: return "unpadded plane: base not 16-byte aligned or row stride not a "
                                  "multiple of 16 bytes";
     case W8_ERR_BIAS: return "a bias was given; the GEMV has none";
     case W8_ERR_MIXED: return "bf16 and FP8 planes mixed in one build";
     case W8_ERR_SHAPE: return "bad shape: N, K >= 1, ldw >= K, 0 <= m <= 256, ldx >= K, ldy >= N "
                               "(N/2 for SiLU-and-multiply); a gate_up plane needs N % 16 == 0";
-    case W8_ERR_SCALE: return "FP8 planes need fp32 row scales, MXFP4 planes E8M0 block scales "
+    case W8_ERR_SCALE: return "FP8 planes need fp32 row scales, block-scaled FP8 planes fp32 block "
+                              "factors (ldb >= ceil(K/128)), MXFP4 planes E8M0 block scales "
                               "(ldb >= ceil(K/32)); no other plane takes either";
-    case W8_ERR_LAYOUT: return "unknown source layout (row-major or gate_up), or SiLU-and-multiply "
-                               "on a plane not bound as gate_up";
+    case W8_ERR_LAYOUT: return "unknown source layout (row-major or gate_up), a block-scaled plane "
+                               "bound as gate_up, or SiLU-and-multiply on a plane not bound as "
+                               "gate_up";
     case W8_ERR_CAPACITY: return "packed buffer or workspace too small";
     case W8_ERR_ALIGN: return "misaligned buffer (packed/workspace: 256 B; x: 16 B with ldx % 8 == 0; y: 2 B)";
     case W8_ERR_PLANE: return "plane index outside the build";
@@ -219,6 +250,7 @@ w8_status w8_packed_bytes(const w8_plane_desc *d, int n_planes, size_t *bytes)
     size_t total = 0;
     for (int i = 0; i < n_planes; ++i) {
         total += w8::align256(plane_scale_bytes(d[i].dtype, d[i].n));
+        total += w8::align256(plane_factor_bytes(d[i].dtype, d[i].n, d[i].k));
         total += w8::align256(plane_packed_bytes(d[i].dtype, d[i].n, d[i].k));
     }
     *bytes = total;
@@ -273,6 +305,13 @@ w8_status w8_bind(const w8_plane_desc *d, int n_planes, void *dst, size_t dst_by
             cursor += w8::align256(sb);
         }
         info.scale = scale_copy;
+        float *factor_copy = nullptr;
+        const size_t fb = plane_factor_bytes(pd.dtype, pd.n, pd.k);
+        if (fb) {
+            factor_copy = reinterpret_cast<float *>(cursor);
+            cursor += w8::align256(fb);
+        }
+        info.block_factors = factor_copy;
         info.packed = cursor;
         info.packed_bytes = plane_packed_bytes(pd.dtype, pd.n, pd.k);
         cursor += w8::align256(info.packed_bytes);
@@ -287,8 +326,11 @@ w8_status w8_bind(const w8_plane_desc *d, int n_planes, void *dst, size_t dst_by
         ra.kb = info.k_blocks;
         ra.rt = info.row_tiles;
         ra.dst = static_cast<uint8_t *>(const_cast<void *>(info.packed));
-        ra.scale_src = pd.scale;
+        const bool b128 = pd.dtype == W8_DT_E4M3FN_B128;
+        ra.scale_src = b128 ? nullptr : pd.scale;
         ra.scale_dst = scale_copy;
+        ra.bfac_src = b128 ? pd.scale : nullptr;
+        ra.bfac_dst = factor_copy;
         ra.half = gated ? pd.n / 2 : 0;
         if (w8::launch_repack(kernel_dt(pd.dtype), ra, reinterpret_cast<cudaStream_t>(s)) !=
             cudaSuccess) {
@@ -423,7 +465,7 @@ int64_t w8_packed_offset(int dtype, int64_t k_blocks, int64_t row, int64_t col)
 {
     if (k_blocks < 1 || row < 0 || col < 0 || col >= k_blocks * w8::kTileK)
         return -1;
-    if (dtype == W8_DT_E4M3FN)
+    if (dtype == W8_DT_E4M3FN || dtype == W8_DT_E4M3FN_B128)
         return w8::packed_offset_fp8(k_blocks, row, col);
     if (dtype == W8_DT_BF16)
         return w8::packed_offset_bf16(k_blocks, row, col);

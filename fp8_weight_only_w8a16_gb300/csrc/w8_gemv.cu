@@ -10,6 +10,11 @@
 // planes skip the widening and the scale; MXFP4 planes (the ATOM Model
 // Support Guide's FP4 GEMMs with 16-bit activations) widen each code times
 // its E8M0 block scale exactly to bf16 instead, with no row scale.
+// Block-scaled FP8 planes (one fp32 factor per 128 x 128 block, the
+// blockscale GEMM's weights) widen like FP8 and sum each 128-column block
+// apart: at the block's end its factor multiplies the block's sum into the
+// row's accumulator (one fma), and the row scale is 1 (NaN for a row holding
+// a NaN code).
 //
 // Why tensor cores for a GEMV: at M = 8 every weight byte costs 8 multiply-adds;
 // at the HBM rate that is ~5e13 FMA/s, more than the fp32 pipes sustain once
@@ -76,6 +81,41 @@ __device__ __forceinline__ uint4 load_x_tail(const uint16_t *p, bool ok, int64_t
                       h[4] | (uint32_t(h[5]) << 16), h[6] | (uint32_t(h[7]) << 16));
 }
 
+// Block-scaled planes: lane l of the warp holds in fac[r] the factor of
+// column block fbase + l of tile r's row block.  Before a stretch of K blocks
+// whose column blocks end at hi, move the window to start at lo if hi lies
+// past it (warp-uniform; at most once per 32 column blocks).
+template <int R>
+__device__ __forceinline__ void factor_window(float (&fac)[R], const float *const (&fac_row)[R],
+                                              int &fbase, int lo, int hi, int lane, int nbf)
+{
+    if (hi - fbase >= 32) {
+        fbase = lo;
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            fac[r] = fbase + lane < nbf ? __ldg(fac_row[r] + fbase + lane) : 0.0f;
+    }
+}
+
+// Block-scaled planes: close column block cb (inside the window) --
+// acc += f * part, part = 0.  Warp-uniform: every lane calls it for the same cb.
+template <int NT, int R>
+__device__ __forceinline__ void close_block(float (&acc)[R][NT][4], float (&part)[R][NT][4],
+                                            const float (&fac)[R], int fbase, int cb)
+{
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const float f = __shfl_sync(0xffffffffu, fac[r], cb - fbase);
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                acc[r][j][e] = fmaf(f, part[r][j][e], acc[r][j][e]);
+                part[r][j][e] = 0.0f;
+            }
+    }
+}
+
 // One K block: widen the R weight fragments and run the two tensor-core steps
 // of every (row tile, 8 tokens) into its accumulator.
 template <int kDt, int NT, int R>
@@ -101,9 +141,13 @@ template <int kDt, int NT, int R, int DW, int DX, int kMinBlocks>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvArgs a)
 {
     static_assert(DW % DX == 0, "the activation ring depth divides the weight ring depth");
+    static_assert(kBlockB == 4 * kTileK, "a block factor covers four K blocks");
+    static_assert(kDt != kDtFp8B || DW % 4 == 0, "block-scaled rings hold whole column blocks");
     extern __shared__ __align__(16) float red[]; // [warp][R][NT][4][32]
-    constexpr bool kFp8 = kDt == kDtFp8; // row scales in the epilogue
-    constexpr int kRun = kDt == kDtFp8 ? kRunFp8 : kDt == kDtFp4 ? kRunFp4 : kRunBf16;
+    constexpr bool kB128 = kDt == kDtFp8B;    // block factors inside the K loop
+    constexpr int kW = kB128 ? kDtFp8 : kDt;   // the format of the weight codes
+    constexpr bool kFp8 = kW == kDtFp8;        // row scales in the epilogue
+    constexpr int kRun = kW == kDtFp8 ? kRunFp8 : kW == kDtFp4 ? kRunFp4 : kRunBf16;
     constexpr int kLaneBytes = kDt == kDtFp4 ? 8 : 16; // a lane's part of a run (bf16: twice)
 
     const int warp = threadIdx.x >> 5;
@@ -117,10 +161,19 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
 
     const int rg = blockIdx.x / a.splits;
     const int sp = blockIdx.x - rg * a.splits;
-    const int cb0 = int((int64_t(sp) * a.kb) / a.splits);   // CTA's K blocks
-    const int cnb = int((int64_t(sp + 1) * a.kb) / a.splits) - cb0;
-    const int kb0 = cb0 + (kp * cnb) / wk;                  // warp's K blocks
-    const int nkb = cb0 + ((kp + 1) * cnb) / wk - kb0;
+    // The CTA's and the warp's K blocks, split in units of kU blocks: single
+    // blocks, or whole column blocks on block-scaled planes, so that every
+    // warp's part starts on a column block and, with a ring of whole column
+    // blocks, each column block ends at a fixed ring slot.
+    constexpr int kU = kB128 ? kBlockB / kTileK : 1;
+    const int nu = (a.kb + kU - 1) / kU;
+    const int cu0 = int((int64_t(sp) * nu) / a.splits);
+    const int cnu = int((int64_t(sp + 1) * nu) / a.splits) - cu0;
+    const int u0 = cu0 + (kp * cnu) / wk;
+    const int u1 = cu0 + ((kp + 1) * cnu) / wk;
+    const int kb0 = u0 * kU;
+    const int kb1 = u1 * kU < a.kb ? u1 * kU : a.kb;
+    const int nkb = kb1 > kb0 ? kb1 - kb0 : 0;
 
     // ---- the warp's row tiles and activation rows ----------------------------
     // Blocks [0, nmain) of the warp's K part lie wholly inside K; when K is not
@@ -166,16 +219,29 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
             for (int r = 0; r < R; ++r)
                 prefetch_l2(wptr[r] + DW * kRun, uint32_t(hi - DW) * kRun);
     }
-    WFrag<kDt> wring[DW][R];
+    WFrag<kW> wring[DW][R];
     uint4 xring[DX][NT];
 #pragma unroll
     for (int i = 0; i < DW; ++i)
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            zero_w<kDt>(wring[i][r]);
+            zero_w<kW>(wring[i][r]);
             if (i < nmain)
-                load_w<kDt>(wring[i][r], wptr[r] + i * kRun, soff);
+                load_w<kW>(wring[i][r], wptr[r] + i * kRun, soff);
         }
+    // block-scaled planes: the first 32 factors of the warp's column blocks
+    // (bind-time data too), one per lane, for each of its row tiles
+    float fac[R];
+    const float *fac_row[R];
+    int fbase = kb0 >> 2;
+    if constexpr (kB128) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int tile = rg * (wt * R) + r * wt + tg;
+            fac_row[r] = a.bfac + int64_t(tile < a.rt ? tile >> 3 : 0) * a.nbf;
+            fac[r] = fbase + lane < a.nbf ? __ldg(fac_row[r] + fbase + lane) : 0.0f;
+        }
+    }
     // the CTA's row scales (bind-time data too) into shared memory
     __shared__ float s_scale[kWarps * 2 * kTileN];
     const int row0 = rg * wt * R * kTileN;
@@ -197,13 +263,16 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
 
     // ---- stream the K part ------------------------------------------------------
     float acc[R][NT][4];
+    float part[R][NT][4]; // block-scaled planes: the open column block's sum
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
         for (int j = 0; j < NT; ++j)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
+            for (int e = 0; e < 4; ++e) {
                 acc[r][j][e] = 0.0f;
+                part[r][j][e] = 0.0f;
+            }
 
     // Blocks in ascending order.  Block b sits in weight slot b % DW and
     // activation slot b % DX; each slot is computed, then refilled (a
@@ -211,6 +280,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
     // further on.
     int b = 0;
     for (; b + DW <= nmain; b += DW) {
+        if constexpr (kB128)
+            factor_window<R>(fac, fac_row, fbase, (kb0 + b) >> 2, (kb0 + b + DW - 1) >> 2, lane,
+                             a.nbf);
         if (kPf > DW && lane == 0 && b + kPf < nmain) {
             const int hi = b + kPf + DW < nmain ? b + kPf + DW : nmain;
 #pragma unroll
@@ -219,11 +291,17 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
         }
 #pragma unroll
         for (int i = 0; i < DW; ++i) {
-            block_step<kDt, NT, R>(acc, wring[i], xring[i % DX]);
+            if constexpr (kB128) {
+                block_step<kW, NT, R>(part, wring[i], xring[i % DX]);
+                if ((i & 3) == 3) // kb0 and b are whole column blocks
+                    close_block<NT, R>(acc, part, fac, fbase, (kb0 + b + i) >> 2);
+            } else {
+                block_step<kW, NT, R>(acc, wring[i], xring[i % DX]);
+            }
             const uint32_t more_w = (b + DW + i) < nmain;
 #pragma unroll
             for (int r = 0; r < R; ++r)
-                load_w_pred<kDt>(wring[i][r], wptr[r] + (b + DW + i) * kRun, soff, more_w);
+                load_w_pred<kW>(wring[i][r], wptr[r] + (b + DW + i) * kRun, soff, more_w);
             const uint32_t more_x = (b + DX + i) < nmain;
 #pragma unroll
             for (int j = 0; j < NT; ++j)
@@ -232,10 +310,18 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
         }
     }
     // the last partial group (fewer than DW blocks, all weights in flight)
+    if constexpr (kB128)
+        factor_window<R>(fac, fac_row, fbase, (kb0 + b) >> 2, (kb0 + b + DW - 1) >> 2, lane, a.nbf);
 #pragma unroll
     for (int i = 0; i < DW - 1; ++i) {
         if (b + i < nmain) {
-            block_step<kDt, NT, R>(acc, wring[i], xring[i % DX]);
+            if constexpr (kB128) {
+                block_step<kW, NT, R>(part, wring[i], xring[i % DX]);
+                if ((i & 3) == 3) // kb0 and b are whole column blocks
+                    close_block<NT, R>(acc, part, fac, fbase, (kb0 + b + i) >> 2);
+            } else {
+                block_step<kW, NT, R>(acc, wring[i], xring[i % DX]);
+            }
             const uint32_t more_x = (b + DX + i) < nmain;
 #pragma unroll
             for (int j = 0; j < NT; ++j)
@@ -246,16 +332,27 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
     if (has_tail) {
         // the partial last block: zero activations past K (its weights past K
         // are zero-filled by the repack)
-        WFrag<kDt> tw[R];
+        WFrag<kW> tw[R];
         uint4 tx[NT];
 #pragma unroll
         for (int r = 0; r < R; ++r)
-            load_w<kDt>(tw[r], wptr[r] + nmain * kRun, soff);
+            load_w<kW>(tw[r], wptr[r] + nmain * kRun, soff);
         const int64_t col = int64_t(kb0 + nmain) * kTileK + 8 * t;
 #pragma unroll
         for (int j = 0; j < NT; ++j)
             tx[j] = load_x_tail(xptr[j] + nmain * kTileK, tok_ok[j] != 0, col, a.k);
-        block_step<kDt, NT, R>(acc, tw, tx);
+        if constexpr (kB128)
+            block_step<kW, NT, R>(part, tw, tx);
+        else
+            block_step<kW, NT, R>(acc, tw, tx);
+    }
+    // block-scaled planes: close the last column block unless the loop did
+    if constexpr (kB128) {
+        if (nkb > 0 && (has_tail || ((kb0 + nkb - 1) & 3) != 3)) {
+            const int cb = (kb0 + nkb - 1) >> 2;
+            factor_window<R>(fac, fac_row, fbase, cb, cb, lane, a.nbf);
+            close_block<NT, R>(acc, part, fac, fbase, cb);
+        }
     }
 
     // ---- K parts meet in shared memory ---------------------------------------
@@ -373,8 +470,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
 template <int kDt, int NT, int R, int OCC>
 void *inst()
 {
-    return reinterpret_cast<void *>(&gemv_kernel<kDt, NT, R, depth_w_dt(NT, R, kDt, OCC),
-                                                 depth_x_dt(NT, R, kDt, OCC), OCC>);
+    constexpr int dw = depth_w_dt(NT, R, kDt, OCC), dx = depth_x_dt(NT, R, kDt, OCC);
+    if constexpr (dw == 0) // a block-scaled instance that does not exist
+        return nullptr;
+    else
+        return reinterpret_cast<void *>(&gemv_kernel<kDt, NT, R, dw, dx, OCC>);
 }
 
 template <int kDt, int I>
@@ -402,9 +502,10 @@ void *pick(int nt, int r, int occ)
 
 void *pick_dt(int dt, int nt, int r, int occ)
 {
-    return dt == kDtFp8 ? pick<kDtFp8>(nt, r, occ)
-           : dt == kDtFp4 ? pick<kDtFp4>(nt, r, occ)
-                          : pick<kDtBf16>(nt, r, occ);
+    return dt == kDtFp8    ? pick<kDtFp8>(nt, r, occ)
+           : dt == kDtFp4  ? pick<kDtFp4>(nt, r, occ)
+           : dt == kDtFp8B ? pick<kDtFp8B>(nt, r, occ)
+                           : pick<kDtBf16>(nt, r, occ);
 }
 
 } // namespace
@@ -413,8 +514,10 @@ cudaError_t prepare_gemv_kernels()
 {
     // the K-part reduction buffer: 8 warps x R x NT x 128 floats, at most 64 KB
     for (int i = 0; i < kNumInst; ++i) {
-        for (int dt : {kDtBf16, kDtFp8, kDtFp4}) {
+        for (int dt : {kDtBf16, kDtFp8, kDtFp4, kDtFp8B}) {
             void *fn = pick_dt(dt, kInst[i].nt, kInst[i].r, kInst[i].occ);
+            if (!fn)
+                continue;
             cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  64 * 1024);
             if (e != cudaSuccess)
@@ -427,7 +530,8 @@ cudaError_t prepare_gemv_kernels()
 cudaError_t launch_gemv(int dt, const Plan &plan, const GemvArgs &a, cudaStream_t s)
 {
     if (plan.tc)
-        return dt == kDtFp4 ? cudaErrorInvalidValue : launch_tc(dt == kDtFp8, plan, a, s);
+        return dt == kDtFp4 || dt == kDtFp8B ? cudaErrorInvalidValue
+                                             : launch_tc(dt == kDtFp8, plan, a, s);
     void *fn = pick_dt(dt, plan.nt, plan.r, plan.occ);
     if (!fn)
         return cudaErrorInvalidValue;

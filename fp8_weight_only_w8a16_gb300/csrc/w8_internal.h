@@ -45,6 +45,8 @@ struct GemvArgs {
     int half;               // gate_up planes: I = n / 2
     int xg;                 // tc kernel: row blocks of a cluster that share the
                             // activation tiles (TMA multicast); set by launch_tc
+    const float *bfac;      // block-scaled FP8: the build's factors [ceil(n/128)][nbf]
+    int nbf;                // block-scaled FP8: column blocks, ceil(k / 128)
 };
 
 // The output mapping of a plane: gate_up planes (bound with W8_SRC_GATE_UP)
@@ -57,8 +59,8 @@ inline void set_output_map(GemvArgs &a, const w8_plane_info &p, bool silu)
 }
 
 // One launch of the GEMV kernel chosen by the plan; dt is the weight dtype
-// (kDtBf16, kDtFp8 or kDtFp4 of w8_device.cuh; MXFP4 plans are register-ring
-// plans).
+// (kDtBf16, kDtFp8, kDtFp4 or kDtFp8B of w8_layout.h; MXFP4 and block-scaled
+// plans are register-ring plans).
 cudaError_t launch_gemv(int dt, const Plan &plan, const GemvArgs &a, cudaStream_t s);
 
 // Raise the dynamic shared-memory limit of every GEMV kernel instance on the
@@ -77,16 +79,20 @@ struct RepackArgs {
     int64_t n, k;
     int64_t kb, rt;
     uint8_t *dst;           // packed weights (device)
-    const float *scale_src; // FP8: caller's row scales (device)
-    float *scale_dst;       // FP8: the build's copy, rt*16 entries (device)
+    const float *scale_src; // FP8: caller's row scales (device); NULL for block-scaled
+                            // FP8, whose row scales are 1
+    float *scale_dst;       // FP8 and block-scaled FP8: the build's copy, rt*16 entries
     int64_t half;           // 0, or I for a gate_up plane (n = 2I, I % 8 == 0):
                             // packed row 16t+i reads source row 8t+i (i < 8)
                             // or I + 8t + i - 8 (i >= 8)
     const uint8_t *bscale_src; // MXFP4: caller's E8M0 block scales [n][ldb] (device)
-    int64_t ldb;
+    int64_t ldb;            // row stride of the block scales (MXFP4: bytes; block-scaled
+                            // FP8: floats)
+    const float *bfac_src;  // block-scaled FP8: caller's factors [ceil(n/128)][ldb] (device)
+    float *bfac_dst;        // block-scaled FP8: the build's copy [ceil(n/128)][ceil(k/128)]
 };
 
-// The repack of one plane (dt: kDtBf16, kDtFp8 or kDtFp4).
+// The repack of one plane (dt: kDtBf16, kDtFp8, kDtFp4 or kDtFp8B).
 cudaError_t launch_repack(int dt, const RepackArgs &a, cudaStream_t s);
 
 } // namespace w8

@@ -41,9 +41,12 @@ constexpr int kRunFp8 = 512;      // bytes of one (tile, block) run, FP8
 constexpr int kRunBf16 = 1024;    // bytes of one (tile, block) run, bf16
 constexpr int kWarps = 8;         // warps per CTA of the GEMV kernel
 constexpr int kThreads = kWarps * 32;
-// Weight dtypes of the kernels (the register ring reads all three; the
-// tensor-memory kernel bf16 and FP8).
-constexpr int kDtBf16 = 0, kDtFp8 = 1, kDtFp4 = 2;
+// Weight dtypes of the kernels (the register ring reads all four; the
+// tensor-memory kernel bf16 and FP8).  kDtFp8B is an FP8 plane with one fp32
+// factor per kBlockB x kBlockB block instead of row scales: the FP8 codes and
+// packed layout, each block's partial sum multiplied by its factor.
+constexpr int kDtBf16 = 0, kDtFp8 = 1, kDtFp4 = 2, kDtFp8B = 3;
+constexpr int kBlockB = 128;      // rows and columns one block factor covers
 constexpr int kMaxM = 256;        // tokens per call (decode steps, draft rows, prefill chunks)
 constexpr int kMaxRingM = 64;     // the register-ring kernel's limit (8 token groups of 8)
 
@@ -166,16 +169,21 @@ W8_HD int nt_for_m(int m) { return m <= 8 ? 1 : m <= 16 ? 2 : m <= 32 ? 4 : 8; }
 // (measured: depths 16/8 -> 12/6 took fused_qkv_a_proj from 5.8 to 5.4 us).
 struct Inst {
     int nt, r, occ;
-    int dw_fp8, dx_fp8, dw_bf16, dx_bf16, dw_fp4, dx_fp4;
+    int dw_fp8, dx_fp8, dw_bf16, dx_bf16, dw_fp4, dx_fp4, dw_b128, dx_b128;
 };
 // (MXFP4 fragments hold 12 bytes a block against FP8's 16 but widen through
-// more temporaries: the FP8 depths, except where they spill.)
+// more temporaries: the FP8 depths, except where they spill.  Block-scaled
+// FP8 keeps a second set of accumulators, the open column block's sum, and
+// its weight ring holds whole column blocks (a multiple of 4 K blocks): the
+// nearest such depth the registers hold, or 0 -- no such instance -- where
+// none does.)
 constexpr int kNumInst = 10;
 constexpr Inst kInst[kNumInst] = {
-    {1, 1, 2, 12, 6, 8, 4, 12, 6}, {1, 2, 2, 6, 6, 4, 2, 6, 6}, {1, 1, 3, 6, 6, 4, 2, 6, 6},
-    {1, 2, 3, 4, 4, 2, 2, 4, 4},   {2, 1, 2, 10, 5, 6, 3, 8, 4}, {2, 2, 2, 6, 3, 2, 2, 6, 3},
-    {4, 1, 2, 6, 2, 4, 2, 6, 2},   {4, 2, 1, 8, 4, 4, 2, 8, 4},
-    {8, 1, 1, 6, 2, 4, 2, 6, 2},   {8, 2, 1, 6, 2, 4, 2, 6, 2},
+    {1, 1, 2, 12, 6, 8, 4, 12, 6, 12, 6}, {1, 2, 2, 6, 6, 4, 2, 6, 6, 4, 4},
+    {1, 1, 3, 6, 6, 4, 2, 6, 6, 8, 2},    {1, 2, 3, 4, 4, 2, 2, 4, 4, 0, 0},
+    {2, 1, 2, 10, 5, 6, 3, 8, 4, 8, 4},   {2, 2, 2, 6, 3, 2, 2, 6, 3, 4, 2},
+    {4, 1, 2, 6, 2, 4, 2, 6, 2, 4, 1},    {4, 2, 1, 8, 4, 4, 2, 8, 4, 8, 4},
+    {8, 1, 1, 6, 2, 4, 2, 6, 2, 4, 2},    {8, 2, 1, 6, 2, 4, 2, 6, 2, 0, 0},
 };
 constexpr int inst_index(int nt, int r, int occ)
 {
@@ -192,14 +200,19 @@ constexpr int depth_x(int nt, int r, bool fp8, int occ)
 {
     return fp8 ? kInst[inst_index(nt, r, occ)].dx_fp8 : kInst[inst_index(nt, r, occ)].dx_bf16;
 }
-// The depths of one kernel dtype (kDtBf16, kDtFp8, kDtFp4).
+// The depths of one kernel dtype (kDtBf16, kDtFp8, kDtFp4, kDtFp8B); 0 for a
+// block-scaled instance that does not exist.
 constexpr int depth_w_dt(int nt, int r, int dt, int occ)
 {
-    return dt == kDtFp4 ? kInst[inst_index(nt, r, occ)].dw_fp4 : depth_w(nt, r, dt == kDtFp8, occ);
+    return dt == kDtFp4    ? kInst[inst_index(nt, r, occ)].dw_fp4
+           : dt == kDtFp8B ? kInst[inst_index(nt, r, occ)].dw_b128
+                           : depth_w(nt, r, dt == kDtFp8, occ);
 }
 constexpr int depth_x_dt(int nt, int r, int dt, int occ)
 {
-    return dt == kDtFp4 ? kInst[inst_index(nt, r, occ)].dx_fp4 : depth_x(nt, r, dt == kDtFp8, occ);
+    return dt == kDtFp4    ? kInst[inst_index(nt, r, occ)].dx_fp4
+           : dt == kDtFp8B ? kInst[inst_index(nt, r, occ)].dx_b128
+                           : depth_x(nt, r, dt == kDtFp8, occ);
 }
 
 inline int64_t plan_ctas(int64_t rt, int r, int wk, int splits)
@@ -313,9 +326,11 @@ inline bool use_tc(int64_t n, int m)
     return m > kMaxRingM || (m >= kTcMinM && ceil_div(n, 128) >= kTcMinRowBlocks);
 }
 
-// The register-ring plan (1..64 tokens), for every dtype; MXFP4 planes run
-// only this kernel.
-inline Plan make_ring_plan(int64_t n, int64_t k, int m, int sm_count)
+// The register-ring plan (1..64 tokens), for every dtype; MXFP4 and
+// block-scaled planes run only this kernel.  The plan is the same for every
+// dtype, except that block-scaled planes (b128) choose among the instances
+// that exist for them, scored with their own ring depths.
+inline Plan make_ring_plan(int64_t n, int64_t k, int m, int sm_count, bool b128 = false)
 {
     Plan p{};
     p.nt = nt_for_m(m);
@@ -328,7 +343,7 @@ inline Plan make_ring_plan(int64_t n, int64_t k, int m, int sm_count)
     int64_t best_waves = 0, best_inflight = 0, best_warps = 0, best_bpw = 0;
     int best_r = 1, best_wk = 1, best_occ = 1;
     for (int ii = 0; ii < kNumInst; ++ii) {
-        if (kInst[ii].nt != p.nt)
+        if (kInst[ii].nt != p.nt || (b128 && kInst[ii].dw_b128 == 0))
             continue;
         const int occ = kInst[ii].occ, r = kInst[ii].r;
         const int64_t slots = int64_t(sms) * occ;
@@ -340,7 +355,7 @@ inline Plan make_ring_plan(int64_t n, int64_t k, int m, int sm_count)
                 const int64_t ctas = plan_ctas(p.rt, r, wk, 1);
                 const int64_t waves = ceil_div(ctas, slots);
                 const int64_t resident = ctas < slots ? ctas : slots;
-                const int64_t dw = depth_w(p.nt, r, true, occ);
+                const int64_t dw = b128 ? kInst[ii].dw_b128 : depth_w(p.nt, r, true, occ);
                 // only row tiles that exist are streamed: a plane with fewer
                 // tiles than its CTAs hold leaves the other warps idle
                 const int64_t cta_tiles = int64_t(kWarps / wk) * r;
@@ -378,7 +393,7 @@ inline Plan make_ring_plan(int64_t n, int64_t k, int m, int sm_count)
     p.r = best_r;
     p.wk = best_wk;
     p.occ = best_occ;
-    p.dw = depth_w(p.nt, p.r, true, p.occ);
+    p.dw = depth_w_dt(p.nt, p.r, b128 ? kDtFp8B : kDtFp8, p.occ);
     int splits = 1;
     while (plan_ctas(p.rt, p.r, p.wk, splits) * 2 <= sms &&
            p.kb / (int64_t(p.wk) * splits * 2) >= 4)

@@ -16,6 +16,9 @@
 // FP8 also writes the build's copy of the row scales; a row that holds a NaN
 // code (0x7F or 0xFF) gets a NaN scale, so its outputs are NaN as the
 // definition gives, while the GEMV's widening stays a fixed exact map.
+// Block-scaled FP8 planes repack their codes the same way, take row scales
+// of 1 (NaN for a row holding a NaN code) and copy their 128 x 128 block
+// factors into the build, one dense row of ceil(K / 128) per 128 rows.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -119,7 +122,9 @@ __global__ void __launch_bounds__(256) repack_fp8_kernel(const RepackArgs a)
         const int64_t n = rt * kTileN + threadIdx.x;
         float s = 0.0f;
         if (n < a.n)
-            s = nan_row[threadIdx.x] ? __int_as_float(0x7FC00000) : a.scale_src[src_row(a, n)];
+            s = nan_row[threadIdx.x] ? __int_as_float(0x7FC00000)
+                : a.scale_src          ? a.scale_src[src_row(a, n)]
+                                       : 1.0f; // block-scaled: the factors are the blocks'
         a.scale_dst[n] = s;
     }
 }
@@ -217,13 +222,25 @@ __global__ void __launch_bounds__(256) repack_fp4_kernel(const RepackArgs a)
     }
 }
 
+// Block-scaled FP8: the factors of one row block (CTA) into the build's copy.
+__global__ void __launch_bounds__(256) copy_factors_kernel(const RepackArgs a)
+{
+    const int64_t rb = blockIdx.x;
+    const int64_t cols = (a.k + kBlockB - 1) / kBlockB;
+    for (int64_t c = threadIdx.x; c < cols; c += blockDim.x)
+        a.bfac_dst[rb * cols + c] = a.bfac_src[rb * a.ldb + c];
+}
+
 } // namespace
 
 cudaError_t launch_repack(int dt, const RepackArgs &a, cudaStream_t s)
 {
     if (a.rt <= 0)
         return cudaSuccess;
-    if (dt == kDtFp8)
+    if (dt == kDtFp8B) {
+        repack_fp8_kernel<<<dim3(unsigned(a.rt)), 256, 0, s>>>(a);
+        copy_factors_kernel<<<dim3(unsigned((a.n + kBlockB - 1) / kBlockB)), 256, 0, s>>>(a);
+    } else if (dt == kDtFp8)
         repack_fp8_kernel<<<dim3(unsigned(a.rt)), 256, 0, s>>>(a);
     else if (dt == kDtFp4)
         repack_fp4_kernel<<<dim3(unsigned(a.rt)), 256, 0, s>>>(a);

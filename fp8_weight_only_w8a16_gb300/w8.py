@@ -22,9 +22,11 @@ from . import build_lib
 LIB_PATH = build_lib.LIB
 
 DT_E4M3FN, DT_BF16, DT_E4M3FNUZ, DT_E5M2, DT_FP16, DT_MXFP4 = 1, 2, 3, 4, 5, 6
+DT_E4M3FN_B128 = 7  # FP8 codes with one fp32 factor per 128 x 128 block
 SRC_ROW_MAJOR, SRC_GATE_UP = 0, 1
 LAYOUT_MMA_16x32, LAYOUT_MMA_16x32_GATE_UP = 1, 2
 MAX_M = 256
+ABI_VERSION = 5  # W8_ABI_VERSION of include/w8.h (the structs below follow it)
 
 STATUS = {
     0: "W8_OK", 1: "W8_ERR_NULL", 2: "W8_ERR_DTYPE", 3: "W8_ERR_UNPADDED", 4: "W8_ERR_BIAS",
@@ -52,7 +54,8 @@ class PlaneInfo(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int32), ("layout", ctypes.c_int32), ("n", ctypes.c_int64),
                 ("k", ctypes.c_int64), ("row_tiles", ctypes.c_int64),
                 ("k_blocks", ctypes.c_int64), ("packed", ctypes.c_void_p),
-                ("scale", ctypes.c_void_p), ("packed_bytes", ctypes.c_size_t)]
+                ("scale", ctypes.c_void_p), ("packed_bytes", ctypes.c_size_t),
+                ("block_factors", ctypes.c_void_p)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -108,6 +111,9 @@ def _load():
     lib.w8_gate_up_packed_row.restype = i64
     lib.w8_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), i32]
     lib.w8_device_status.restype = st
+    if lib.w8_abi_version() != ABI_VERSION:
+        raise ImportError(f"{LIB_PATH} has ABI {lib.w8_abi_version()}, this binding "
+                          f"{ABI_VERSION}: rebuild it")
     return lib
 
 
@@ -147,6 +153,7 @@ class Plane:
     bias: torch.Tensor | None = None
     layout: int = SRC_ROW_MAJOR
     block_scale: torch.Tensor | None = None  # MXFP4: [n, ldb] uint8 E8M0 scales
+    ldb: int | None = None  # block-scaled FP8: row stride of scale in floats
 
     @staticmethod
     def from_tensor(w: torch.Tensor, scale: torch.Tensor | None = None, k: int | None = None,
@@ -181,14 +188,24 @@ class Plane:
         return Plane(w=w, dtype=DT_MXFP4, n=w.shape[0], k=2 * w.shape[1] if k is None else k,
                      ldw=ldw, layout=layout, block_scale=block_scale)
 
+    @staticmethod
+    def e4m3_b128(w: torch.Tensor, factors: torch.Tensor, k: int | None = None) -> "Plane":
+        """A block-scaled FP8 plane: w [n, ldw] uint8 E4M3fn codes, factors
+        [ceil(n/128), ldb] fp32, entry (i, j) covering rows 128i.. and columns
+        128j.. of W."""
+        assert w.dim() == 2 and w.stride(1) == 1 and w.element_size() == 1
+        assert factors.dim() == 2 and factors.stride(1) == 1 and factors.dtype == torch.float32
+        return Plane(w=w, dtype=DT_E4M3FN_B128, n=w.shape[0], k=w.shape[1] if k is None else k,
+                     ldw=w.stride(0), scale=factors, ldb=factors.stride(0))
+
     def desc(self) -> PlaneDesc:
         bs = self.block_scale
+        ldb = bs.stride(0) if bs is not None else (self.ldb or 0)
         return PlaneDesc(self.w.data_ptr() if self.w is not None else None, self.dtype,
                          self.layout, self.n, self.k, self.ldw,
                          self.scale.data_ptr() if self.scale is not None else None,
                          self.bias.data_ptr() if self.bias is not None else None,
-                         bs.data_ptr() if bs is not None else None,
-                         bs.stride(0) if bs is not None else 0)
+                         bs.data_ptr() if bs is not None else None, ldb)
 
 
 def _descs(planes):

@@ -21,7 +21,7 @@ class Projection:
     name: str
     n: int
     k: int
-    dtype: str                  # "e4m3fn" or "bf16"
+    dtype: str                  # "e4m3fn", "e4m3fn_b128", "bf16" or "mxfp4"
     ms: tuple                   # decode-token counts exercised
     ldw: int | None = None      # source row stride when the plane is padded
     act: str = ""               # "silu_mul": a merged gate_up plane (gate rows first)
@@ -31,6 +31,8 @@ class Projection:
     def weight_bytes(self) -> int:
         if self.dtype == "mxfp4":  # codes, half a byte each, and one E8M0 byte per 32
             return self.n * self.k // 2 + self.n * -(-self.k // 32)
+        if self.dtype == "e4m3fn_b128":  # codes and one fp32 factor per 128 x 128 block
+            return self.n * self.k + 4 * -(-self.n // 128) * -(-self.k // 128)
         return self.n * self.k * (1 if self.dtype == "e4m3fn" else 2)
 
     @property
@@ -45,7 +47,9 @@ class Projection:
         return b
 
     def flops(self, m: int) -> int:
-        return 2 * m * self.n * self.k + (m * self.n if self.dtype == "e4m3fn" else 0)
+        extra = (m * self.n if self.dtype == "e4m3fn" else
+                 2 * m * self.n * -(-self.k // 128) if self.dtype == "e4m3fn_b128" else 0)
+        return 2 * m * self.n * self.k + extra
 
 
 SWEEP_M = (1, 2, 4, 8, 16, 32, 64)
@@ -86,15 +90,23 @@ O_PROJ_MXFP4 = Projection("o_proj_mxfp4", 6144, 16384, "mxfp4", (1, 2, 8, 32))
 Q_B_MXFP4 = Projection("q_b_proj_mxfp4", 16384, 2048, "mxfp4", (1, 8, 64))
 FUSED_QKV_A_MXFP4 = Projection("fused_qkv_a_proj_mxfp4", 2624, 6144, "mxfp4", (1, 4, 16))
 
+# Block-scaled FP8 (one fp32 factor per 128 x 128 block): the GLM-5.2 anatomy
+# page runs fused_qkv_a_proj through a blockscale GEMM; o_proj as the largest
+# attention plane.  Register ring, 1..64 tokens.
+FUSED_QKV_A_B128 = Projection("fused_qkv_a_proj_b128", 2624, 6144, "e4m3fn_b128", (1, 4, 16))
+O_PROJ_B128 = Projection("o_proj_b128", 6144, 16384, "e4m3fn_b128", (1, 2, 8, 32))
+
 ALL = (TINY, FUSED_QKV_A, O_PROJ, O_PROJ_BF16, SHARED_GATE_UP, SHARED_DOWN,
        SHARED_GATE_UP_KPAD, SHARED_GATE_UP_SILU, Q_B, KV_B, WQ_B, WK, WEIGHTS_PROJ, WK_WEIGHTS_PROJ, LM_HEAD,
-       O_PROJ_LARGE_M, Q_B_LARGE_M, KV_B_LARGE_M, O_PROJ_MXFP4, Q_B_MXFP4, FUSED_QKV_A_MXFP4)
+       O_PROJ_LARGE_M, Q_B_LARGE_M, KV_B_LARGE_M, O_PROJ_MXFP4, Q_B_MXFP4, FUSED_QKV_A_MXFP4,
+       FUSED_QKV_A_B128, O_PROJ_B128)
 BY_NAME = {p.name: p for p in ALL}
 
 # The workload groups, in order: the tiny correctness case, the fused
 # qkv_a projection, o_proj (FP8 and bf16), the shared-expert pair with its
 # K-padded variant and its gate_up with SiLU-and-multiply, the full-layer
-# sweep, 96..256 tokens on the large attention projections, and MXFP4 planes.
+# sweep, 96..256 tokens on the large attention projections, MXFP4 planes and
+# block-scaled FP8 planes.
 GROUPS = {
     "tiny": (TINY,),
     "fused_qkv_a_proj": (FUSED_QKV_A,),
@@ -103,4 +115,5 @@ GROUPS = {
     "layer_sweep": (Q_B, KV_B, WQ_B, WK, WEIGHTS_PROJ, WK_WEIGHTS_PROJ, LM_HEAD),
     "large_m": (O_PROJ_LARGE_M, Q_B_LARGE_M, KV_B_LARGE_M),
     "mxfp4": (O_PROJ_MXFP4, Q_B_MXFP4, FUSED_QKV_A_MXFP4),
+    "block_scaled": (FUSED_QKV_A_B128, O_PROJ_B128),
 }

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define W8_ABI_VERSION 4
+#define W8_ABI_VERSION 5
 
 /* A cudaStream_t: the runtime's stream type is this same pointer type. */
 typedef struct CUstream_st *w8_stream;
@@ -56,15 +56,18 @@ typedef enum {
     W8_ERR_UNPADDED = 3,  /* plane base not 16-byte aligned, or row stride not a multiple
                              of 16 bytes */
     W8_ERR_BIAS = 4,      /* a bias pointer was given: the GEMV has no bias */
-    W8_ERR_MIXED = 5,     /* bf16 and FP8 planes mixed in one build */
+    W8_ERR_MIXED = 5,     /* planes of different dtypes in one build (bf16 and FP8 among
+                             them) */
     W8_ERR_SHAPE = 6,     /* N or K < 1 or too large, ldw < K, M outside 0..256,
                              ldx < K, ldy < N (< N/2 for w8_gemv_silu_mul), or a
                              W8_SRC_GATE_UP plane whose N is not a multiple of 16 */
-    W8_ERR_SCALE = 7,     /* an FP8 plane without row scales, a bf16 or MXFP4 plane with
-                             them, an MXFP4 plane without block scales or ldb too short,
-                             or another plane with block scales */
-    W8_ERR_LAYOUT = 8,    /* unknown source layout, or w8_gemv_silu_mul on a plane not
-                             bound as W8_SRC_GATE_UP */
+    W8_ERR_SCALE = 7,     /* an FP8 plane without row scales, a block-scaled FP8 plane
+                             without factors or ldb < ceil(k / 128), a bf16 or MXFP4
+                             plane with scale set, an MXFP4 plane without block scales
+                             or ldb too short, or another plane with block_scale set */
+    W8_ERR_LAYOUT = 8,    /* unknown source layout, a block-scaled FP8 plane given as
+                             W8_SRC_GATE_UP, or w8_gemv_silu_mul on a plane not bound as
+                             W8_SRC_GATE_UP */
     W8_ERR_CAPACITY = 9,  /* packed buffer or workspace smaller than required */
     W8_ERR_ALIGN = 10,    /* packed buffer or workspace not 256-byte aligned, x not 16-byte
                              aligned or ldx not a multiple of 8, or y not 2-byte aligned */
@@ -75,9 +78,10 @@ typedef enum {
                              library's fixed W8_NOALLOC_SCRATCH_BYTES */
 } w8_status;
 
-/* Source element types.  Bind accepts E4M3FN, BF16 and (w4a16) MXFP4 and
- * refuses every other format, e4m3fnuz among them (the PR page, Changes and
- * Limitations: bind turns away planes its kernels cannot decode). */
+/* Source element types.  Bind accepts E4M3FN, E4M3FN_B128, BF16 and (w4a16)
+ * MXFP4 and refuses every other format, e4m3fnuz among them (the PR page,
+ * Changes and Limitations: bind turns away planes its kernels cannot
+ * decode). */
 typedef enum {
     W8_DT_E4M3FN = 1,
     W8_DT_BF16 = 2,
@@ -90,7 +94,18 @@ typedef enum {
      * checkpoint).  The OCP microscaling format: E2M1 elements, two per
      * byte (the even column in the low nibble), 32 consecutive elements
      * along K sharing one E8M0 scale 2^(e - 127) (255 = NaN). */
-    W8_DT_MXFP4 = 6
+    W8_DT_MXFP4 = 6,
+    /* Block-scaled FP8: E4M3fn codes with one fp32 factor per block of 128
+     * rows x 128 columns instead of row scales (the GLM-5.2 anatomy page runs
+     * fused_qkv_a_proj through a blockscale GEMM; the ATOM Model Support
+     * Guide, Weight loading, loads a checkpoint's weight_scale_inv tensors as
+     * the weight scales).  The pages fix neither the block shape nor where
+     * the factor enters; this library takes 128 x 128 and applies each
+     * factor to the finished sum of its block's 128 columns:
+     *   y[m, n] = bf16( sum_j f[n/128, j] * sum_{k in block j} W[n, k] x[m, k] ),
+     * the inner sums and the total in fp32.  Register-ring kernel only
+     * (m <= 64); not with W8_SRC_GATE_UP. */
+    W8_DT_E4M3FN_B128 = 7
 } w8_dtype;
 
 /* Source layouts: row-major [n][ldw] planes (K contiguous).
@@ -130,23 +145,30 @@ typedef struct {
     int64_t k;            /* logical reduction columns, >= 1; columns k..ldw-1 are ignored */
     int64_t ldw;          /* row stride in elements, >= k, ldw * element bytes % 16 == 0
                              (MXFP4: ldw % 32 == 0) */
-    const float *scale;   /* device, [n] fp32 row scales: required for E4M3FN, NULL otherwise */
+    const float *scale;   /* device fp32: E4M3FN [n] row scales; E4M3FN_B128
+                             [ceil(n / 128)][ldb] block factors, entry (i, j) covering
+                             rows 128i .. 128i+127 and columns 128j .. 128j+127;
+                             NULL for the other dtypes */
     const void *bias;     /* must be NULL */
     const uint8_t *block_scale; /* device, MXFP4 only: [n][ldb] E8M0 scales, block j covering
                              columns 32j .. 32j+31; NULL for the other dtypes */
-    int64_t ldb;          /* MXFP4: row stride of block_scale in bytes, >= ceil(k / 32) */
+    int64_t ldb;          /* MXFP4: row stride of block_scale in bytes, >= ceil(k / 32);
+                             E4M3FN_B128: row stride of scale in floats, >= ceil(k / 128) */
 } w8_plane_desc;
 
 /* What a build records about one bound plane. */
 typedef struct {
-    int32_t dtype;           /* W8_DT_E4M3FN, W8_DT_BF16 or W8_DT_MXFP4 */
+    int32_t dtype;           /* W8_DT_E4M3FN, W8_DT_E4M3FN_B128, W8_DT_BF16 or W8_DT_MXFP4 */
     int32_t layout;          /* W8_LAYOUT_MMA_16x32 or W8_LAYOUT_MMA_16x32_GATE_UP */
     int64_t n, k;
     int64_t row_tiles;       /* ceil(n / 16) */
     int64_t k_blocks;        /* ceil(k / 32) */
     const void *packed;      /* device, inside the caller's packed buffer */
-    const float *scale;      /* device, the build's copy of the row scales (FP8), else NULL */
+    const float *scale;      /* device, the build's copy of the row scales (FP8; 1 for
+                                block-scaled FP8), else NULL */
     size_t packed_bytes;     /* bytes of the packed weights (MXFP4: with the block scales) */
+    const float *block_factors; /* device, block-scaled FP8: the build's copy of the factors,
+                                [ceil(n / 128)][ceil(k / 128)]; else NULL */
 } w8_plane_info;
 
 /* The launch a gemv call makes for one (plane, m); returned for inspection.
@@ -193,7 +215,8 @@ int w8_abi_version(void);
 
 /* Host-only check of n_planes descriptors, as w8_bind makes them: dtype, layout,
  * bias, shape, scale presence, 16-byte padding and alignment, and that all
- * planes share one dtype.  Touches no device memory and calls no CUDA API. */
+ * planes share one dtype (W8_ERR_MIXED).  Touches no device memory and calls
+ * no CUDA API. */
 w8_status w8_validate(const w8_plane_desc *d, int n_planes);
 
 /* Bytes of the packed buffer w8_bind needs for these planes (host-only).
@@ -202,8 +225,9 @@ w8_status w8_packed_bytes(const w8_plane_desc *d, int n_planes, size_t *bytes);
 
 /* Validate the planes, then repack each into the caller's device buffer dst
  * (256-byte aligned, at least w8_packed_bytes) on stream s: the weights in
- * W8_LAYOUT_MMA_16x32 and, for FP8, a copy of the row scales.  An FP8 row
- * holding a NaN code (0x7F / 0xFF) gets a NaN scale in that copy, so its
+ * W8_LAYOUT_MMA_16x32 and, for FP8, a copy of the row scales (all 1 for a
+ * block-scaled plane, which also gets a copy of its block factors).  An FP8
+ * row holding a NaN code (0x7F / 0xFF) gets a NaN scale in that copy, so its
  * outputs are NaN, as the definition gives.  On W8_OK *out is a new handle
  * for the device current at the call, the repack has completed (the stream
  * is synchronised) and the source planes and scales may be freed.  dst must
@@ -224,7 +248,10 @@ w8_status w8_plan_info(const w8_build *b, int plane, int m, w8_plan *plan);
 
 /* The same plan for a plane of n rows and k columns on a GPU with sm_count
  * SMs, computed on the host without a build (no CUDA call).  The plan depends
- * on (n, k, m, sm_count) only, never on the weight dtype. */
+ * on (n, k, m, sm_count) only, not on the weight dtype, except that MXFP4 and
+ * block-scaled FP8 planes always run the register ring, block-scaled ones on
+ * the instances that hold their second set of accumulators (w8_plan_info
+ * gives a bound plane's own plan). */
 w8_status w8_plan_shape(int64_t n, int64_t k, int m, int sm_count, w8_plan *plan);
 
 /* Workspace bytes a gemv call on `plane` with `m` tokens needs (0 if none).
@@ -238,7 +265,9 @@ w8_status w8_plan_shape(int64_t n, int64_t k, int m, int sm_count, w8_plan *plan
 w8_status w8_workspace_bytes(const w8_build *b, int plane, int m, size_t *bytes);
 
 /* The FP8 (w8a16) GEMV on an E4M3FN build:
- *   y[i*ldy + n] = bf16(scale[n] * sum_k W[n,k] * x[i*ldx + k]),  0 <= i < m, 0 <= n < N.
+ *   y[i*ldy + n] = bf16(scale[n] * sum_k W[n,k] * x[i*ldx + k]),  0 <= i < m, 0 <= n < N;
+ * on an E4M3FN_B128 build the block-factor form of that dtype's comment
+ * (m: 0..64, W8_ERR_SHAPE above).
  * x: device bf16 [m][ldx], ldx >= K, ldx % 8 == 0, 16-byte aligned (every
  *    row is read with 16-byte loads; columns K..ldx-1 are never read);
  * y: device bf16 [m][ldy], ldy >= N, written for n < N only;
@@ -323,9 +352,9 @@ w8_status w8_gemv_noalloc(const w8_build *b, int plane, const uint16_t *x, int64
 /* Host-side address map of W8_LAYOUT_MMA_16x32: byte offset, inside one
  * plane's packed weights, of element (row, col) of a plane with k_blocks
  * blocks of 32 columns (row is the packed row: for a gate_up plane, see
- * w8_gate_up_packed_row).  dtype is W8_DT_E4M3FN or W8_DT_BF16 (MXFP4 codes
- * are not byte-addressable: see w8_mxfp4_code_bits); returns -1 on a bad
- * argument.  The repack kernel places every element at this offset. */
+ * w8_gate_up_packed_row).  dtype is W8_DT_E4M3FN, W8_DT_E4M3FN_B128 (the
+ * same layout) or W8_DT_BF16 (MXFP4 codes are not byte-addressable: see
+ * w8_mxfp4_code_bits); returns -1 on a bad argument.  The repack kernel places every element at this offset. */
 int64_t w8_packed_offset(int dtype, int64_t k_blocks, int64_t row, int64_t col);
 
 /* Host-side address map of an MXFP4 plane's packed runs: the BIT offsets of

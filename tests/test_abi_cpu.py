@@ -43,7 +43,7 @@ def test_every_declared_function_is_exported():
 
 
 def test_abi_version_and_status_strings():
-    assert w8.lib.w8_abi_version() == 4
+    assert w8.lib.w8_abi_version() == 5
     for code in range(15):
         assert w8.status_str(code)
     assert w8.status_str(99) == "unknown status"
@@ -61,6 +61,7 @@ def _desc(**kw):
 
 
 MX = dict(dtype=w8.DT_MXFP4, scale=None, block_scale=FAKE + 8192, ldb=4)
+B128 = dict(dtype=w8.DT_E4M3FN_B128, ldb=1)
 
 
 def _status(*descs):
@@ -106,6 +107,15 @@ def _status(*descs):
     (dict(MX, ldw=129, k=100), "W8_ERR_UNPADDED"),
     (dict(MX, ldw=160), "W8_OK"),                # 80 bytes a row
     ({"block_scale": FAKE + 8192, "ldb": 4}, "W8_ERR_SCALE"),  # FP8 plane with block scales
+    # block-scaled FP8: fp32 factors [ceil(n/128)][ldb] in scale, ldb >= ceil(k/128)
+    (dict(B128), "W8_OK"),
+    (dict(B128, k=300, ldw=304, ldb=3), "W8_OK"),
+    (dict(B128, k=300, ldw=304, ldb=2), "W8_ERR_SCALE"),
+    (dict(B128, ldb=0), "W8_ERR_SCALE"),
+    (dict(B128, scale=None), "W8_ERR_SCALE"),
+    (dict(B128, block_scale=FAKE + 8192), "W8_ERR_SCALE"),
+    (dict(B128, layout=w8.SRC_GATE_UP), "W8_ERR_LAYOUT"),
+    (dict(B128, ldw=136), "W8_ERR_UNPADDED"),
 ])
 def test_validate_refusal_matrix(kw, want):
     assert w8.STATUS[_status(_desc(**kw))] == want
@@ -117,6 +127,8 @@ def test_mixed_build_refused_and_empty_list():
     assert w8.STATUS[_status(bf, _desc())] == "W8_ERR_MIXED"
     assert w8.STATUS[_status(_desc(), _desc(n=7, k=33, ldw=48))] == "W8_OK"
     assert w8.STATUS[w8.lib.w8_validate(None, 0)] == "W8_ERR_NULL"
+    # row-scaled and block-scaled FP8 are different dtypes too
+    assert w8.STATUS[_status(_desc(), _desc(**B128))] == "W8_ERR_MIXED"
     # a bad plane anywhere in the list is reported before the mix check
     assert w8.STATUS[_status(_desc(), _desc(bias=FAKE))] == "W8_ERR_BIAS"
 
@@ -149,6 +161,14 @@ def test_mxfp4_bit_map_is_a_bijection_onto_the_code_bits():
         w8.mxfp4_code_bits(1, 0, 32)
 
 
+def test_packed_bytes_block_scaled():
+    # [300, 500]: 19 tiles x 16 blocks x 512 B, row copy 19*16*4 B, factors 3 x 4 x 4 B
+    d = _desc(n=300, k=500, ldw=512, **B128)
+    d.ldb = 4
+    want = 19 * 16 * 512 + (-(-19 * 16 * 4 // 256)) * 256 + 256
+    assert w8.packed_bytes([d]) == want
+
+
 def test_packed_bytes_formula():
     # FP8 [100, 200]: 7 tiles x 7 blocks x 512 B, scales 7*16*4 B (each 256-aligned)
     assert w8.packed_bytes([_desc(n=100, k=200, ldw=208)]) == 25088 + 512
@@ -174,7 +194,8 @@ def test_gate_up_packed_row_interleaves_gate_and_up(n):
         assert w8.gate_up_packed_row(bad_n, 0) == -1
 
 
-@pytest.mark.parametrize("dtype,elt", [(w8.DT_E4M3FN, 1), (w8.DT_BF16, 2)])
+@pytest.mark.parametrize("dtype,elt", [(w8.DT_E4M3FN, 1), (w8.DT_E4M3FN_B128, 1),
+                                       (w8.DT_BF16, 2)])
 def test_packed_offset_is_a_bijection(dtype, elt):
     rt, kb = 3, 4
     offs = [w8.packed_offset(dtype, kb, r, c) for r in range(rt * 16) for c in range(kb * 32)]

@@ -455,8 +455,9 @@ def test_multi_plane_build(w8):
 # ---------------------------------------------------------------------------
 
 # (gate_up planes with SiLU-and-multiply: tests/test_gpu_gate_up.py; MXFP4
-# planes: tests/test_gpu_mxfp4.py)
-FULL = [p for p in workloads.ALL if p.name != "lm_head" and not p.act and p.dtype != "mxfp4"]
+# planes: tests/test_gpu_mxfp4.py; block-scaled FP8 planes: tests/test_gpu_b128.py)
+FULL = [p for p in workloads.ALL
+        if p.name != "lm_head" and not p.act and p.dtype in ("e4m3fn", "bf16")]
 
 
 @pytest.mark.parametrize("proj", FULL, ids=[p.name for p in FULL])
