@@ -199,8 +199,13 @@ class GemvBench:
         assert x_all.shape[0] >= mmax, "the workload draws fewer token rows than the largest M"
         self.x_host = np.ascontiguousarray(x_all[:mmax])
         self.x = torch.from_numpy(self.x_host.view(np.int16)).to(device)
-        self.y = {m: torch.zeros((m, proj.out_n), dtype=torch.int16, device=device)
-                  for m in self.ms}
+        # every call's output rows in one buffer (row blocks of m rows, in the
+        # order of ms), so that a step's results leave the device in one copy
+        self.y_all = torch.zeros((sum(self.ms), proj.out_n), dtype=torch.int16, device=device)
+        self.y, row = {}, 0
+        for m in self.ms:
+            self.y[m] = self.y_all[row: row + m]
+            row += m
         self.ws = self.build.new_workspace()
 
     def step_bytes(self):
@@ -297,20 +302,20 @@ def cpu_oracle_rate(proj, ms, budget_s=10.0, rows=None, threads=None):
 def e2e_rate(b: GemvBench, steps, torch):
     """Through the public API with host buffers: per step, copy the step's
     tokens from pinned host memory, run the three calls, read every output
-    back into pinned host memory and wait for it on the host.  As a serving
+    back into pinned host memory (the calls write row blocks of one buffer,
+    read back in one copy) and wait for it on the host.  As a serving
     loop would, each step's device work (the copies and the three library
     calls, made through the Python binding of the C ABI) is captured once in
     a CUDA graph and replayed; the host waits for every step."""
     mmax = max(b.ms)
     x_pin = torch.from_numpy(b.x_host.view(np.int16)).pin_memory()
-    y_pin = {m: torch.empty((m, b.proj.out_n), dtype=torch.int16).pin_memory() for m in b.ms}
+    y_pin = torch.empty(tuple(b.y_all.shape), dtype=torch.int16).pin_memory()
 
     def body(j):
         b.x.copy_(x_pin, non_blocking=True)
         for c, m in b.step_calls(j):
             b.launch(c, m)
-        for m in b.ms:
-            y_pin[m].copy_(b.y[m], non_blocking=True)
+        y_pin.copy_(b.y_all, non_blocking=True)  # every call's output, one copy
 
     cyc = b.copies // len(b.ms)
     s = torch.cuda.Stream()
