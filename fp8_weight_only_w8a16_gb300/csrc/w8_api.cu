@@ -390,6 +390,50 @@ w8_status w8_plan_shape(int64_t n, int64_t k, int m, int sm_count, w8_plan *out)
     return W8_OK;
 }
 
+// The plan a gemv call on a plane of this dtype and shape makes, with the
+// dtype's own ring depth.
+static void fill_plan_dt(int32_t dtype, int64_t n, int64_t k, int m, int sms, w8_plan *out)
+{
+    const w8::Plan pl = plan_for(dtype, n, k, m, sms);
+    fill_plan(pl, out);
+    if (dtype == W8_DT_BF16)
+        out->depth = pl.tc ? w8::tc_stages(false, pl.npad).nw * w8::kTcStageBlocks
+                           : w8::depth_w(pl.nt, pl.r, false, pl.occ);
+    if (dtype == W8_DT_MXFP4)
+        out->depth = w8::depth_w_dt(pl.nt, pl.r, w8::kDtFp4, pl.occ);
+    if (dtype == W8_DT_E4M3FN_B128 && !pl.tc) {
+        // the kernel splits K among CTAs and warps in whole column blocks
+        // (units of 4 K blocks, floor boundaries, the last unit cut at kb)
+        const int64_t u = w8::kBlockB / w8::kTileK, nu = w8::ceil_div(pl.kb, u);
+        int64_t most = 0;
+        for (int sp = 0; sp < pl.splits; ++sp) {
+            const int64_t c0 = sp * nu / pl.splits, c1 = (sp + 1) * nu / pl.splits;
+            for (int q = 0; q < pl.wk; ++q) {
+                const int64_t k0 = (c0 + q * (c1 - c0) / pl.wk) * u;
+                const int64_t k1 = (c0 + (q + 1) * (c1 - c0) / pl.wk) * u;
+                const int64_t len = (k1 < pl.kb ? k1 : pl.kb) - k0;
+                most = len > most ? len : most;
+            }
+        }
+        out->k_blocks_per_warp_max = int32_t(most);
+    }
+}
+
+w8_status w8_plan_shape_dtype(int64_t n, int64_t k, int m, int sm_count, int32_t dtype,
+                              w8_plan *out)
+{
+    if (!out)
+        return W8_ERR_NULL;
+    if (dtype != W8_DT_E4M3FN && dtype != W8_DT_E4M3FN_B128 && dtype != W8_DT_BF16 &&
+        dtype != W8_DT_MXFP4)
+        return W8_ERR_DTYPE;
+    if (n < 1 || k < 1 || n > kMaxDim || k > kMaxDim || m < 1 || m > max_m(dtype) ||
+        sm_count < 1)
+        return W8_ERR_SHAPE;
+    fill_plan_dt(dtype, n, k, m, sm_count, out);
+    return W8_OK;
+}
+
 w8_status w8_plan_info(const w8_build *b, int plane, int m, w8_plan *out)
 {
     if (!b || !out)
@@ -399,13 +443,7 @@ w8_status w8_plan_info(const w8_build *b, int plane, int m, w8_plan *out)
     const w8_plane_info &p = b->planes[size_t(plane)];
     if (m < 1 || m > max_m(p.dtype))
         return W8_ERR_SHAPE;
-    const w8::Plan pl = plan_for(p.dtype, p.n, p.k, m, b->sm_count);
-    fill_plan(pl, out);
-    if (p.dtype == W8_DT_BF16)
-        out->depth = pl.tc ? w8::tc_stages(false, pl.npad).nw * w8::kTcStageBlocks
-                           : w8::depth_w(pl.nt, pl.r, false, pl.occ);
-    if (p.dtype == W8_DT_MXFP4)
-        out->depth = w8::depth_w_dt(pl.nt, pl.r, w8::kDtFp4, pl.occ);
+    fill_plan_dt(p.dtype, p.n, p.k, m, b->sm_count, out);
     return W8_OK;
 }
 

@@ -95,6 +95,8 @@ def _load():
     lib.w8_plan_info.restype = st
     lib.w8_plan_shape.argtypes = [i64, i64, i32, i32, ctypes.POINTER(PlanInfo)]
     lib.w8_plan_shape.restype = st
+    lib.w8_plan_shape_dtype.argtypes = [i64, i64, i32, i32, i32, ctypes.POINTER(PlanInfo)]
+    lib.w8_plan_shape_dtype.restype = st
     lib.w8_workspace_bytes.argtypes = [vp, i32, i32, ctypes.POINTER(sz)]
     lib.w8_workspace_bytes.restype = st
     for name in ("w8_gemv", "bf16_gemv", "w8_gemv_silu_mul", "mxfp4_gemv"):
@@ -122,6 +124,7 @@ lib = _load()
 # every symbol include/w8.h declares
 EXPORTS = ("w8_status_str", "w8_abi_version", "w8_validate", "w8_packed_bytes", "w8_bind",
            "w8_release", "w8_build_planes", "w8_build_info", "w8_plan_info", "w8_plan_shape",
+           "w8_plan_shape_dtype",
            "w8_workspace_bytes", "w8_gemv", "bf16_gemv", "w8_gemv_silu_mul", "mxfp4_gemv",
            "w8_gemv_noalloc",
            "w8_packed_offset", "w8_mxfp4_code_bits", "w8_gate_up_packed_row", "w8_device_status")
@@ -331,6 +334,13 @@ def w8_gemv_silu_mul(build: Build, plane: int, x: torch.Tensor, y: torch.Tensor,
 def plan_shape(n: int, k: int, m: int, sm_count: int) -> PlanInfo:
     out = PlanInfo()
     _check(lib.w8_plan_shape(n, k, m, sm_count, ctypes.byref(out)))
+    return out
+
+
+def plan_shape_dtype(n: int, k: int, m: int, sm_count: int, dtype: int) -> PlanInfo:
+    """The plan a bound plane of this dtype and shape gets (w8_plan_shape_dtype)."""
+    out = PlanInfo()
+    _check(lib.w8_plan_shape_dtype(n, k, m, sm_count, dtype, ctypes.byref(out)))
     return out
 
 

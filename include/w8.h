@@ -254,6 +254,17 @@ w8_status w8_plan_info(const w8_build *b, int plane, int m, w8_plan *plan);
  * gives a bound plane's own plan). */
 w8_status w8_plan_shape(int64_t n, int64_t k, int m, int sm_count, w8_plan *plan);
 
+/* The plan, with the dtype's own ring depth, that a gemv call makes on a
+ * bound plane of this dtype (W8_DT_E4M3FN, W8_DT_E4M3FN_B128, W8_DT_BF16 or
+ * W8_DT_MXFP4), n rows and k columns on a GPU of sm_count SMs: what
+ * w8_plan_info returns for such a plane, computed on the host without a
+ * build (no CUDA call).  m: 1..256, or 1..64 for the register-ring-only
+ * dtypes (MXFP4, block-scaled FP8); W8_ERR_SHAPE otherwise, W8_ERR_DTYPE
+ * for another dtype.  No counterpart on the pages: it reports this
+ * library's own launch plan. */
+w8_status w8_plan_shape_dtype(int64_t n, int64_t k, int m, int sm_count, int32_t dtype,
+                              w8_plan *plan);
+
 /* Workspace bytes a gemv call on `plane` with `m` tokens needs (0 if none).
  * plane = -1 takes the largest over all planes, m = 0 the largest over
  * m = 1..256, so one workspace can serve every call of a build.

@@ -284,6 +284,69 @@ def test_plan_invariants(n, k, m):
         assert min(b - a for a, b in parts) >= 1
 
 
+PLAN_FIELDS = ("kernel", "grid", "block", "smem_bytes", "n_tiles", "row_tiles_per_warp",
+               "warps_k", "row_groups", "splits", "workspace_bytes")
+
+
+@pytest.mark.parametrize("n,k", SHAPES)
+@pytest.mark.parametrize("m", [1, 4, 8, 16, 17, 32, 64, 65, 200])
+def test_plan_shape_dtype_row_and_bf16_planes_match_the_shape_plan(n, k, m):
+    """E4M3FN and bf16 planes of one shape launch the same plan (the same
+    summation order); only the ring depth differs."""
+    base = w8.plan_shape(n, k, m, 152)
+    for dt in (w8.DT_E4M3FN, w8.DT_BF16):
+        p = w8.plan_shape_dtype(n, k, m, 152, dt)
+        assert all(getattr(p, f) == getattr(base, f) for f in PLAN_FIELDS), dt
+        assert p.k_blocks_per_warp_max == base.k_blocks_per_warp_max
+    assert w8.plan_shape_dtype(n, k, m, 152, w8.DT_E4M3FN).depth == base.depth
+
+
+@pytest.mark.parametrize("n,k", SHAPES)
+@pytest.mark.parametrize("m", [1, 2, 8, 9, 16, 17, 32, 33, 64])
+def test_plan_shape_dtype_ring_only_planes(n, k, m):
+    """MXFP4 and block-scaled planes run the register ring at every m; MXFP4
+    takes the ring plan FP8 would take there, block-scaled planes a ring of
+    whole column blocks, with K split among CTAs and warps in whole column
+    blocks."""
+    kb = -(-k // 32)
+    mx = w8.plan_shape_dtype(n, k, m, 152, w8.DT_MXFP4)
+    b1 = w8.plan_shape_dtype(n, k, m, 152, w8.DT_E4M3FN_B128)
+    for p in (mx, b1):
+        assert p.kernel == 0 and p.block == 256 and p.grid == p.row_groups * p.splits
+        assert p.n_tiles * 8 >= m and p.depth >= 1
+    fp8 = w8.plan_shape(n, k, m, 152)
+    if fp8.kernel == 0:
+        assert all(getattr(mx, f) == getattr(fp8, f) for f in PLAN_FIELDS)
+    assert b1.depth % 4 == 0
+    # the block-scaled K parts: units of 4 blocks, floor boundaries, the last cut at kb
+    nu = -(-kb // 4)
+    parts = []
+    for s in range(b1.splits):
+        c0, c1 = (s * nu) // b1.splits, ((s + 1) * nu) // b1.splits
+        for q in range(b1.warps_k):
+            a0 = 4 * (c0 + (q * (c1 - c0)) // b1.warps_k)
+            a1 = min(4 * (c0 + ((q + 1) * (c1 - c0)) // b1.warps_k), kb)
+            parts.append((min(a0, kb), max(a1, min(a0, kb))))
+    assert parts[0][0] == 0 and parts[-1][1] == kb
+    assert all(a1 == b0 for (_, a1), (b0, _) in zip(parts, parts[1:]))
+    assert all(a0 % 4 == 0 for a0, a1 in parts if a1 > a0)
+    assert max(b - a for a, b in parts) == b1.k_blocks_per_warp_max
+
+
+def test_plan_shape_dtype_refusals():
+    for dt in (w8.DT_MXFP4, w8.DT_E4M3FN_B128):
+        with pytest.raises(w8.W8Error) as e:
+            w8.plan_shape_dtype(2624, 6144, 65, 152, dt)
+        assert e.value.name == "W8_ERR_SHAPE"
+    for dt in (w8.DT_E4M3FNUZ, w8.DT_E5M2, w8.DT_FP16, 0, 99):
+        with pytest.raises(w8.W8Error) as e:
+            w8.plan_shape_dtype(2624, 6144, 1, 152, dt)
+        assert e.value.name == "W8_ERR_DTYPE"
+    with pytest.raises(w8.W8Error) as e:
+        w8.plan_shape_dtype(2624, 6144, 0, 152, w8.DT_E4M3FN)
+    assert e.value.name == "W8_ERR_SHAPE"
+
+
 def test_plan_does_not_depend_on_anything_but_shape():
     a = w8.plan_shape(2624, 6144, 4, 152)
     b = w8.plan_shape(2624, 6144, 4, 152)
