@@ -128,6 +128,8 @@ def _mutant(tmp_path, name):
     return oracle.load_variant(so)
 
 
+# (a mutant may produce garbage bit patterns whose numpy casts warn)
+@pytest.mark.filterwarnings("ignore::RuntimeWarning")
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_pins_catch_planted_mistake(tmp_path, name):
     mut = _mutant(str(tmp_path), name)
