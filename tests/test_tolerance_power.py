@@ -56,3 +56,29 @@ def test_tolerance_accepts_the_definition_and_rejects_mistakes(n, k, m):
         ym = oracle.gemv(wm, DT8, sm, xm, threads=8)
         ok, worst = oracle.within_tolerance(ym, y64, mag)
         assert not ok, f"{name} passes the tolerance (worst {worst:.3g})"
+
+
+def test_silu_mul_tolerance_rejects_mistakes():
+    """The propagated SiLU-and-multiply bound accepts the two-step result and
+    rejects gate and up swapped, the SiLU left out, the multiply left out, a
+    gate row paired with the next up row, and the sign of the SiLU's
+    exponent flipped."""
+    half, k, m = 128, 6144, 8
+    w, scale, x = _case(2 * half, k, m, seed=3)
+    y = oracle.gemv(w, DT8, scale, x, threads=8)
+    y64, mag = oracle.gemv_f64(w, DT8, scale, x, threads=8)
+    g, u = y[:, :half], y[:, half:]
+    args = (y64[:, :half], mag[:, :half], y64[:, half:], mag[:, half:])
+    ok, worst = oracle.silu_mul_within_tolerance(oracle.silu_mul(g, u), *args)
+    assert ok, worst
+    gf, uf = oracle.bf16_bits_to_f64(g), oracle.bf16_bits_to_f64(u)
+    wrong = {
+        "gate and up swapped": oracle.silu_mul(u, g),
+        "SiLU left out": oracle.f64_to_bf16_rne(gf * uf),
+        "multiply left out": oracle.f64_to_bf16_rne(oracle.silu_mul_f64(gf, 1.0)),
+        "up row of the next gate row": oracle.silu_mul(g, np.roll(u, -1, axis=1)),
+        "exponent sign flipped": oracle.f64_to_bf16_rne(gf / (1.0 + np.exp(gf)) * uf),
+    }
+    for name, h in wrong.items():
+        ok, worst = oracle.silu_mul_within_tolerance(h, *args)
+        assert not ok, f"{name} passes the tolerance (worst {worst:.3g})"
