@@ -82,3 +82,25 @@ def test_silu_mul_tolerance_rejects_mistakes():
     for name, h in wrong.items():
         ok, worst = oracle.silu_mul_within_tolerance(h, *args)
         assert not ok, f"{name} passes the tolerance (worst {worst:.3g})"
+
+
+def test_block_scaled_tolerance_rejects_wrong_factors():
+    """On a block-scaled plane the bound rejects the factor of the next column
+    block, of the next row block, and factors applied to each 32-column K
+    block's neighbour."""
+    n, k, m = 300, 1000, 4
+    plane, x_all = synth.workload(n, k, "e4m3fn_b128", seed=5)
+    w, f, x = plane.w, plane.scale, np.ascontiguousarray(x_all[:m])
+    y64, mag = oracle.gemv_b128_f64(w, f, x, threads=8)
+    ok, worst = oracle.within_tolerance(oracle.gemv_b128(w, f, x, threads=8), y64, mag)
+    assert ok, worst
+    xs = x.copy()
+    xs[:, 96:128], xs[:, 128:160] = x[:, 128:160], x[:, 96:128]  # across a block edge
+    wrong = {
+        "next column block's factor": (w, np.ascontiguousarray(np.roll(f, -1, axis=1)), x),
+        "next row block's factor": (w, np.ascontiguousarray(np.roll(f, -1, axis=0)), x),
+        "K blocks swapped across a factor edge": (w, f, xs),
+    }
+    for name, (wm, fm, xm) in wrong.items():
+        ok, worst = oracle.within_tolerance(oracle.gemv_b128(wm, fm, xm, threads=8), y64, mag)
+        assert not ok, f"{name} passes the tolerance (worst {worst:.3g})"
