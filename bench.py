@@ -454,6 +454,10 @@ def run_ours(args):
         cpu = None
         if world == 1 and not args.no_cpu:
             cpu = cpu_oracle_rate(proj, ms, budget_s=args.cpu_seconds)
+            one = cpu_oracle_rate(proj, ms, budget_s=min(3.0, args.cpu_seconds), rows=256,
+                                  threads=1)
+            cpu["value_1_thread"] = one["value"]
+            cpu["sample_1_thread"] = one["sample"]
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,

@@ -33,3 +33,12 @@ def test_reference_arm_prints_one_contract_line():
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_cpu_baseline_rate_on_one_thread_and_all():
+    p = bench.DEFAULT_WORKLOAD
+    for threads in (1, None):
+        r = bench.cpu_oracle_rate(p, p.ms, budget_s=0.2, rows=64, threads=threads)
+        assert r["value"] > 0 and r["unit"] == "GB/s" and r["kind"] == "oracle"
+        assert r["cores"] == (threads or bench.host_cores())
+        assert "64 of 2624 rows" in r["sample"]
