@@ -75,11 +75,42 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def strip_c_comments(src: str) -> str:
+    """C/C++/CUDA source without its // and /* */ comments (string and
+    character literals kept as they are): what the compiler sees."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def gemv_source_sha() -> str:
+    """A hash of the GEMV kernels' source code, comments excluded: a recorded
+    DRAM traffic figure stays valid while the compiled kernels cannot have
+    changed."""
     h = hashlib.sha256()
     for f in ("w8_gemv.cu", "w8_tc.cu", "w8_device.cuh", "w8_layout.h", "w8_internal.h"):
-        with open(os.path.join(ROOT, "fp8_weight_only_w8a16_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "fp8_weight_only_w8a16_gb300", "csrc", f)) as fh:
+            code = strip_c_comments(fh.read())
+        # code lines only: trailing blanks and lines left empty do not count
+        lines = [ln.rstrip() for ln in code.splitlines()]
+        h.update("\n".join(ln for ln in lines if ln).encode())
     return h.hexdigest()[:16]
 
 

@@ -68,7 +68,8 @@ __device__ __forceinline__ int out_col(int p, bool gated, int half)
 // SiLU-and-multiply of one gate/up pair, from the scaled fp32 row sums: g
 // and u are rounded to bf16 first (the projection's outputs), then
 // h = bf16(silu(g) * u) with silu(g) = g / (1 + exp(-g)) in fp32 (CUDA's
-// expf and a correctly rounded division: no fast-math in this build).
+// expf and a correctly rounded division: the library is compiled without
+// fast-math).
 __device__ __forceinline__ uint16_t silu_mul_bf16(float g_sum, float u_sum)
 {
     const float g = __uint_as_float(uint32_t(to_bf16(g_sum)) << 16);

@@ -42,3 +42,12 @@ def test_cpu_baseline_rate_on_one_thread_and_all():
         assert r["value"] > 0 and r["unit"] == "GB/s" and r["kind"] == "oracle"
         assert r["cores"] == (threads or bench.host_cores())
         assert "64 of 2624 rows" in r["sample"]
+
+
+def test_source_hash_sees_code_not_comments():
+    src = ('#define A 1\nint f(int x) { return x + A; } // add\n/* block\ncomment */\n'
+           'const char *s = "// not a comment /* either */";\n')
+    code = bench.strip_c_comments(src)
+    assert "// add" not in code and "block" not in code
+    assert '"// not a comment /* either */"' in code and "#define A 1\n" in code
+    assert bench.strip_c_comments("char c = '/'; // x\n") == "char c = '/'; \n"
