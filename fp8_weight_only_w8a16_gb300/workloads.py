@@ -13,7 +13,7 @@ W is [N, K]: N output rows, K reduction columns, K contiguous in memory.
 """
 from __future__ import annotations
 
-from dataclasses import dataclass, field
+from dataclasses import dataclass
 
 
 @dataclass(frozen=True)

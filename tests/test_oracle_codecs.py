@@ -14,7 +14,6 @@ import os
 from fractions import Fraction
 
 import numpy as np
-import pytest
 import torch
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "e4m3_special_codes.txt")
