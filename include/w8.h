@@ -13,6 +13,10 @@
  * are summed in fp32, and the row's factor is applied to that finished sum
  * just before the one conversion to bf16.  A bf16 plane takes the same path
  * with no factor at all (the PR keeps bf16 weights on their existing path).
+ * Three more plane kinds share the entry points' shape: block-scaled FP8
+ * (W8_DT_E4M3FN_B128, through w8_gemv), w4a16 MXFP4 (W8_DT_MXFP4,
+ * mxfp4_gemv) and merged gate_up planes whose call applies SiLU-and-multiply
+ * (W8_SRC_GATE_UP, w8_gemv_silu_mul); each is defined where it is declared.
  *
  * Conventions for every function below:
  *  - Pointers named "device" point into CUDA device memory of the device that
