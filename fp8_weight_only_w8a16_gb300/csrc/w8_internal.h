@@ -43,8 +43,6 @@ struct GemvArgs {
     float *partial;         // workspace body: [splits][rt*16][m] fp32 (splits > 1)
     int act;                // kActPlain, kActGateUp or kActSiluMul
     int half;               // gate_up planes: I = n / 2
-    int xg;                 // tc kernel: row blocks of a cluster that share the
-                            // activation tiles (TMA multicast); set by launch_tc
     const float *bfac;      // block-scaled FP8: the build's factors [ceil(n/128)][nbf]
     int nbf;                // block-scaled FP8: column blocks, ceil(k / 128)
 };

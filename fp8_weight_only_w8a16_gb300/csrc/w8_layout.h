@@ -148,7 +148,6 @@ struct Plan {
     int splits;
     int kbs_max;     // most K blocks one warp streams
     int grid;
-    int xg;          // tc: row blocks per cluster sharing the activation tiles (else 1)
     int smem;        // dynamic shared memory bytes (the K-part reduction)
     size_t ws_counters; // bytes of the counter head of the workspace
     size_t ws_bytes;    // total workspace bytes (0 when splits == 1)
@@ -272,7 +271,6 @@ W8_HD constexpr int tc_smem_bytes(bool fp8, int npad)
            tc_stages(fp8, npad).nb * 4 * npad * 64;
 }
 constexpr int kTcMaxSplits = 8;  // CTAs per cluster (the portable cluster size)
-constexpr int kTcMaxXg = 2;      // row blocks sharing one activation tile
 
 inline Plan make_tc_plan(int64_t n, int64_t k, int m, int sm_count)
 {
@@ -299,14 +297,6 @@ inline Plan make_tc_plan(int64_t n, int64_t k, int m, int sm_count)
            p.kb / (int64_t(splits) * 2) >= kTcStageBlocks)
         splits *= 2;
     p.splits = splits;
-    // from 48 tokens on, adjacent row blocks of one K range join the cluster
-    // and share each activation tile (as many bytes per CTA as its weights at
-    // 64 tokens): each CTA loads 1/xg of it and multicasts it to the others.
-    // Measured: q_b 64 tokens 18.6 -> 16.7 us; at 32 tokens within +-5 %.
-    int xg = 1;
-    while (p.npad >= 48 && xg < kTcMaxXg && splits * xg * 2 <= kTcMaxSplits && rbs % (xg * 2) == 0)
-        xg *= 2;
-    p.xg = xg;
     p.row_groups = int(rbs);
     p.grid = int(rbs * splits);
     p.kbs_max = int(ceil_div(p.kb, splits));
@@ -401,7 +391,6 @@ inline Plan make_ring_plan(int64_t n, int64_t k, int m, int sm_count, bool b128 
     p.splits = splits;
     p.row_groups = int(ceil_div(p.rt, int64_t(kWarps / p.wk) * p.r));
     p.grid = p.row_groups * p.splits;
-    p.xg = 1;
     p.kbs_max = int(ceil_div(ceil_div(p.kb, p.splits), p.wk));
     p.smem = kWarps * p.r * p.nt * 4 * 32 * int(sizeof(float));
     if (p.splits > 1) {

@@ -176,19 +176,6 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
                      smem_u32(bar))
                  : "memory");
 }
-// The same arrival on the barrier at this offset in every CTA of `mask`
-// (cluster ranks) of the cluster.
-__device__ __forceinline__ void umma_commit_mc(uint64_t *bar, uint16_t mask)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-                 "[%0], %1;" ::"r"(smem_u32(bar)),
-                 "h"(mask)
-                 : "memory");
-}
-__device__ __forceinline__ void cluster_sync_all()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
 {
@@ -219,17 +206,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
                  "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
                  : "memory");
 }
-// The same box written at this shared-memory offset in every CTA of `mask`
-// (cluster ranks), each CTA's barrier at `bar`'s offset counting the bytes.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *map, int c0, int c1,
-                                               uint64_t *bar, uint16_t mask)
-{
-    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
-                 "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-                 "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(mask)
-                 : "memory");
-}
-
 // The A operand of a whole stage (4 blocks = 64 columns) for 16 rows:
 // tcgen05.st 16x256b.x8, registers 8j..8j+7 = block j in tm_store_a's order.
 __device__ __forceinline__ void tm_store_stage(uint32_t taddr, const uint32_t (&r)[32])
@@ -279,10 +255,10 @@ __device__ __forceinline__ void a_units(uint32_t *r, uint32_t run, int g, int t)
 }
 
 // The fp32 sums of one row's four tokens over the splits of a row block
-// (cluster ranks rank0 .. rank0 + splits - 1): every split CTA's tile at the
-// same shared-memory offset, loaded first (all independent), then added in
-// split order.
-__device__ __forceinline__ float4 cluster_sum4(uint32_t off, int splits, int rank0)
+// (cluster ranks 0 .. splits - 1): every split CTA's tile at the same
+// shared-memory offset, loaded first (all independent), then added in split
+// order.
+__device__ __forceinline__ float4 cluster_sum4(uint32_t off, int splits)
 {
     float4 p[kTcMaxSplits];
 #pragma unroll
@@ -290,7 +266,7 @@ __device__ __forceinline__ float4 cluster_sum4(uint32_t off, int splits, int ran
         p[r] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (r < splits) {
             uint32_t remote;
-            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(off), "r"(rank0 + r));
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(off), "r"(r));
             asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
                          : "=f"(p[r].x), "=f"(p[r].y), "=f"(p[r].z), "=f"(p[r].w)
                          : "r"(remote)
@@ -346,17 +322,9 @@ __global__ void __launch_bounds__(kTcThreads, tc_occ(NPAD))
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // A cluster holds xg adjacent row blocks x splits K ranges; cluster rank
-    // g * splits + sp is row block g of the cluster, K range sp.
-    const int csz = a.splits * a.xg;
-    const int crank = int(blockIdx.x) % csz;
-    const int g = crank / a.splits;                     // row block within the cluster
-    const int sp = crank - g * a.splits;                // K range (split)
-    const int rb = (int(blockIdx.x) / csz) * a.xg + g;  // row block: rows rb*128 ..
-    // the CTAs that share this CTA's activation tiles (same K range)
-    uint16_t xmask = 0;
-    for (int q = 0; q < a.xg; ++q)
-        xmask = uint16_t(xmask | (1u << (q * a.splits + sp)));
+    // The splits of a row block form one cluster: cluster rank = K range.
+    const int sp = int(blockIdx.x) % a.splits;          // K range (split)
+    const int rb = int(blockIdx.x) / a.splits;          // row block: rows rb*128 ..
     const int cb0 = int((int64_t(sp) * a.kb) / a.splits); // this CTA's K blocks
     const int cnb = int((int64_t(sp + 1) * a.kb) / a.splits) - cb0;
     const int nst = (cnb + kTcKs - 1) / kTcKs;          // stages
@@ -376,7 +344,7 @@ __global__ void __launch_bounds__(kTcThreads, tc_occ(NPAD))
         }
         for (int s = 0; s < kNB; ++s) {
             mbar_init(&bar_full_b[s], 1);
-            mbar_init(&bar_empty_b[s], uint32_t(a.xg)); // every sharer's tensor steps
+            mbar_init(&bar_empty_b[s], 1);
         }
         mbar_init(&bar_done, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -391,10 +359,6 @@ __global__ void __launch_bounds__(kTcThreads, tc_occ(NPAD))
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // sharers write into each other's activation stages and barriers: every
-    // CTA of the cluster has initialised its barriers before any of that
-    if (a.xg > 1)
-        cluster_sync_all();
     const uint32_t tbase = s_tmem;
     pdl_launch_dependents();
 
@@ -466,10 +430,7 @@ __global__ void __launch_bounds__(kTcThreads, tc_occ(NPAD))
     } else if (warp == kWarpAct) {
         // ---- activations: x -> B tiles in shared memory (tensor-map copies) -----
         // Lane 4j + k copies K group k of block j of the stage (16 copies in
-        // parallel), each an 8-column x NPAD-row box.  With xg sharers, this
-        // CTA copies the boxes of lanes g, g + xg, ... into every sharer (a
-        // stage slot is refilled once all sharers' tensor steps are done with
-        // it), and its barrier expects the whole stage from all of them.
+        // parallel), each an 8-column x NPAD-row box.
         pdl_wait(); // x may be the previous kernel's output
         bool ok = true;
         for (int st = 0; st < nst && ok; ++st) {
@@ -483,13 +444,10 @@ __global__ void __launch_bounds__(kTcThreads, tc_occ(NPAD))
                 mbar_expect_tx(&bar_full_b[s], uint32_t(nb * kBlockB));
             __syncwarp();
             const int j = lane >> 2, kg = lane & 3;
-            if (j < nb && lane % a.xg == g) {
+            if (j < nb) {
                 const uint32_t dst = smem_u32(s_b + s * kStageB + j * kBlockB + kg * NPAD * 16);
                 const int c0 = (cb0 + st * kTcKs + j) * kTileK + 8 * kg;
-                if (a.xg == 1)
-                    tma_load_2d(dst, &tmx, c0, 0, &bar_full_b[s]);
-                else
-                    tma_load_2d_mc(dst, &tmx, c0, 0, &bar_full_b[s], xmask);
+                tma_load_2d(dst, &tmx, c0, 0, &bar_full_b[s]);
             }
         }
         if (!ok && lane == 0)
@@ -529,10 +487,7 @@ __global__ void __launch_bounds__(kTcThreads, tc_occ(NPAD))
                                 uint32_t(st | j | q));
             }
             umma_commit(&bar_empty_a[sa_]);
-            if (a.xg == 1)
-                umma_commit(&bar_empty_b[sb]);
-            else
-                umma_commit_mc(&bar_empty_b[sb], xmask); // the slot is free in no sharer until all are done
+            umma_commit(&bar_empty_b[sb]);
         }
         umma_commit(&bar_done);
         if (!ok)
@@ -616,7 +571,7 @@ __global__ void __launch_bounds__(kTcThreads, tc_occ(NPAD))
             if (a.act == kActSiluMul && (rl & 8))
                 continue; // an up row: added with its gate row (rl - 8), whichever split has it
             const uint32_t off = red_local + uint32_t((rl * kRedPitch + 4 * q) * 4);
-            const float4 v = cluster_sum4(off, a.splits, g * a.splits);
+            const float4 v = cluster_sum4(off, a.splits);
             const float sc = kFp8 ? __ldg(a.scale + orow) : 1.0f;
             const float out[4] = {v.x, v.y, v.z, v.w};
             const int col = out_col(orow, a.act != kActPlain, a.half);
@@ -626,7 +581,7 @@ __global__ void __launch_bounds__(kTcThreads, tc_occ(NPAD))
                     if (4 * q + e < a.m)
                         a.y[int64_t(4 * q + e) * a.ldy + col] = to_bf16(kFp8 ? sc * out[e] : out[e]);
             } else {
-                const float4 vu = cluster_sum4(off + uint32_t(8 * kRedPitch * 4), a.splits, g * a.splits);
+                const float4 vu = cluster_sum4(off + uint32_t(8 * kRedPitch * 4), a.splits);
                 const float scu = kFp8 ? __ldg(a.scale + orow + 8) : 1.0f;
                 const float up[4] = {vu.x, vu.y, vu.z, vu.w};
 #pragma unroll
@@ -639,11 +594,6 @@ __global__ void __launch_bounds__(kTcThreads, tc_occ(NPAD))
         // no CTA leaves while another may still read its tile
         __syncwarp();
         asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-    }
-    if (a.splits == 1 && a.xg > 1) {
-        // no CTA leaves while a sharer may still signal its barriers
-        __syncwarp();
-        cluster_sync_all();
     }
 
     // ---- release tensor memory -------------------------------------------------
@@ -733,7 +683,6 @@ cudaError_t launch_tc(bool fp8, const Plan &plan, const GemvArgs &a, cudaStream_
     if (!encode_x_map(&tmx, a, plan.npad))
         return cudaErrorInvalidValue;
     GemvArgs aa = a;
-    aa.xg = plan.xg;
     void *args[] = {&aa, &tmx};
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(unsigned(plan.grid));
@@ -743,9 +692,8 @@ cudaError_t launch_tc(bool fp8, const Plan &plan, const GemvArgs &a, cudaStream_
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    // a cluster: the splits of xg adjacent row blocks (the splits exchange
-    // partial tiles, the row blocks share activation tiles)
-    const int csz = plan.splits * plan.xg;
+    // a cluster: the splits of one row block (they exchange partial tiles)
+    const int csz = plan.splits;
     attr[1].id = cudaLaunchAttributeClusterDimension;
     attr[1].val.clusterDim.x = unsigned(csz);
     attr[1].val.clusterDim.y = 1;

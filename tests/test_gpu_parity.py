@@ -354,10 +354,8 @@ def test_workspace_reuse_graph_replay_and_errors(w8):
                                    (6144, 2048, 33)])
 def test_tensor_memory_kernel_clusters_and_graph_replay(w8, n, k, m):
     """Planes of >= 48 row blocks with >= 17 tokens run the tensor-memory
-    kernel; with split K its CTAs form a cluster and add their partial tiles on
-    chip, and from 48 tokens on two adjacent row blocks of a cluster share each
-    activation tile by multicast (clusters of up to 8: 4 splits x 2 row
-    blocks; 28672 rows: 2 row blocks, no split).  Repeated calls and a
+    kernel; with split K its CTAs form a cluster (up to 8 splits) and add
+    their partial tiles on chip (28672 rows: no split).  Repeated calls and a
     CUDA-graph replay give identical bits, within tolerance, and every bounded
     wait of the kernel ended normally (device status 0)."""
     plane, x_all = _case(45, n, k, m)
