@@ -16,8 +16,10 @@
 // the first call on each device looks up the real address with
 // cudaGetSymbolAddress, with that device current, zeroes the array (its head
 // holds the arrival counters, which every call leaves at zero again) and
-// caches the address.  That first call therefore synchronises the device and
-// must come before any stream capture.  All calls on a device share the array:
+// caches the address -- every first call on a device does this, whether or
+// not its own plan needs the scratch, so which call pays for it never depends
+// on the shape.  That first call therefore synchronises the device and must
+// come before any stream capture.  All calls on a device share the array:
 // calls that overlap on the GPU (different streams without ordering) race on
 // it and must not be issued.
 #include <cuda_runtime.h>
@@ -85,6 +87,11 @@ extern "C" w8_status w8_gemv_noalloc(const w8_build *b, int plane, const uint16_
         return W8_ERR_CUDA;
     if (dev != b->device)
         return W8_ERR_DEVICE;
+    // the first call on this device sets the scratch up, whatever its plan
+    void *ws = nullptr;
+    const w8_status st = scratch_on(dev, &ws);
+    if (st != W8_OK)
+        return st;
 
     const w8::Plan plan = w8::make_plan(p.n, p.k, m, b->sm_count);
     if (plan.ws_bytes > kScratchBytes)
@@ -105,10 +112,6 @@ extern "C" w8_status w8_gemv_noalloc(const w8_build *b, int plane, const uint16_
     a.wk = plan.wk;
     w8::set_output_map(a, p, false);
     if (plan.ws_bytes > 0) {
-        void *ws = nullptr;
-        const w8_status st = scratch_on(dev, &ws);
-        if (st != W8_OK)
-            return st;
         a.counters = static_cast<int *>(ws);
         a.partial = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + plan.ws_counters);
     }

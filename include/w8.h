@@ -345,21 +345,24 @@ w8_status mxfp4_gemv(const w8_build *b, int plane, const uint16_t *x, int64_t ld
  * while it records or replays a step) and so cannot provide the workspace
  * w8_gemv asks for when a plan splits K across CTAs.
  *
- * Same arguments and result as w8_gemv without the workspace: the scratch
+ * It serves row-scaled FP8 builds (W8_DT_E4M3FN) only, plain or gate_up
+ * planes; on such a build it takes w8_gemv's arguments without the workspace
+ * and gives w8_gemv's result.  Every other build (bf16, block-scaled FP8,
+ * MXFP4) returns W8_ERR_DTYPE.  The scratch
  * comes from a fixed array of W8_NOALLOC_SCRATCH_BYTES (32 KiB) inside the
  * library, which every GPU that loads the library holds until the process
  * exits.  A call whose plan needs more (w8_plan_info's workspace_bytes)
  * returns W8_ERR_SCRATCH before any launch.  It allocates nothing: no
  * cudaMalloc, no cudaFree, no allocating library routine.
  *
- * The first call on each device that needs the scratch sets it up: with that
- * device current it looks up the array's device address and zeroes the array,
- * which synchronises the device, so that first call must come before any
- * stream capture.  Every call leaves the array's counters at zero again.  All
- * calls on a device share the one array, so calls that could overlap on the
- * GPU (different streams without ordering between them) race and must not be
- * made; calls on one stream are fine.  Returns W8_ERR_DTYPE on a bf16 build.
- * One kernel launch on s. */
+ * The first call on each device sets the array up, whatever the shape of
+ * that call: with that device current it looks up the array's device address
+ * and zeroes the array, which synchronises the device, so that first call
+ * must come before any stream capture.  Every call leaves the array's
+ * counters at zero again.  All calls on a device share the one array, so
+ * calls that could overlap on the GPU (different streams without ordering
+ * between them) race and must not be made; calls in order on one stream are
+ * fine, with no synchronisation between them.  One kernel launch on s. */
 #define W8_NOALLOC_SCRATCH_BYTES (32u << 10)
 w8_status w8_gemv_noalloc(const w8_build *b, int plane, const uint16_t *x, int64_t ldx, int m,
                           uint16_t *y, int64_t ldy, w8_stream s);
