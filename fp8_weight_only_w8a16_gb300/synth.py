@@ -167,3 +167,23 @@ def workload(n: int, k: int, dtype: str = "e4m3fn", seed: int = 0, ldw: int | No
     plane = weight_plane(rng, n, k, dtype, ldw)
     x = activations(rng, k, x_rows)
     return plane, x
+
+
+def plane_rows(n: int, k: int, dtype: str = "e4m3fn", seed: int = 0, rows: int | None = None,
+               ldw: int | None = None) -> Plane:
+    """The first `rows` rows (all when None) of the [n, k] plane that
+    ``weight_plane(default_rng(seed), n, k, dtype, ldw)`` draws.  The draw
+    fills row-major and every supported format quantises each row on its own,
+    so a prefix of rows is exactly those rows of the whole plane (block-scaled
+    planes only in whole 128-row blocks)."""
+    rows = n if rows is None else min(rows, n)
+    if dtype == "e4m3fn_b128":
+        assert rows == n or rows % 128 == 0, "block-scaled planes: whole row blocks"
+    return weight_plane(np.random.default_rng(seed), rows, k, dtype, ldw)
+
+
+def tokens(k: int, rows: int, seed: int = 0) -> np.ndarray:
+    """[rows, k] bf16 bits ~ N(0, 1) drawn from their own stream
+    (``default_rng([seed, 1])``), so that they do not depend on a plane's
+    draw: the bench's decode tokens."""
+    return activations(np.random.default_rng([seed, 1]), k, rows)

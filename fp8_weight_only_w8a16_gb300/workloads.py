@@ -102,6 +102,13 @@ ALL = (TINY, FUSED_QKV_A, O_PROJ, O_PROJ_BF16, SHARED_GATE_UP, SHARED_DOWN,
        FUSED_QKV_A_B128, O_PROJ_B128)
 BY_NAME = {p.name: p for p in ALL}
 
+# The bench's step, one call per plane and token count: o_proj as an FP8 and
+# as a bf16 plane at M in {1, 2, 8, 32}; the GLM-5.2 layer sweep -- q_b, kv_b,
+# the indexer's wq_b, and its wk and weights_proj bound as one [160, 6144]
+# bf16 plane (both read the hidden states; one call gives both outputs) -- at
+# M in {1, 2, 4, 8, 16, 32, 64}; and the bf16 lm_head at M = 1.
+BENCH_STEP = (O_PROJ, O_PROJ_BF16, Q_B, KV_B, WQ_B, WK_WEIGHTS_PROJ, LM_HEAD)
+
 # The workload groups, in order: the tiny correctness case, the fused
 # qkv_a projection, o_proj (FP8 and bf16), the shared-expert pair with its
 # K-padded variant and its gate_up with SiLU-and-multiply, the full-layer

@@ -26,7 +26,11 @@ def test_reference_arm_prints_one_contract_line():
     assert d["metric"] == bench.METRIC and d["unit"] == "GB/s" and d["higher_is_better"] is True
     assert d["value"] > 0 and d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 0
     assert d["ms_per_step"] > 0 and d["scaling"] == "weak" and d["vs_baseline"] is None
-    assert d["config"]["workload"].startswith("fused_qkv_a_proj")
+    assert d["config"] == bench.bench_config()  # the GPU arm prints the same config
+    assert d["config"]["calls_per_step"] == 37
+    for name in ("o_proj", "o_proj_bf16", "q_b_proj", "kv_b_proj", "indexer_wq_b",
+                 "indexer_wk_weights_proj", "lm_head"):
+        assert name in d["config"]["workload"]
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
     assert cb["unit"] == d["unit"] and cb["sample"]
@@ -36,12 +40,35 @@ def test_reference_arm_prints_one_contract_line():
 
 
 def test_cpu_baseline_rate_on_one_thread_and_all():
-    p = bench.DEFAULT_WORKLOAD
     for threads in (1, None):
-        r = bench.cpu_oracle_rate(p, p.ms, budget_s=0.2, rows=64, threads=threads)
+        r = bench.cpu_oracle_rate(bench.STEP, budget_s=0.2, threads=threads, frac=0.0)
         assert r["value"] > 0 and r["unit"] == "GB/s" and r["kind"] == "oracle"
         assert r["cores"] == (threads or bench.host_cores())
-        assert "64 of 2624 rows" in r["sample"]
+        assert "112 rows in all" in r["sample"]  # 16 rows of each of the 7 planes
+
+
+def test_step_is_the_layer_sweep_and_o_proj():
+    calls = bench.step_calls()
+    assert len(calls) == 37
+    names = {p.name for p, _, _ in calls}
+    assert names == {"o_proj", "o_proj_bf16", "q_b_proj", "kv_b_proj", "indexer_wq_b",
+                     "indexer_wk_weights_proj", "lm_head"}
+    ms = {(p.name, m) for p, _, m in calls}
+    assert ("lm_head", 1) in ms and ("o_proj", 32) in ms and ("q_b_proj", 64) in ms
+    # algorithmic bytes: W (+ fp32 row scales) + x + y with the logical K
+    o = next(p for p, _, _ in calls if p.name == "o_proj")
+    assert o.algorithmic_bytes(8) == 6144 * 16384 + 4 * 6144 + 2 * 8 * 16384 + 2 * 8 * 6144
+    assert bench.step_bytes() == sum(p.algorithmic_bytes(m) for p, _, m in calls)
+
+
+def test_oracle_sample_rows_are_the_planes_first_rows():
+    import numpy as np
+    from fp8_weight_only_w8a16_gb300 import synth
+
+    p = bench.STEP[2]  # q_b_proj, FP8
+    full = synth.plane_rows(p.n, 64, p.dtype, seed=2)  # a narrower plane: same row rule
+    head = synth.plane_rows(p.n, 64, p.dtype, seed=2, rows=40)
+    assert np.array_equal(full.w[:40], head.w) and np.array_equal(full.scale[:40], head.scale)
 
 
 def test_source_hash_sees_code_not_comments():
