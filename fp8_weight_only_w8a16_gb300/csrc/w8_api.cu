@@ -169,10 +169,12 @@ w8_status gemv_common(const w8_build *b, int plane, int32_t want_dtype, bool sil
             return W8_ERR_NULL;
         if (reinterpret_cast<uintptr_t>(ws) & 255u)
             return W8_ERR_ALIGN;
-        if (ws_bytes < plan.ws_bytes)
+        if (ws_bytes < build_ws_bytes(b, plan.ws_bytes, plan.ws_counters))
             return W8_ERR_CAPACITY;
+        // the counters at the head, in the same place for every plan of the
+        // build (each call leaves them zero); the partial sums after them
         a.counters = static_cast<int *>(ws);
-        a.partial = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + plan.ws_counters);
+        a.partial = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + b->ws_counters);
     }
     if (w8::launch_gemv(kernel_dt(p.dtype), plan, a, reinterpret_cast<cudaStream_t>(s)) !=
         cudaSuccess)
@@ -287,6 +289,11 @@ w8_status w8_bind(const w8_plane_desc *d, int n_planes, void *dst, size_t dst_by
     b->device = dev;
     b->sm_count = sms;
     b->dtype = d[0].dtype;
+    b->ws_counters = 0;
+    for (int i = 0; i < n_planes; ++i) {
+        const size_t c = w8::align256(size_t(w8::ceil_div(d[i].n, w8::kTileN)) * sizeof(int));
+        b->ws_counters = c > b->ws_counters ? c : b->ws_counters;
+    }
     uint8_t *cursor = static_cast<uint8_t *>(dst);
     for (int i = 0; i < n_planes; ++i) {
         const w8_plane_desc &pd = d[i];
@@ -444,6 +451,8 @@ w8_status w8_plan_info(const w8_build *b, int plane, int m, w8_plan *out)
     if (m < 1 || m > max_m(p.dtype))
         return W8_ERR_SHAPE;
     fill_plan_dt(p.dtype, p.n, p.k, m, b->sm_count, out);
+    const w8::Plan pl = plan_for(p.dtype, p.n, p.k, m, b->sm_count);
+    out->workspace_bytes = build_ws_bytes(b, pl.ws_bytes, pl.ws_counters);
     return W8_OK;
 }
 
@@ -462,7 +471,8 @@ w8_status w8_workspace_bytes(const w8_build *b, int plane, int m, size_t *bytes)
         const w8_plane_info &p = b->planes[size_t(pi)];
         const int m0 = m == 0 ? 1 : m, m1 = m == 0 ? max_m(p.dtype) : m;
         for (int mm = m0; mm <= m1 && mm <= max_m(p.dtype); ++mm) {
-            const size_t ws = plan_for(p.dtype, p.n, p.k, mm, b->sm_count).ws_bytes;
+            const w8::Plan pl = plan_for(p.dtype, p.n, p.k, mm, b->sm_count);
+            const size_t ws = build_ws_bytes(b, pl.ws_bytes, pl.ws_counters);
             if (ws > best)
                 best = ws;
         }

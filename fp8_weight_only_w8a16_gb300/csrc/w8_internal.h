@@ -14,8 +14,17 @@ struct w8_build {
     int device;
     int sm_count;
     int32_t dtype;
+    size_t ws_counters; // the workspace's counter head for every call of the build:
+                        // one counter per row tile of its largest plane
     std::vector<w8_plane_info> planes;
 };
+
+// Workspace bytes a call with this plan needs on this build: the build's
+// counter head, then the plan's partial sums (0 when the plan needs none).
+inline size_t build_ws_bytes(const w8_build *b, size_t plan_ws_bytes, size_t plan_ws_counters)
+{
+    return plan_ws_bytes == 0 ? 0 : b->ws_counters + (plan_ws_bytes - plan_ws_counters);
+}
 
 namespace w8 {
 

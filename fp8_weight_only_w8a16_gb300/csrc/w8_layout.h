@@ -149,7 +149,9 @@ struct Plan {
     int kbs_max;     // most K blocks one warp streams
     int grid;
     int smem;        // dynamic shared memory bytes (the K-part reduction)
-    size_t ws_counters; // bytes of the counter head of the workspace
+    size_t ws_counters; // bytes of the counter head of the workspace: one counter
+                        // per row tile of the plane, whatever the plan, so that
+                        // every plan of a build finds its counters in one place
     size_t ws_bytes;    // total workspace bytes (0 when splits == 1)
 };
 
@@ -394,7 +396,7 @@ inline Plan make_ring_plan(int64_t n, int64_t k, int m, int sm_count, bool b128 
     p.kbs_max = int(ceil_div(ceil_div(p.kb, p.splits), p.wk));
     p.smem = kWarps * p.r * p.nt * 4 * 32 * int(sizeof(float));
     if (p.splits > 1) {
-        p.ws_counters = align256(size_t(p.row_groups) * sizeof(int));
+        p.ws_counters = align256(size_t(p.rt) * sizeof(int));
         p.ws_bytes = p.ws_counters + align256(size_t(p.splits) * size_t(p.rt) * kTileN *
                                               size_t(m) * sizeof(float));
     } else {

@@ -32,8 +32,12 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = size_t(32) << 10; // W8_NOALLOC_SCRATCH_BYTES
+constexpr size_t kScratchBytes = size_t(64) << 10; // W8_NOALLOC_SCRATCH_BYTES
 static_assert(kScratchBytes == W8_NOALLOC_SCRATCH_BYTES, "keep w8.h in step");
+// The arrival counters live in the first kCounterBytes of the array for every
+// call and every build (each call leaves them zero), the partial sums after:
+// a call's partials never land where another call's counters are.
+constexpr size_t kCounterBytes = size_t(4) << 10;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
@@ -94,7 +98,8 @@ extern "C" w8_status w8_gemv_noalloc(const w8_build *b, int plane, const uint16_
         return st;
 
     const w8::Plan plan = w8::make_plan(p.n, p.k, m, b->sm_count);
-    if (plan.ws_bytes > kScratchBytes)
+    if (plan.ws_bytes > 0 && (plan.ws_counters > kCounterBytes ||
+                              kCounterBytes + (plan.ws_bytes - plan.ws_counters) > kScratchBytes))
         return W8_ERR_SCRATCH;
     w8::GemvArgs a{};
     a.wp = static_cast<const uint8_t *>(p.packed);
@@ -113,7 +118,7 @@ extern "C" w8_status w8_gemv_noalloc(const w8_build *b, int plane, const uint16_
     w8::set_output_map(a, p, false);
     if (plan.ws_bytes > 0) {
         a.counters = static_cast<int *>(ws);
-        a.partial = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + plan.ws_counters);
+        a.partial = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kCounterBytes);
     }
     if (w8::launch_gemv(w8::kDtFp8, plan, a, reinterpret_cast<cudaStream_t>(s)) != cudaSuccess)
         return W8_ERR_CUDA;

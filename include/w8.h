@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define W8_ABI_VERSION 5
+#define W8_ABI_VERSION 6
 
 /* A cudaStream_t: the runtime's stream type is this same pointer type. */
 typedef struct CUstream_st *w8_stream;
@@ -274,9 +274,11 @@ w8_status w8_plan_shape_dtype(int64_t n, int64_t k, int m, int sm_count, int32_t
  * m = 1..256, so one workspace can serve every call of a build.
  *
  * Workspace contract: 256-byte aligned device memory, zero-filled once by the
- * caller before its first use (its head holds arrival counters that every
- * call leaves at zero again).  Calls that share a workspace must not overlap
- * on the GPU: order them on one stream or synchronise between them. */
+ * caller before its first use.  Its head holds one arrival counter per row
+ * tile of the build's largest plane, in the same place for every call of the
+ * build, and every call leaves them at zero again; the partial sums follow.
+ * Calls that share a workspace must not overlap on the GPU: order them on one
+ * stream or synchronise between them. */
 w8_status w8_workspace_bytes(const w8_build *b, int plane, int m, size_t *bytes);
 
 /* The FP8 (w8a16) GEMV on an E4M3FN build:
@@ -349,10 +351,12 @@ w8_status mxfp4_gemv(const w8_build *b, int plane, const uint16_t *x, int64_t ld
  * planes; on such a build it takes w8_gemv's arguments without the workspace
  * and gives w8_gemv's result.  Every other build (bf16, block-scaled FP8,
  * MXFP4) returns W8_ERR_DTYPE.  The scratch
- * comes from a fixed array of W8_NOALLOC_SCRATCH_BYTES (32 KiB) inside the
+ * comes from a fixed array of W8_NOALLOC_SCRATCH_BYTES (64 KiB) inside the
  * library, which every GPU that loads the library holds until the process
- * exits.  A call whose plan needs more (w8_plan_info's workspace_bytes)
- * returns W8_ERR_SCRATCH before any launch.  It allocates nothing: no
+ * exits: its first 4 KiB hold the arrival counters (one per row tile) of
+ * every call and every build, the rest the partial sums.  A call whose plan
+ * needs more (more than 1024 row tiles with K split, or partial sums past the
+ * array's end) returns W8_ERR_SCRATCH before any launch.  It allocates nothing: no
  * cudaMalloc, no cudaFree, no allocating library routine.
  *
  * The first call on each device sets the array up, whatever the shape of
@@ -363,7 +367,7 @@ w8_status mxfp4_gemv(const w8_build *b, int plane, const uint16_t *x, int64_t ld
  * calls that could overlap on the GPU (different streams without ordering
  * between them) race and must not be made; calls in order on one stream are
  * fine, with no synchronisation between them.  One kernel launch on s. */
-#define W8_NOALLOC_SCRATCH_BYTES (32u << 10)
+#define W8_NOALLOC_SCRATCH_BYTES (64u << 10)
 w8_status w8_gemv_noalloc(const w8_build *b, int plane, const uint16_t *x, int64_t ldx, int m,
                           uint16_t *y, int64_t ldy, w8_stream s);
 

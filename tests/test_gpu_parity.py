@@ -558,3 +558,32 @@ def test_large_token_counts_graph_replay(w8):
     torch.cuda.synchronize()
     assert np.array_equal(from_dev(yd), y1)
     assert w8.device_status() == 0
+
+
+def test_one_workspace_across_planes_of_a_build(w8):
+    """Split-K calls on planes of different sizes in one build share one
+    workspace, back to back.  The counter head sits in the same place for
+    every call of the build, so one call's partial sums never land on another
+    call's arrival counters: here the second plane (1040 rows, 65 row groups
+    at one token) counts past the 64 counters that fill the first 256 bytes,
+    where the first plane's partial sums would otherwise start."""
+    rng = np.random.default_rng(92)
+    shapes = [(128, 6144), (1040, 2048)]
+    planes = [synth.weight_plane(rng, n, k) for n, k in shapes]
+    b = w8.bind([w8.Plane.from_tensor(to_dev(p.w), to_dev(p.scale)) for p in planes])
+    ws = b.new_workspace()
+    calls = [(0, 8), (1, 1), (0, 24), (1, 1), (1, 8), (0, 1)]
+    p1 = b.plan(1, 1)
+    assert p1.kernel == 0 and p1.splits > 1 and p1.row_groups > 64
+    assert all(b.plan(i, m).splits > 1 for i, m in calls)
+    xs = {k: synth.activations(rng, k, 24) for k in (2048, 6144)}
+    outs = []
+    for i, m in calls:
+        n, k = shapes[i]
+        outs.append(run_gemv(w8, b, i, np.ascontiguousarray(xs[k][:m]), n, ws=ws))
+    for (i, m), y in zip(calls, outs):
+        n, k = shapes[i]
+        own, _src = bind_plane(w8, planes[i])
+        x = np.ascontiguousarray(xs[k][:m])
+        assert np.array_equal(y, run_gemv(w8, own, 0, x, n))
+        _check_tol(planes[i], x, y)

@@ -28,7 +28,7 @@ from .gpu_util import bind_plane, dev, from_dev, to_dev
 
 pytestmark = pytest.mark.gpu
 
-LIMIT = 32 << 10  # W8_NOALLOC_SCRATCH_BYTES
+LIMIT = 64 << 10  # W8_NOALLOC_SCRATCH_BYTES
 
 
 @pytest.fixture(scope="module")
