@@ -176,6 +176,22 @@ __device__ __forceinline__ void load_w(WFrag<kDt> &f, const uint8_t *p, int soff
 {
     load_w_pred<kDt>(f, p, soff, 1u);
 }
+// The same load with no predicate at all (the steady part of a stream).
+template <int kDt>
+__device__ __forceinline__ void load_w_now(WFrag<kDt> &f, const uint8_t *p, int soff)
+{
+    if constexpr (kDt == kDtFp8) {
+        f.v = ld_stream(p);
+    } else if constexpr (kDt == kDtBf16) {
+        f.v[0] = ld_stream(p);
+        f.v[1] = ld_stream(p + 512);
+    } else {
+        asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v2.u32 {%0,%1}, [%2];"
+                     : "=r"(f.v.x), "=r"(f.v.y)
+                     : "l"(p));
+        asm volatile("ld.global.nc.L1::no_allocate.L2::256B.u32 %0, [%1];" : "=r"(f.s) : "l"(p + soff));
+    }
+}
 
 template <int kDt>
 __device__ __forceinline__ void zero_w(WFrag<kDt> &f)

@@ -70,6 +70,14 @@ __device__ __forceinline__ void ld_act_pred(uint4 &v, const uint16_t *p, uint32_
                  : "l"(p), "r"(ok));
 }
 
+// The same load with no predicate (the steady part of the stream).
+__device__ __forceinline__ void ld_act(uint4 &v, const uint16_t *p)
+{
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+}
+
 // The activations of the K-tail block, element by element (zero past K).
 __device__ __forceinline__ uint4 load_x_tail(const uint16_t *p, bool ok, int64_t col, int64_t k)
 {
@@ -137,7 +145,7 @@ __device__ __forceinline__ void block_step(float (&acc)[R][NT][4], const WFrag<k
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int kDt, int NT, int R, int DW, int DX, int kMinBlocks>
+template <int kDt, int NT, int R, int DW, int DX, int kMinBlocks, bool kLong>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvArgs a)
 {
     static_assert(DW % DX == 0, "the activation ring depth divides the weight ring depth");
@@ -279,6 +287,35 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
     // predicated load) with the block DW (weights) or DX (activations)
     // further on.
     int b = 0;
+    if constexpr (kLong) {
+        // The kLong copies of the 1..16-token FP8 and one-group, one-tile
+        // MXFP4 instances, which the planner picks for K parts of at least four
+        // ring groups: while every refill of a group lies inside the K part
+        // (b + 2 DW <= nmain) the loads carry no predicate -- and activations
+        // of tokens past m, whose sums are never stored, read token 0's row
+        // instead of being masked; the last full group refills under
+        // predicates.  Measured: o_proj 18.4 -> 17.8 us, MXFP4 o_proj 19.8 ->
+        // 18.8 us at one token; compiled into the kernels of short K parts,
+        // the second body made those 3-4 % slower, hence the separate copies.
+        for (; b + 2 * DW <= nmain; b += DW) {
+            if (kPf > DW && lane == 0 && b + kPf < nmain) {
+                const int hi = b + kPf + DW < nmain ? b + kPf + DW : nmain;
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    prefetch_l2(wptr[r] + (b + kPf) * kRun, uint32_t(hi - b - kPf) * kRun);
+            }
+#pragma unroll
+            for (int i = 0; i < DW; ++i) {
+                block_step<kW, NT, R>(acc, wring[i], xring[i % DX]);
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    load_w_now<kW>(wring[i][r], wptr[r] + (b + DW + i) * kRun, soff);
+#pragma unroll
+                for (int j = 0; j < NT; ++j)
+                    ld_act(xring[i % DX][j], xptr[j] + (b + DX + i) * kTileK);
+            }
+        }
+    }
     for (; b + DW <= nmain; b += DW) {
         if constexpr (kB128)
             factor_window<R>(fac, fac_row, fbase, (kb0 + b) >> 2, (kb0 + b + DW - 1) >> 2, lane,
@@ -467,45 +504,56 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
 // instance table: one kernel per (dtype, NT, R, occupancy) with the depths of
 // w8_layout.h
 // ---------------------------------------------------------------------------
-template <int kDt, int NT, int R, int OCC>
+// Whether (dtype, token groups, row tiles per warp) has a kLong copy with
+// the steady body (the copies whose registers hold it without spills).
+constexpr bool has_long(int dt, int nt, int r)
+{
+    return nt <= 2 && (dt == kDtFp8 || (dt == kDtFp4 && nt == 1 && r == 1));
+}
+
+template <int kDt, int NT, int R, int OCC, bool kLong>
 void *inst()
 {
     constexpr int dw = depth_w_dt(NT, R, kDt, OCC), dx = depth_x_dt(NT, R, kDt, OCC);
     if constexpr (dw == 0) // a block-scaled instance that does not exist
         return nullptr;
+    else if constexpr (kLong && !has_long(kDt, NT, R))
+        return nullptr;
     else
-        return reinterpret_cast<void *>(&gemv_kernel<kDt, NT, R, dw, dx, OCC>);
+        return reinterpret_cast<void *>(&gemv_kernel<kDt, NT, R, dw, dx, OCC, kLong>);
 }
 
-template <int kDt, int I>
+template <int kDt, int I, bool kLong>
 void *inst_at()
 {
-    return inst<kDt, kInst[I].nt, kInst[I].r, kInst[I].occ>();
+    return inst<kDt, kInst[I].nt, kInst[I].r, kInst[I].occ, kLong>();
 }
 
-template <int kDt, int... Is>
+template <int kDt, bool kLong, int... Is>
 void *pick_from(int idx, std::integer_sequence<int, Is...>)
 {
     void *fn = nullptr;
-    ((fn = (idx == Is ? inst_at<kDt, Is>() : fn)), ...);
+    ((fn = (idx == Is ? inst_at<kDt, Is, kLong>() : fn)), ...);
     return fn;
 }
 
 template <int kDt>
-void *pick(int nt, int r, int occ)
+void *pick(int nt, int r, int occ, bool lng)
 {
     const int idx = inst_index(nt, r, occ);
     if (idx < 0)
         return nullptr;
-    return pick_from<kDt>(idx, std::make_integer_sequence<int, kNumInst>{});
+    if (lng && has_long(kDt, nt, r))
+        return pick_from<kDt, true>(idx, std::make_integer_sequence<int, kNumInst>{});
+    return pick_from<kDt, false>(idx, std::make_integer_sequence<int, kNumInst>{});
 }
 
-void *pick_dt(int dt, int nt, int r, int occ)
+void *pick_dt(int dt, int nt, int r, int occ, bool lng)
 {
-    return dt == kDtFp8    ? pick<kDtFp8>(nt, r, occ)
-           : dt == kDtFp4  ? pick<kDtFp4>(nt, r, occ)
-           : dt == kDtFp8B ? pick<kDtFp8B>(nt, r, occ)
-                           : pick<kDtBf16>(nt, r, occ);
+    return dt == kDtFp8    ? pick<kDtFp8>(nt, r, occ, lng)
+           : dt == kDtFp4  ? pick<kDtFp4>(nt, r, occ, lng)
+           : dt == kDtFp8B ? pick<kDtFp8B>(nt, r, occ, lng)
+                           : pick<kDtBf16>(nt, r, occ, lng);
 }
 
 } // namespace
@@ -515,13 +563,15 @@ cudaError_t prepare_gemv_kernels()
     // the K-part reduction buffer: 8 warps x R x NT x 128 floats, at most 64 KB
     for (int i = 0; i < kNumInst; ++i) {
         for (int dt : {kDtBf16, kDtFp8, kDtFp4, kDtFp8B}) {
-            void *fn = pick_dt(dt, kInst[i].nt, kInst[i].r, kInst[i].occ);
-            if (!fn)
-                continue;
-            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 64 * 1024);
-            if (e != cudaSuccess)
-                return e;
+            for (bool lng : {false, true}) {
+                void *fn = pick_dt(dt, kInst[i].nt, kInst[i].r, kInst[i].occ, lng);
+                if (!fn)
+                    continue;
+                cudaError_t e = cudaFuncSetAttribute(
+                    fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+                if (e != cudaSuccess)
+                    return e;
+            }
         }
     }
     return prepare_tc_kernels();
@@ -532,7 +582,7 @@ cudaError_t launch_gemv(int dt, const Plan &plan, const GemvArgs &a, cudaStream_
     if (plan.tc)
         return dt == kDtFp4 || dt == kDtFp8B ? cudaErrorInvalidValue
                                              : launch_tc(dt == kDtFp8, plan, a, s);
-    void *fn = pick_dt(dt, plan.nt, plan.r, plan.occ);
+    void *fn = pick_dt(dt, plan.nt, plan.r, plan.occ, plan.long_k);
     if (!fn)
         return cudaErrorInvalidValue;
     void *args[] = {const_cast<GemvArgs *>(&a)};

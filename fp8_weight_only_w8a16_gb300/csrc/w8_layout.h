@@ -147,6 +147,8 @@ struct Plan {
     int row_groups;
     int splits;
     int kbs_max;     // most K blocks one warp streams
+    bool long_k;     // ring: K parts of at least four ring groups (the kernel copy
+                     // with a predicate-free steady loop)
     int grid;
     int smem;        // dynamic shared memory bytes (the K-part reduction)
     size_t ws_counters; // bytes of the counter head of the workspace: one counter
@@ -394,6 +396,7 @@ inline Plan make_ring_plan(int64_t n, int64_t k, int m, int sm_count, bool b128 
     p.row_groups = int(ceil_div(p.rt, int64_t(kWarps / p.wk) * p.r));
     p.grid = p.row_groups * p.splits;
     p.kbs_max = int(ceil_div(ceil_div(p.kb, p.splits), p.wk));
+    p.long_k = p.kbs_max >= 4 * p.dw;
     p.smem = kWarps * p.r * p.nt * 4 * 32 * int(sizeof(float));
     if (p.splits > 1) {
         p.ws_counters = align256(size_t(p.rt) * sizeof(int));
