@@ -182,6 +182,23 @@ w8_status gemv_common(const w8_build *b, int plane, int32_t want_dtype, bool sil
     return W8_OK;
 }
 
+// The checks of a w8_mlp call on the two planes: a gate_up plane and a
+// row-major down plane whose K is the gate_up plane's I.
+w8_status mlp_check(const w8_build *b, int gate_up, int down, int m)
+{
+    if (!b)
+        return W8_ERR_NULL;
+    if (gate_up < 0 || gate_up >= int(b->planes.size()) || down < 0 ||
+        down >= int(b->planes.size()))
+        return W8_ERR_PLANE;
+    const w8_plane_info &u = b->planes[size_t(gate_up)], &d = b->planes[size_t(down)];
+    if (u.layout != W8_LAYOUT_MMA_16x32_GATE_UP || d.layout != W8_LAYOUT_MMA_16x32)
+        return W8_ERR_LAYOUT;
+    if (d.k != u.n / 2 || m < 0 || m > max_m(u.dtype))
+        return W8_ERR_SHAPE;
+    return W8_OK;
+}
+
 } // namespace
 
 extern "C" {
@@ -507,6 +524,52 @@ w8_status w8_gemv_silu_mul(const w8_build *b, int plane, const uint16_t *x, int6
                            w8_stream s)
 {
     return gemv_common(b, plane, 0, true, x, ldx, m, y, ldy, workspace, workspace_bytes, s);
+}
+
+w8_status w8_mlp_workspace_bytes(const w8_build *b, int gate_up, int down, int m, size_t *bytes)
+{
+    if (!bytes)
+        return W8_ERR_NULL;
+    const w8_status st = mlp_check(b, gate_up, down, m);
+    if (st != W8_OK)
+        return st;
+    size_t wu = 0, wd = 0;
+    w8_workspace_bytes(b, gate_up, m, &wu);
+    w8_workspace_bytes(b, down, m, &wd);
+    *bytes = wu > wd ? wu : wd;
+    return W8_OK;
+}
+
+w8_status w8_mlp(const w8_build *b, int gate_up, int down, const uint16_t *x, int64_t ldx, int m,
+                 uint16_t *h, int64_t ldh, uint16_t *y, int64_t ldy, void *workspace,
+                 size_t workspace_bytes, w8_stream s)
+{
+    w8_status st = mlp_check(b, gate_up, down, m);
+    if (st != W8_OK || m == 0)
+        return st;
+    // The down launch's host checks before the first launch is enqueued, so
+    // that a refused call enqueues nothing: h as its x (16-byte loads), y,
+    // and the workspace of either projection (x and the device are checked
+    // by the gate_up launch, before it is enqueued).
+    const w8_plane_info &pd = b->planes[size_t(down)];
+    if (!h || !y)
+        return W8_ERR_NULL;
+    if (ldh < pd.k || ldy < pd.n)
+        return W8_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(h) & 15u) || (ldh & 7) || (reinterpret_cast<uintptr_t>(y) & 1u))
+        return W8_ERR_ALIGN;
+    size_t need = 0;
+    w8_mlp_workspace_bytes(b, gate_up, down, m, &need);
+    if (need > 0 && !workspace)
+        return W8_ERR_NULL;
+    if (workspace_bytes < need)
+        return W8_ERR_CAPACITY;
+    st = gemv_common(b, gate_up, 0, true, x, ldx, m, h, ldh, workspace, workspace_bytes, s);
+    if (st != W8_OK)
+        return st;
+    // the down projection of h: it may begin streaming its weights while the
+    // gate_up kernel drains, and reads h once that kernel has completed
+    return gemv_common(b, down, 0, false, h, ldh, m, y, ldy, workspace, workspace_bytes, s);
 }
 
 int64_t w8_packed_offset(int dtype, int64_t k_blocks, int64_t row, int64_t col)

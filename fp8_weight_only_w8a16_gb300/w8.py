@@ -6,7 +6,7 @@ into exceptions.  PyTorch provides device memory and streams only.  There is
 no fallback: if libw8.so is missing, importing this module raises.
 
 Names follow the C ABI: ``validate``, ``packed_bytes``, ``bind`` (w8_bind),
-``w8_gemv``, ``bf16_gemv``, ``mxfp4_gemv``, ``w8_gemv_silu_mul``, ``workspace_bytes``,
+``w8_gemv``, ``bf16_gemv``, ``mxfp4_gemv``, ``w8_gemv_silu_mul``, ``w8_mlp``, ``workspace_bytes``,
 ``plan_info``, ``packed_offset``, ``gate_up_packed_row``.
 """
 from __future__ import annotations
@@ -26,7 +26,7 @@ DT_E4M3FN_B128 = 7  # FP8 codes with one fp32 factor per 128 x 128 block
 SRC_ROW_MAJOR, SRC_GATE_UP = 0, 1
 LAYOUT_MMA_16x32, LAYOUT_MMA_16x32_GATE_UP = 1, 2
 MAX_M = 256
-ABI_VERSION = 6  # W8_ABI_VERSION of include/w8.h (the structs below follow it)
+ABI_VERSION = 7  # W8_ABI_VERSION of include/w8.h (the structs below follow it)
 
 STATUS = {
     0: "W8_OK", 1: "W8_ERR_NULL", 2: "W8_ERR_DTYPE", 3: "W8_ERR_UNPADDED", 4: "W8_ERR_BIAS",
@@ -105,6 +105,10 @@ def _load():
         f.restype = st
     lib.w8_gemv_noalloc.argtypes = [vp, i32, vp, i64, i32, vp, i64, vp]
     lib.w8_gemv_noalloc.restype = st
+    lib.w8_mlp.argtypes = [vp, i32, i32, vp, i64, i32, vp, i64, vp, i64, vp, sz, vp]
+    lib.w8_mlp.restype = st
+    lib.w8_mlp_workspace_bytes.argtypes = [vp, i32, i32, i32, ctypes.POINTER(sz)]
+    lib.w8_mlp_workspace_bytes.restype = st
     lib.w8_packed_offset.argtypes = [i32, i64, i64, i64]
     lib.w8_packed_offset.restype = i64
     lib.w8_mxfp4_code_bits.argtypes = [i64, i64, i64, ctypes.POINTER(i64)]
@@ -126,7 +130,7 @@ EXPORTS = ("w8_status_str", "w8_abi_version", "w8_validate", "w8_packed_bytes", 
            "w8_release", "w8_build_planes", "w8_build_info", "w8_plan_info", "w8_plan_shape",
            "w8_plan_shape_dtype",
            "w8_workspace_bytes", "w8_gemv", "bf16_gemv", "w8_gemv_silu_mul", "mxfp4_gemv",
-           "w8_gemv_noalloc",
+           "w8_gemv_noalloc", "w8_mlp", "w8_mlp_workspace_bytes",
            "w8_packed_offset", "w8_mxfp4_code_bits", "w8_gate_up_packed_row", "w8_device_status")
 
 
@@ -270,6 +274,17 @@ class Build:
         nbytes = max(self.workspace_bytes(plane, m), 256)
         return torch.zeros(nbytes, dtype=torch.uint8, device=device or self.dst.device)
 
+    def mlp_workspace_bytes(self, gate_up: int, down: int, m: int = 0) -> int:
+        out = ctypes.c_size_t(0)
+        _check(lib.w8_mlp_workspace_bytes(self.handle, gate_up, down, m, ctypes.byref(out)))
+        return int(out.value)
+
+    def new_mlp_workspace(self, gate_up: int, down: int, m: int = 0, device=None) -> torch.Tensor:
+        """A zero-filled workspace for w8_mlp on (gate_up, down), large enough
+        for every gemv call of the build as well."""
+        nbytes = max(self.mlp_workspace_bytes(gate_up, down, m), self.workspace_bytes(), 256)
+        return torch.zeros(nbytes, dtype=torch.uint8, device=device or self.dst.device)
+
     def release(self):
         if self._h:
             lib.w8_release(self._h)
@@ -329,6 +344,23 @@ def w8_gemv_silu_mul(build: Build, plane: int, x: torch.Tensor, y: torch.Tensor,
                      workspace: torch.Tensor | None = None, m: int | None = None, stream=None):
     """y[:m, :I] = bf16(silu(g) * u) on a gate_up plane of either dtype (one kernel launch)."""
     return _gemv(lib.w8_gemv_silu_mul, build, plane, x, y, workspace, m, stream)
+
+
+def w8_mlp(build: Build, gate_up: int, down: int, x: torch.Tensor, h: torch.Tensor,
+           y: torch.Tensor, workspace: torch.Tensor | None = None, m: int | None = None,
+           stream=None):
+    """h[:m, :I] = silu(g) * u on the gate_up plane, then y[:m, :N] = the down
+    plane's GEMV on h (two kernel launches, the second dependent on the first)."""
+    for t in (x, h, y):
+        assert t.dim() == 2 and t.stride(1) == 1 and t.element_size() == 2
+    m = x.shape[0] if m is None else m
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.w8_mlp(build.handle, gate_up, down, ctypes.c_void_p(x.data_ptr()), x.stride(0), m,
+                      ctypes.c_void_p(h.data_ptr()), h.stride(0),
+                      ctypes.c_void_p(y.data_ptr()), y.stride(0),
+                      ctypes.c_void_p(ws_ptr), ws_bytes, _stream_ptr(stream)))
+    return y
 
 
 def plan_shape(n: int, k: int, m: int, sm_count: int) -> PlanInfo:

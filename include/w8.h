@@ -16,7 +16,9 @@
  * Three more plane kinds share the entry points' shape: block-scaled FP8
  * (W8_DT_E4M3FN_B128, through w8_gemv), w4a16 MXFP4 (W8_DT_MXFP4,
  * mxfp4_gemv) and merged gate_up planes whose call applies SiLU-and-multiply
- * (W8_SRC_GATE_UP, w8_gemv_silu_mul); each is defined where it is declared.
+ * (W8_SRC_GATE_UP, w8_gemv_silu_mul, and w8_mlp: gate_up, SiLU-and-multiply
+ * and the down projection in one call); each is defined where it is
+ * declared.
  *
  * Conventions for every function below:
  *  - Pointers named "device" point into CUDA device memory of the device that
@@ -32,7 +34,8 @@
  *    synchronise and launch exactly one kernel, with programmatic dependent
  *    launch: the kernel may begin streaming weights while the previous kernel
  *    of the stream drains, and reads activations and writes outputs only
- *    after that kernel has completed.  w8_bind runs its repack kernels on the
+ *    after that kernel has completed.  w8_mlp is asynchronous in the same
+ *    way and launches two such kernels, the second dependent on the first.  w8_bind runs its repack kernels on the
  *    caller's stream and synchronises that stream before it returns (load
  *    time; it must not be captured in a CUDA graph).
  *  - A stream argument is a cudaStream_t (NULL is the legacy default stream).
@@ -47,7 +50,7 @@
 extern "C" {
 #endif
 
-#define W8_ABI_VERSION 6
+#define W8_ABI_VERSION 7
 
 /* A cudaStream_t: the runtime's stream type is this same pointer type. */
 typedef struct CUstream_st *w8_stream;
@@ -338,6 +341,41 @@ w8_status w8_gemv_silu_mul(const w8_build *b, int plane, const uint16_t *x, int6
 w8_status mxfp4_gemv(const w8_build *b, int plane, const uint16_t *x, int64_t ldx, int m,
                      uint16_t *y, int64_t ldy, void *workspace, size_t workspace_bytes,
                      w8_stream s);
+
+/* The MLP block in one call (ATOM Model Support Guide, Model architecture
+ * details, Llama MLP: the merged gate and up projection, SiLU-and-multiply,
+ * then the down projection), on two planes of one build:
+ *   gate_up: bound as W8_SRC_GATE_UP, [2I, K];  down: row-major, [N, I];
+ *   h[i*ldh + j] = w8_gemv_silu_mul's output on gate_up and x,  j < I,
+ *   y[i*ldy + n] = the gemv's output on down and h,            n < N,
+ * for 0 <= i < m, on any build that can hold a gate_up plane (E4M3FN, BF16,
+ * MXFP4; the gemv of the build's dtype).  Exactly the two calls in sequence,
+ * bit for bit.
+ * x: device bf16 [m][ldx], ldx >= K, ldx % 8 == 0, 16-byte aligned;
+ * h: device bf16 [m][ldh], ldh >= I, ldh % 8 == 0, 16-byte aligned (the down
+ *    projection reads it as its x), written for j < I only;
+ * y: device bf16 [m][ldy], ldy >= N, written for n < N only;
+ * x, h and y must not overlap.  m: as the build's gemv (0 is a no-op);
+ * W8_ERR_SHAPE above, or when down's K is not I.
+ * workspace: w8_mlp_workspace_bytes bytes (0 when neither plan splits K),
+ *    the contract of w8_workspace_bytes.
+ * W8_ERR_LAYOUT when gate_up is not a gate_up plane or down is one.  Every
+ * check of both launches is made before the first is enqueued.
+ * Two kernel launches on s: gate_up with SiLU-and-multiply into h, then the
+ * down projection, which may stream its weights while the first drains
+ * (programmatic dependent launch) and reads h once it has completed.  (A
+ * single kernel for both, its down items waiting inside the launch for every
+ * gate_up item, measured 40-50 % slower on GB300: a down item cannot stream
+ * its weights before knowing its item, and its CTA slot opens only when a
+ * gate_up CTA ends.) */
+w8_status w8_mlp(const w8_build *b, int gate_up, int down, const uint16_t *x, int64_t ldx, int m,
+                 uint16_t *h, int64_t ldh, uint16_t *y, int64_t ldy, void *workspace,
+                 size_t workspace_bytes, w8_stream s);
+
+/* Workspace bytes of w8_mlp on (gate_up, down) with m tokens (m = 0: the
+ * largest over every m): the larger of the two projections'
+ * w8_workspace_bytes.  Same checks as w8_mlp's on the planes and m. */
+w8_status w8_mlp_workspace_bytes(const w8_build *b, int gate_up, int down, int m, size_t *bytes);
 
 /* The FP8 GEMV for callers that cannot allocate device memory.
  *

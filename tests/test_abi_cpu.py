@@ -43,7 +43,7 @@ def test_every_declared_function_is_exported():
 
 
 def test_abi_version_and_status_strings():
-    assert w8.lib.w8_abi_version() == 6
+    assert w8.lib.w8_abi_version() == 7
     for code in range(15):
         assert w8.status_str(code)
     assert w8.status_str(99) == "unknown status"
