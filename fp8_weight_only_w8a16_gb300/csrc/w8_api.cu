@@ -176,7 +176,7 @@ w8_status gemv_common(const w8_build *b, int plane, int32_t want_dtype, bool sil
         a.counters = static_cast<int *>(ws);
         a.partial = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + b->ws_counters);
     }
-    if (w8::launch_gemv(kernel_dt(p.dtype), plan, a, reinterpret_cast<cudaStream_t>(s)) !=
+    if (w8::launch_gemv(b->kdt[size_t(plane)], plan, a, reinterpret_cast<cudaStream_t>(s)) !=
         cudaSuccess)
         return W8_ERR_CUDA;
     return W8_OK;
@@ -356,12 +356,26 @@ w8_status w8_bind(const w8_plane_desc *d, int n_planes, void *dst, size_t dst_by
         ra.bfac_src = b128 ? pd.scale : nullptr;
         ra.bfac_dst = factor_copy;
         ra.half = gated ? pd.n / 2 : 0;
-        if (w8::launch_repack(kernel_dt(pd.dtype), ra, reinterpret_cast<cudaStream_t>(s)) !=
-            cudaSuccess) {
+        int kdt = kernel_dt(pd.dtype);
+        if (pd.dtype == W8_DT_MXFP4) {
+            // the plane's first 4 packed bytes hold the scan's flag until the
+            // repack writes them
+            bool wide = false;
+            if (w8::fp4_scales_wide(ra, static_cast<unsigned *>(const_cast<void *>(info.packed)),
+                                    &wide, reinterpret_cast<cudaStream_t>(s)) != cudaSuccess) {
+                delete b;
+                return W8_ERR_CUDA;
+            }
+            ra.fp4_fold = !wide;
+            kdt = wide ? w8::kDtFp4Wide : w8::kDtFp4;
+            info.mxfp4_wide_scales = wide ? 1 : 0;
+        }
+        if (w8::launch_repack(kdt, ra, reinterpret_cast<cudaStream_t>(s)) != cudaSuccess) {
             delete b;
             return W8_ERR_CUDA;
         }
         b->planes.push_back(info);
+        b->kdt.push_back(kdt);
     }
     // The GEMV kernels start reading the packed weights before they wait for
     // the previous kernel of their stream (programmatic dependent launch), so

@@ -130,6 +130,7 @@ template <int kDt> struct WFrag;
 template <> struct WFrag<kDtFp8> { uint4 v; };
 template <> struct WFrag<kDtBf16> { uint4 v[2]; };
 template <> struct WFrag<kDtFp4> { uint2 v; uint32_t s; };
+template <> struct WFrag<kDtFp4Wide> { uint2 v; uint32_t s; };
 
 // Predicated streaming loads: fill the destination only when ok (it keeps
 // its value otherwise).
@@ -248,9 +249,11 @@ __device__ __forceinline__ void a_operands(uint32_t (&a)[8], const WFrag<kDt> &f
         a[0] = f.v[0].x; a[1] = f.v[0].y; a[2] = f.v[0].z; a[3] = f.v[0].w;
         a[4] = f.v[1].x; a[5] = f.v[1].y; a[6] = f.v[1].z; a[7] = f.v[1].w;
     } else {
-        // E2M1 x 2^-126 (exact) x 2^126 (exact) x the block scale 2^(e-127)
-        // (exact: the value keeps 2 significant bits within bf16's range; a
-        // NaN scale gives NaN, a product past bf16's range gives inf)
+        // E2M1 x 2^-126 (exact) x the stored factor: 2^126 x the block scale
+        // 2^(e-127) = 2^(e-1) for kDtFp4 (exact: bf16 holds 2^(e-1) for e <=
+        // 128, and the product keeps 2 significant bits within bf16's range),
+        // or 2^126 and then the scale for kDtFp4Wide (scales past 2^1).  A NaN
+        // scale gives NaN, a product past bf16's range gives inf.
         uint32_t sg, sg8;
         asm("prmt.b32 %0, %1, 0, 0x1010;" : "=r"(sg) : "r"(f.s));  // (row g, row g)
         asm("prmt.b32 %0, %1, 0, 0x3232;" : "=r"(sg8) : "r"(f.s)); // (row g+8, row g+8)
@@ -258,10 +261,17 @@ __device__ __forceinline__ void a_operands(uint32_t (&a)[8], const WFrag<kDt> &f
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const uint32_t w = q ? f.v.y : f.v.x;
-            a[4 * q + 0] = mul_bf16x2(mul_bf16x2(e2m1x2_bits<0>(w), k2p126), sg);
-            a[4 * q + 1] = mul_bf16x2(mul_bf16x2(e2m1x2_bits<1>(w), k2p126), sg8);
-            a[4 * q + 2] = mul_bf16x2(mul_bf16x2(e2m1x2_bits<2>(w), k2p126), sg);
-            a[4 * q + 3] = mul_bf16x2(mul_bf16x2(e2m1x2_bits<3>(w), k2p126), sg8);
+            if constexpr (kDt == kDtFp4Wide) {
+                a[4 * q + 0] = mul_bf16x2(mul_bf16x2(e2m1x2_bits<0>(w), k2p126), sg);
+                a[4 * q + 1] = mul_bf16x2(mul_bf16x2(e2m1x2_bits<1>(w), k2p126), sg8);
+                a[4 * q + 2] = mul_bf16x2(mul_bf16x2(e2m1x2_bits<2>(w), k2p126), sg);
+                a[4 * q + 3] = mul_bf16x2(mul_bf16x2(e2m1x2_bits<3>(w), k2p126), sg8);
+            } else {
+                a[4 * q + 0] = mul_bf16x2(e2m1x2_bits<0>(w), sg);
+                a[4 * q + 1] = mul_bf16x2(e2m1x2_bits<1>(w), sg8);
+                a[4 * q + 2] = mul_bf16x2(e2m1x2_bits<2>(w), sg);
+                a[4 * q + 3] = mul_bf16x2(e2m1x2_bits<3>(w), sg8);
+            }
         }
     }
 }

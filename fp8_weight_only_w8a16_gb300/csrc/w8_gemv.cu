@@ -155,8 +155,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
     constexpr bool kB128 = kDt == kDtFp8B;    // block factors inside the K loop
     constexpr int kW = kB128 ? kDtFp8 : kDt;   // the format of the weight codes
     constexpr bool kFp8 = kW == kDtFp8;        // row scales in the epilogue
-    constexpr int kRun = kW == kDtFp8 ? kRunFp8 : kW == kDtFp4 ? kRunFp4 : kRunBf16;
-    constexpr int kLaneBytes = kDt == kDtFp4 ? 8 : 16; // a lane's part of a run (bf16: twice)
+    constexpr int kRun = kW == kDtFp8 ? kRunFp8 : is_fp4(kW) ? kRunFp4 : kRunBf16;
+    constexpr int kLaneBytes = is_fp4(kDt) ? 8 : 16; // a lane's part of a run (bf16: twice)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
         wptr[r] = a.wp + (t64 * a.kb + kb0) * kRun + lane * kLaneBytes;
     }
     // MXFP4: from the lane's codes to its rows' scale word (g) after the codes
-    const int soff = kDt == kDtFp4 ? kRunFp4Codes - kLaneBytes * lane + 4 * g : 0;
+    const int soff = is_fp4(kDt) ? kRunFp4Codes - kLaneBytes * lane + 4 * g : 0;
     const uint16_t *xptr[NT];
     uint32_t tok_ok[NT];
 #pragma unroll
@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
 // the steady body (the copies whose registers hold it without spills).
 constexpr bool has_long(int dt, int nt, int r)
 {
-    return nt <= 2 && (dt == kDtFp8 || (dt == kDtFp4 && nt == 1 && r == 1));
+    return nt <= 2 && (dt == kDtFp8 || (is_fp4(dt) && nt == 1 && r == 1));
 }
 
 template <int kDt, int NT, int R, int OCC, bool kLong>
@@ -552,6 +552,7 @@ void *pick_dt(int dt, int nt, int r, int occ, bool lng)
 {
     return dt == kDtFp8    ? pick<kDtFp8>(nt, r, occ, lng)
            : dt == kDtFp4  ? pick<kDtFp4>(nt, r, occ, lng)
+           : dt == kDtFp4Wide ? pick<kDtFp4Wide>(nt, r, occ, lng)
            : dt == kDtFp8B ? pick<kDtFp8B>(nt, r, occ, lng)
                            : pick<kDtBf16>(nt, r, occ, lng);
 }
@@ -562,7 +563,7 @@ cudaError_t prepare_gemv_kernels()
 {
     // the K-part reduction buffer: 8 warps x R x NT x 128 floats, at most 64 KB
     for (int i = 0; i < kNumInst; ++i) {
-        for (int dt : {kDtBf16, kDtFp8, kDtFp4, kDtFp8B}) {
+        for (int dt : {kDtBf16, kDtFp8, kDtFp4, kDtFp4Wide, kDtFp8B}) {
             for (bool lng : {false, true}) {
                 void *fn = pick_dt(dt, kInst[i].nt, kInst[i].r, kInst[i].occ, lng);
                 if (!fn)
@@ -580,7 +581,7 @@ cudaError_t prepare_gemv_kernels()
 cudaError_t launch_gemv(int dt, const Plan &plan, const GemvArgs &a, cudaStream_t s)
 {
     if (plan.tc)
-        return dt == kDtFp4 || dt == kDtFp8B ? cudaErrorInvalidValue
+        return is_fp4(dt) || dt == kDtFp8B ? cudaErrorInvalidValue
                                              : launch_tc(dt == kDtFp8, plan, a, s);
     void *fn = pick_dt(dt, plan.nt, plan.r, plan.occ, plan.long_k);
     if (!fn)

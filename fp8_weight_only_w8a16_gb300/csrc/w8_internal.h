@@ -17,6 +17,7 @@ struct w8_build {
     size_t ws_counters; // the workspace's counter head for every call of the build:
                         // one counter per row tile of its largest plane
     std::vector<w8_plane_info> planes;
+    std::vector<int> kdt; // each plane's kernel dtype (w8_layout.h)
 };
 
 // Workspace bytes a call with this plan needs on this build: the build's
@@ -66,8 +67,8 @@ inline void set_output_map(GemvArgs &a, const w8_plane_info &p, bool silu)
 }
 
 // One launch of the GEMV kernel chosen by the plan; dt is the weight dtype
-// (kDtBf16, kDtFp8, kDtFp4 or kDtFp8B of w8_layout.h; MXFP4 and block-scaled
-// plans are register-ring plans).
+// (kDtBf16, kDtFp8, kDtFp4, kDtFp4Wide or kDtFp8B of w8_layout.h; MXFP4 and
+// block-scaled plans are register-ring plans).
 cudaError_t launch_gemv(int dt, const Plan &plan, const GemvArgs &a, cudaStream_t s);
 
 // Raise the dynamic shared-memory limit of every GEMV kernel instance on the
@@ -97,9 +98,16 @@ struct RepackArgs {
                             // FP8: floats)
     const float *bfac_src;  // block-scaled FP8: caller's factors [ceil(n/128)][ldb] (device)
     float *bfac_dst;        // block-scaled FP8: the build's copy [ceil(n/128)][ceil(k/128)]
+    bool fp4_fold;          // MXFP4: store 2^126 x each scale (kDtFp4), else the scale
+                            // (kDtFp4Wide)
 };
 
-// The repack of one plane (dt: kDtBf16, kDtFp8, kDtFp4 or kDtFp8B).
+// MXFP4: whether any block scale of the plane is past 2^1 (E8M0 129..254), so
+// that the plane needs kDtFp4Wide.  Uses 4 bytes of device scratch and
+// synchronises s (bind time).
+cudaError_t fp4_scales_wide(const RepackArgs &a, unsigned *scratch, bool *wide, cudaStream_t s);
+
+// The repack of one plane (dt: kDtBf16, kDtFp8, kDtFp4, kDtFp4Wide or kDtFp8B).
 cudaError_t launch_repack(int dt, const RepackArgs &a, cudaStream_t s);
 
 } // namespace w8

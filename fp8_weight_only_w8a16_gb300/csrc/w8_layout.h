@@ -41,11 +41,16 @@ constexpr int kRunFp8 = 512;      // bytes of one (tile, block) run, FP8
 constexpr int kRunBf16 = 1024;    // bytes of one (tile, block) run, bf16
 constexpr int kWarps = 8;         // warps per CTA of the GEMV kernel
 constexpr int kThreads = kWarps * 32;
-// Weight dtypes of the kernels (the register ring reads all four; the
+// Weight dtypes of the kernels (the register ring reads all five; the
 // tensor-memory kernel bf16 and FP8).  kDtFp8B is an FP8 plane with one fp32
 // factor per kBlockB x kBlockB block instead of row scales: the FP8 codes and
-// packed layout, each block's partial sum multiplied by its factor.
-constexpr int kDtBf16 = 0, kDtFp8 = 1, kDtFp4 = 2, kDtFp8B = 3;
+// packed layout, each block's partial sum multiplied by its factor.  kDtFp4
+// and kDtFp4Wide are MXFP4 planes in one packed layout; they differ in the
+// bf16 factor stored beside each block's codes: 2^126 times the E8M0 scale
+// (one multiply per code pair) when every scale of the plane is at most 2^1,
+// else the scale alone (kDtFp4Wide: times 2^126 first, a second multiply).
+constexpr int kDtBf16 = 0, kDtFp8 = 1, kDtFp4 = 2, kDtFp8B = 3, kDtFp4Wide = 4;
+W8_HD constexpr bool is_fp4(int dt) { return dt == kDtFp4 || dt == kDtFp4Wide; }
 constexpr int kBlockB = 128;      // rows and columns one block factor covers
 constexpr int kMaxM = 256;        // tokens per call (decode steps, draft rows, prefill chunks)
 constexpr int kMaxRingM = 64;     // the register-ring kernel's limit (8 token groups of 8)
@@ -203,17 +208,17 @@ constexpr int depth_x(int nt, int r, bool fp8, int occ)
 {
     return fp8 ? kInst[inst_index(nt, r, occ)].dx_fp8 : kInst[inst_index(nt, r, occ)].dx_bf16;
 }
-// The depths of one kernel dtype (kDtBf16, kDtFp8, kDtFp4, kDtFp8B); 0 for a
+// The depths of one kernel dtype (kDtBf16, kDtFp8, kDtFp4, kDtFp4Wide, kDtFp8B); 0 for a
 // block-scaled instance that does not exist.
 constexpr int depth_w_dt(int nt, int r, int dt, int occ)
 {
-    return dt == kDtFp4    ? kInst[inst_index(nt, r, occ)].dw_fp4
+    return is_fp4(dt)      ? kInst[inst_index(nt, r, occ)].dw_fp4
            : dt == kDtFp8B ? kInst[inst_index(nt, r, occ)].dw_b128
                            : depth_w(nt, r, dt == kDtFp8, occ);
 }
 constexpr int depth_x_dt(int nt, int r, int dt, int occ)
 {
-    return dt == kDtFp4    ? kInst[inst_index(nt, r, occ)].dx_fp4
+    return is_fp4(dt)      ? kInst[inst_index(nt, r, occ)].dx_fp4
            : dt == kDtFp8B ? kInst[inst_index(nt, r, occ)].dx_b128
                            : depth_x(nt, r, dt == kDtFp8, occ);
 }

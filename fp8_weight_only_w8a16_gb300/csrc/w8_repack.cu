@@ -170,11 +170,31 @@ __device__ __forceinline__ uint32_t load8_fp4(const uint8_t *row, int64_t col, i
     return v;
 }
 
-// E8M0 scale -> bf16 bits of 2^(e - 127): the exponent field, except e = 0
-// (2^-127, a bf16 subnormal) and e = 255 (NaN).
-__device__ __forceinline__ uint32_t e8m0_to_bf16(uint32_t e)
+// E8M0 scale -> the bf16 factor stored beside the codes.  Folded (kDtFp4):
+// 2^126 x 2^(e - 127) = 2^(e - 1), exponent field e + 126, for e <= 128.
+// Otherwise (kDtFp4Wide) 2^(e - 127): the exponent field, except e = 0
+// (2^-127, a bf16 subnormal).  e = 255 is NaN either way.
+__device__ __forceinline__ uint32_t e8m0_to_bf16(uint32_t e, bool fold)
 {
-    return e == 0 ? 0x0040u : e == 255 ? 0x7FC0u : (e << 7);
+    if (e == 255)
+        return 0x7FC0u;
+    if (fold)
+        return (e + 126u) << 7;
+    return e == 0 ? 0x0040u : (e << 7);
+}
+
+// Whether any block scale of an MXFP4 plane lies in 129..254, where the
+// folded factor 2^(e - 1) is past bf16's range: one CTA per source row.
+__global__ void __launch_bounds__(256) fp4_scale_scan_kernel(const RepackArgs a, unsigned *wide)
+{
+    const int64_t row = blockIdx.x;
+    for (int64_t kb = threadIdx.x; kb < a.kb; kb += blockDim.x) {
+        const uint32_t e = a.bscale_src[row * a.ldb + kb];
+        if (e > 128u && e < 255u) {
+            atomicOr(wide, 1u);
+            return;
+        }
+    }
 }
 
 __global__ void __launch_bounds__(256) repack_fp4_kernel(const RepackArgs a)
@@ -190,11 +210,11 @@ __global__ void __launch_bounds__(256) repack_fp4_kernel(const RepackArgs a)
         const int64_t n0 = rt * kTileN + g, n1 = n0 + 8;
         if (n0 < a.n) {
             lo = load8_fp4(a.src + src_row(a, n0) * a.ld_bytes, col, a.k);
-            slo = e8m0_to_bf16(a.bscale_src[src_row(a, n0) * a.ldb + kb]);
+            slo = e8m0_to_bf16(a.bscale_src[src_row(a, n0) * a.ldb + kb], a.fp4_fold);
         }
         if (n1 < a.n) {
             hi = load8_fp4(a.src + src_row(a, n1) * a.ld_bytes, col, a.k);
-            shi = e8m0_to_bf16(a.bscale_src[src_row(a, n1) * a.ldb + kb]);
+            shi = e8m0_to_bf16(a.bscale_src[src_row(a, n1) * a.ldb + kb], a.fp4_fold);
         }
         // word q holds A registers reg = 0..3 of step q: (row g, cols 4q, +1),
         // (row g+8, same), (row g, cols 4q+2, +3), (row g+8, same) of the lane's
@@ -233,6 +253,25 @@ __global__ void __launch_bounds__(256) copy_factors_kernel(const RepackArgs a)
 
 } // namespace
 
+cudaError_t fp4_scales_wide(const RepackArgs &a, unsigned *scratch, bool *wide, cudaStream_t s)
+{
+    *wide = false;
+    if (a.n <= 0 || a.kb <= 0)
+        return cudaSuccess;
+    unsigned h = 0;
+    cudaError_t e = cudaMemsetAsync(scratch, 0, sizeof(unsigned), s);
+    if (e != cudaSuccess)
+        return e;
+    fp4_scale_scan_kernel<<<dim3(unsigned(a.n)), 256, 0, s>>>(a, scratch);
+    if ((e = cudaGetLastError()) != cudaSuccess ||
+        (e = cudaMemcpyAsync(&h, scratch, sizeof(unsigned), cudaMemcpyDeviceToHost, s)) !=
+            cudaSuccess ||
+        (e = cudaStreamSynchronize(s)) != cudaSuccess)
+        return e;
+    *wide = h != 0;
+    return cudaSuccess;
+}
+
 cudaError_t launch_repack(int dt, const RepackArgs &a, cudaStream_t s)
 {
     if (a.rt <= 0)
@@ -242,7 +281,7 @@ cudaError_t launch_repack(int dt, const RepackArgs &a, cudaStream_t s)
         copy_factors_kernel<<<dim3(unsigned((a.n + kBlockB - 1) / kBlockB)), 256, 0, s>>>(a);
     } else if (dt == kDtFp8)
         repack_fp8_kernel<<<dim3(unsigned(a.rt)), 256, 0, s>>>(a);
-    else if (dt == kDtFp4)
+    else if (is_fp4(dt))
         repack_fp4_kernel<<<dim3(unsigned(a.rt)), 256, 0, s>>>(a);
     else
         repack_bf16_kernel<<<dim3(unsigned(a.rt)), 256, 0, s>>>(a);

@@ -55,7 +55,7 @@ class PlaneInfo(ctypes.Structure):
                 ("k", ctypes.c_int64), ("row_tiles", ctypes.c_int64),
                 ("k_blocks", ctypes.c_int64), ("packed", ctypes.c_void_p),
                 ("scale", ctypes.c_void_p), ("packed_bytes", ctypes.c_size_t),
-                ("block_factors", ctypes.c_void_p)]
+                ("block_factors", ctypes.c_void_p), ("mxfp4_wide_scales", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):

@@ -176,6 +176,10 @@ typedef struct {
     size_t packed_bytes;     /* bytes of the packed weights (MXFP4: with the block scales) */
     const float *block_factors; /* device, block-scaled FP8: the build's copy of the factors,
                                 [ceil(n / 128)][ceil(k / 128)]; else NULL */
+    int32_t mxfp4_wide_scales; /* MXFP4: 1 when a block scale of the plane is above 2^1
+                                (E8M0 129..254), so its codes take two multiplies (2^126,
+                                then the scale) instead of one by 2^126 x the scale folded
+                                at bind; the result is the same.  0 otherwise. */
 } w8_plane_info;
 
 /* The launch a gemv call makes for one (plane, m); returned for inspection.

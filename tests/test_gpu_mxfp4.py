@@ -14,7 +14,11 @@ Checked against the oracle:
 * exact-sum inputs bit for bit; with every scale 1 the result equals the
   bf16 plane of the dequantized codes bit for bit (same summation order);
 * one-hot tokens over every code and edge scales (E8M0 0, 1, 254, 255):
-  each output exactly the oracle's, NaN rows included;
+  each output exactly the oracle's, NaN rows included -- on a plane whose
+  scales reach past 2^1 (two multiplies per code pair) and on one whose
+  scales stay at or below it, down to E8M0 0 and up to 128 (2^126 folded
+  into the stored factor at bind, one multiply);
+* the two forms agree bit for bit on the rows they share;
 * the full-size o_proj and q_b planes on sampled rows;
 * the refusals: other entry points, other builds, more than 64 tokens.
 """
@@ -67,12 +71,16 @@ def _run(w8, b, x, n, fn=None):
     return from_dev(y)
 
 
+@pytest.mark.parametrize("wide", [False, True], ids=["folded", "wide"])
 @pytest.mark.parametrize("n,k", [(37, 77), (16, 32), (100, 300), (5, 1)])
-def test_repack_matches_host_bit_map(w8, n, k):
+def test_repack_matches_host_bit_map(w8, n, k, wide):
     plane, _ = _case(1, n, k, 1)
+    if wide:  # one scale above 2^1: the plane keeps the plain scales
+        plane.scale[n // 2, 0] = 131
     b, _src = _bind(w8, plane)
     info = b.info(0)
     assert info.dtype == w8.DT_MXFP4 and info.layout == w8.LAYOUT_MMA_16x32
+    assert info.mxfp4_wide_scales == int(wide)
     rt, kb = info.row_tiles, info.k_blocks
     assert info.packed_bytes == rt * kb * 288
     base = info.packed - b.dst.data_ptr()
@@ -83,9 +91,14 @@ def test_repack_matches_host_bit_map(w8, n, k):
             code = int(plane.w[r, c // 2] >> (4 * (c & 1))) & 15 if (r < n and c < k) else 0
             for i, b in enumerate(w8.mxfp4_code_bits(kb, r, c)):
                 want[b // 8] |= np.uint8(((code >> i) & 1) << (b % 8))
-    # the scale words: bf16 of 2^(e - 127) for rows g and g+8 of each run
+    # the scale words for rows g and g+8 of each run: bf16 of 2^126 x 2^(e - 127)
+    # on a folded plane, of 2^(e - 127) on a wide one; NaN for e = 255
     def bf16_of(e):
-        return 0x0040 if e == 0 else 0x7FC0 if e == 255 else (int(e) << 7)
+        if e == 255:
+            return 0x7FC0
+        if not wide:
+            return (int(e) + 126) << 7
+        return 0x0040 if e == 0 else (int(e) << 7)
     for t in range(rt):
         for blk in range(kb):
             run = (t * kb + blk) * 288
@@ -172,6 +185,50 @@ def test_one_hot_every_code_and_edge_scales(w8):
     want = oracle.gemv_mxfp4(w, bs, x, k=k)
     assert oracle.same_values(y, want)
     assert np.all(np.isnan(oracle.bf16_bits_to_f64(y[:, 5])))
+
+
+def test_one_hot_folded_edge_scales(w8):
+    """The folded factor's range ends: E8M0 0 (2^-1 stored), 1, 127, 128 (2^127
+    stored), with a NaN block; every output exactly the oracle's."""
+    n, k = 64, 96
+    codes = np.arange(n) % 16
+    w = np.repeat((codes | (((codes + 7) % 16) << 4)).astype(np.uint8)[:, None], k // 2, axis=1)
+    edge = np.array([0, 1, 127, 128, 126, 2, 100, 10, 120, 64, 125], dtype=np.uint8)
+    bs = np.stack([np.resize(edge, n), np.resize(edge[::-1], n), np.resize(np.roll(edge, 3), n)],
+                  axis=1).astype(np.uint8)
+    bs[9, 1] = 255
+    plane = synth.Plane("mxfp4", n, k, k, w, bs)
+    cols = [0, 1, 33, 34, 64, 95]
+    x = np.zeros((len(cols), k), dtype=np.uint16)
+    for i, c in enumerate(cols):
+        x[i, c] = 0xBF80  # -1: the signs too
+    b, _src = _bind(w8, plane)
+    assert b.info(0).mxfp4_wide_scales == 0
+    y = _run(w8, b, x, n)
+    assert oracle.same_values(y, oracle.gemv_mxfp4(w, bs, x, k=k))
+    assert np.all(np.isnan(oracle.bf16_bits_to_f64(y[:, 9])))
+
+
+@pytest.mark.parametrize("n,k,m", [(256, 512, 8), (300, 2100, 16), (2624, 6144, 1)])
+def test_folded_and_wide_planes_agree(w8, n, k, m):
+    """One plane bound twice: as drawn (every scale at most 2^1, folded) and
+    with one block's scale raised past 2^1 (wide).  Every row but that one is
+    the same bit for bit (both multiply exactly, in the same order); all rows
+    are within the oracle's tolerance."""
+    plane, x = _case(n * 3 + k + m, n, k, m)
+    b1, _s1 = _bind(w8, plane)
+    wide = synth.Plane("mxfp4", n, k, plane.ldw, plane.w, plane.scale.copy())
+    r = n // 3
+    wide.scale[r, 1] = 140
+    b2, _s2 = _bind(w8, wide)
+    assert b1.info(0).mxfp4_wide_scales == 0 and b2.info(0).mxfp4_wide_scales == 1
+    y1, y2 = _run(w8, b1, x, n), _run(w8, b2, x, n)
+    others = np.arange(n) != r
+    assert oracle.same_values(y1[:, others], y2[:, others])
+    for pl, y in ((plane, y1), (wide, y2)):
+        y64, mag = oracle.gemv_mxfp4_f64(pl.w, pl.scale, x, k=k, threads=8)
+        ok, worst = oracle.within_tolerance(y, y64, mag)
+        assert ok, worst
 
 
 @pytest.mark.parametrize("n,k,ms", [(6144, 16384, (1, 2, 8, 32)), (16384, 2048, (1, 8, 64)),
