@@ -288,8 +288,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
     // further on.
     int b = 0;
     if constexpr (kLong) {
-        // The kLong copies of the 1..16-token FP8 and one-group, one-tile
-        // MXFP4 instances, which the planner picks for K parts of at least four
+        // The kLong copies of the 1..16-token FP8 (row- or block-scaled) and
+        // one-group, one-tile MXFP4 instances, which the planner picks for K parts of at least four
         // ring groups: while every refill of a group lies inside the K part
         // (b + 2 DW <= nmain) the loads carry no predicate -- and activations
         // of tokens past m, whose sums are never stored, read token 0's row
@@ -298,6 +298,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
         // 18.8 us at one token; compiled into the kernels of short K parts,
         // the second body made those 3-4 % slower, hence the separate copies.
         for (; b + 2 * DW <= nmain; b += DW) {
+            if constexpr (kB128)
+                factor_window<R>(fac, fac_row, fbase, (kb0 + b) >> 2, (kb0 + b + DW - 1) >> 2,
+                                 lane, a.nbf);
             if (kPf > DW && lane == 0 && b + kPf < nmain) {
                 const int hi = b + kPf + DW < nmain ? b + kPf + DW : nmain;
 #pragma unroll
@@ -306,7 +309,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
             }
 #pragma unroll
             for (int i = 0; i < DW; ++i) {
-                block_step<kW, NT, R>(acc, wring[i], xring[i % DX]);
+                if constexpr (kB128) {
+                    block_step<kW, NT, R>(part, wring[i], xring[i % DX]);
+                    if ((i & 3) == 3) // kb0 and b are whole column blocks
+                        close_block<NT, R>(acc, part, fac, fbase, (kb0 + b + i) >> 2);
+                } else {
+                    block_step<kW, NT, R>(acc, wring[i], xring[i % DX]);
+                }
 #pragma unroll
                 for (int r = 0; r < R; ++r)
                     load_w_now<kW>(wring[i][r], wptr[r] + (b + DW + i) * kRun, soff);
@@ -508,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gemv_kernel(const GemvAr
 // the steady body (the copies whose registers hold it without spills).
 constexpr bool has_long(int dt, int nt, int r)
 {
-    return nt <= 2 && (dt == kDtFp8 || (is_fp4(dt) && nt == 1 && r == 1));
+    return nt <= 2 && (dt == kDtFp8 || dt == kDtFp8B || (is_fp4(dt) && nt == 1 && r == 1));
 }
 
 template <int kDt, int NT, int R, int OCC, bool kLong>
