@@ -23,8 +23,9 @@
 //   warp 8 (activations): after the dependency wait, one thread copies the
 //     activation tiles with tensor-map bulk copies (TMA): one 8-column x
 //     tokens box per K group, landing as the 8-row x 16-byte core matrices
-//     of the tensor cores' K-major layout; rows past the tokens and columns
-//     past K arrive as zeros;
+//     of the tensor cores' K-major layout; columns past K arrive as zeros,
+//     rows past the tokens are not copied (their accumulator columns are
+//     never stored);
 //   warp 9 (issuer): one thread issues the tensor-core steps
 //     D[128 x NPAD] += A[128 x 16] (TMEM) * B[16 x NPAD] (shared memory) and
 //     commits them to the stages' "empty" barriers.
@@ -430,7 +431,9 @@ __global__ void __launch_bounds__(kTcThreads, tc_occ(NPAD))
     } else if (warp == kWarpAct) {
         // ---- activations: x -> B tiles in shared memory (tensor-map copies) -----
         // Lane 4j + k copies K group k of block j of the stage (16 copies in
-        // parallel), each an 8-column x NPAD-row box.
+        // parallel), each an 8-column x min(m, NPAD)-row box (rows past m
+        // keep whatever the slot held: they meet only the accumulator columns
+        // of tokens >= m, which are never stored).
         pdl_wait(); // x may be the previous kernel's output
         bool ok = true;
         for (int st = 0; st < nst && ok; ++st) {
@@ -441,7 +444,7 @@ __global__ void __launch_bounds__(kTcThreads, tc_occ(NPAD))
                 break;
             const int nb = cnb - st * kTcKs < kTcKs ? cnb - st * kTcKs : kTcKs;
             if (lane == 0)
-                mbar_expect_tx(&bar_full_b[s], uint32_t(nb * kBlockB));
+                mbar_expect_tx(&bar_full_b[s], uint32_t(nb * 4 * 16 * (a.m < NPAD ? a.m : NPAD)));
             __syncwarp();
             const int j = lane >> 2, kg = lane & 3;
             if (j < nb) {
@@ -665,7 +668,11 @@ bool encode_x_map(CUtensorMap *map, const GemvArgs &a, int npad)
         return false;
     const cuuint64_t dims[2] = {cuuint64_t(a.k), cuuint64_t(a.m)};
     const cuuint64_t strides[1] = {cuuint64_t(a.ldx) * 2};
-    const cuuint32_t box[2] = {8, cuuint32_t(npad)};
+    // m rows, not npad: the stage rows of tokens m..npad-1 are never written
+    // (they feed only accumulator columns that are never stored), so no copy
+    // reads past the tensor's last row (measured: boxes with out-of-range
+    // rows, filled by the copy engine, made 17..31 tokens slower than 32)
+    const cuuint32_t box[2] = {8, cuuint32_t(a.m < npad ? a.m : npad)};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(a.x), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,

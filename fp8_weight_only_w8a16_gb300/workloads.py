@@ -76,6 +76,12 @@ LM_HEAD = Projection("lm_head", 154880, 6144, "bf16", (1,))
 # K = 6144), so their bf16 planes bind as one [160, 6144] plane: one call
 # instead of two, rows 0..127 = wk, 128..159 = weights_proj.
 WK_WEIGHTS_PROJ = Projection("indexer_wk_weights_proj", 160, 6144, "bf16", SWEEP_M)
+# q_b_proj and the indexer's wq_b read the same q_lora_rank latent (q_c, 2048
+# wide, after q_a_layernorm: the GLM-5.2 anatomy page's config table notes
+# that wq_b takes this rank too, and its layer diagram feeds q_c to both), and
+# both are E4M3 planes with row scales, so they bind as one [20480, 2048]
+# plane: rows 0..16383 = q_b, 16384..20479 = wq_b, one call instead of two.
+Q_B_WQ_B = Projection("q_b_wq_b_proj", 20480, 2048, "e4m3fn", SWEEP_M)
 
 # Above the decode range: draft rows and prefill chunks of 96..256 tokens on
 # the largest attention projections (the tensor-memory kernel only).
@@ -97,7 +103,8 @@ FUSED_QKV_A_B128 = Projection("fused_qkv_a_proj_b128", 2624, 6144, "e4m3fn_b128"
 O_PROJ_B128 = Projection("o_proj_b128", 6144, 16384, "e4m3fn_b128", (1, 2, 8, 32))
 
 ALL = (TINY, FUSED_QKV_A, O_PROJ, O_PROJ_BF16, SHARED_GATE_UP, SHARED_DOWN,
-       SHARED_GATE_UP_KPAD, SHARED_GATE_UP_SILU, Q_B, KV_B, WQ_B, WK, WEIGHTS_PROJ, WK_WEIGHTS_PROJ, LM_HEAD,
+       SHARED_GATE_UP_KPAD, SHARED_GATE_UP_SILU, Q_B, KV_B, WQ_B, WK, WEIGHTS_PROJ, WK_WEIGHTS_PROJ,
+       Q_B_WQ_B, LM_HEAD,
        O_PROJ_LARGE_M, Q_B_LARGE_M, KV_B_LARGE_M, O_PROJ_MXFP4, Q_B_MXFP4, FUSED_QKV_A_MXFP4,
        FUSED_QKV_A_B128, O_PROJ_B128)
 BY_NAME = {p.name: p for p in ALL}
@@ -119,7 +126,7 @@ GROUPS = {
     "fused_qkv_a_proj": (FUSED_QKV_A,),
     "o_proj": (O_PROJ, O_PROJ_BF16),
     "shared_expert": (SHARED_GATE_UP, SHARED_DOWN, SHARED_GATE_UP_KPAD, SHARED_GATE_UP_SILU),
-    "layer_sweep": (Q_B, KV_B, WQ_B, WK, WEIGHTS_PROJ, WK_WEIGHTS_PROJ, LM_HEAD),
+    "layer_sweep": (Q_B, KV_B, WQ_B, WK, WEIGHTS_PROJ, WK_WEIGHTS_PROJ, Q_B_WQ_B, LM_HEAD),
     "large_m": (O_PROJ_LARGE_M, Q_B_LARGE_M, KV_B_LARGE_M),
     "mxfp4": (O_PROJ_MXFP4, Q_B_MXFP4, FUSED_QKV_A_MXFP4),
     "block_scaled": (FUSED_QKV_A_B128, O_PROJ_B128),
