@@ -416,6 +416,7 @@ static void fill_plan(const w8::Plan &pl, w8_plan *out)
     out->splits = pl.splits;
     out->k_blocks_per_warp_max = pl.kbs_max;
     out->workspace_bytes = pl.ws_bytes;
+    out->cluster = pl.tc ? pl.cluster : 1;
 }
 
 w8_status w8_plan_shape(int64_t n, int64_t k, int m, int sm_count, w8_plan *out)

@@ -55,6 +55,8 @@ struct GemvArgs {
     int half;               // gate_up planes: I = n / 2
     const float *bfac;      // block-scaled FP8: the build's factors [ceil(n/128)][nbf]
     int nbf;                // block-scaled FP8: column blocks, ceil(k / 128)
+    int gsplit;             // tc, splits > 1: the partial tiles meet in the workspace
+                            // (counters, partial) instead of a cluster's shared memory
 };
 
 // The output mapping of a plane: gate_up planes (bound with W8_SRC_GATE_UP)

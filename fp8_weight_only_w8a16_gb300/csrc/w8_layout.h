@@ -151,6 +151,9 @@ struct Plan {
     int64_t kb;      // K blocks of the plane
     int row_groups;
     int splits;
+    int cluster;     // tc: CTAs of a thread-block cluster -- the splits of a row
+                     // block, whose partial tiles meet in distributed shared
+                     // memory; 1 with splits > 1: they meet in the workspace
     int kbs_max;     // most K blocks one warp streams
     bool long_k;     // ring: K parts of at least four ring groups (the kernel copy
                      // with a predicate-free steady loop)
@@ -280,6 +283,9 @@ W8_HD constexpr int tc_smem_bytes(bool fp8, int npad)
            tc_stages(fp8, npad).nb * 4 * npad * 64;
 }
 constexpr int kTcMaxSplits = 8;  // CTAs per cluster (the portable cluster size)
+constexpr int kTcMaxGlobalSplits = 8; // K ranges of a row block that meet in the workspace
+constexpr int kTcMinGlobalSplitBlocks = 32; // ... each at least this many K blocks (8 stages),
+                                            // so that the stream outweighs the reduction
 
 inline Plan make_tc_plan(int64_t n, int64_t k, int m, int sm_count)
 {
@@ -305,12 +311,37 @@ inline Plan make_tc_plan(int64_t n, int64_t k, int m, int sm_count)
     while (splits < kTcMaxSplits && rbs * splits * 2 <= target &&
            p.kb / (int64_t(splits) * 2) >= kTcStageBlocks)
         splits *= 2;
+    p.cluster = splits;
+    p.ws_counters = p.ws_bytes = 0; // partial sums stay on chip (cluster exchange)
+    // Planes of few row blocks (o_proj's 48): the power-of-two cluster splits
+    // leave SMs idle (96 CTAs on 152 SMs) or some SMs with one CTA more than
+    // the rest (192), which end long after the others.  Where more K ranges
+    // fit the resident slots, split K into that many instead and add the
+    // partial tiles through the workspace (the last CTA of a row block to
+    // arrive), so that no cluster has to be placed whole: up to
+    // kTcMaxGlobalSplits, each range at least kTcMinGlobalSplitBlocks; up to
+    // 64 tokens only, where the last CTA's reduction (128 rows x the tokens x
+    // the splits) stays short.  Measured: o_proj 36.4 -> 28.8 us at 17 tokens,
+    // 38.1 -> 31.8 at 32, 53.7 -> 52.3 at 64; above 64 tokens the reduction
+    // cost more than the balance gained (6144 x 4096 at 96 tokens 21.3 ->
+    // 32.0 us).
+    int64_t sg = target / rbs;
+    if (sg > kTcMaxGlobalSplits)
+        sg = kTcMaxGlobalSplits;
+    while (sg > 1 && p.kb / sg < kTcMinGlobalSplitBlocks)
+        --sg;
+    if (sg > splits && p.npad <= 64) {
+        splits = int(sg);
+        p.cluster = 1;
+        p.ws_counters = align256(size_t(p.rt) * sizeof(int));
+        p.ws_bytes = p.ws_counters + align256(size_t(splits) * size_t(p.rt) * kTileN *
+                                              size_t((m + 3) & ~3) * sizeof(float));
+    }
     p.splits = splits;
     p.row_groups = int(rbs);
     p.grid = int(rbs * splits);
     p.kbs_max = int(ceil_div(p.kb, splits));
     p.smem = tc_smem_bytes(true, p.npad); // the FP8 instance (bf16: its own table)
-    p.ws_counters = p.ws_bytes = 0; // partial sums stay on chip (cluster exchange)
     return p;
 }
 

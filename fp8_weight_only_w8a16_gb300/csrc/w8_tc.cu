@@ -191,6 +191,15 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_
                  "l"(src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
 }
+// 16 bytes of fp32 through L2 only (partial sums other CTAs wrote).
+__device__ __forceinline__ float4 ld_cg_f32x4(const float4 *p)
+{
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
 __device__ __forceinline__ uint4 ld_shared16(uint32_t addr)
 {
     uint4 v;
@@ -540,6 +549,100 @@ __global__ void __launch_bounds__(kTcThreads, tc_occ(NPAD))
                 }
             }
         }
+    } else if (a.gsplit) {
+        // Split K across CTAs that meet in the workspace (no cluster): each
+        // CTA stores its partial tile, [split][row][token] with the tokens
+        // padded to a multiple of 4 (mq), and counts its arrival; the last CTA
+        // of the row block adds the splits in split order (all of a quad's
+        // loads in flight at once), then scales, rounds and stores.  Every
+        // global write follows the wait for the previous kernel (the
+        // workspace may be its too).
+        pdl_wait();
+        const int mq = (a.m + 3) & ~3;
+        const int64_t rows_pad = int64_t(a.rt) * kTileN;
+        if (warp < 4) {
+            // the tensor-memory loads are warp-collective: the whole warp
+            // loads, and only the rows inside the plane are stored
+            float4 *dst = reinterpret_cast<float4 *>(a.partial + (int64_t(sp) * rows_pad + row) * mq);
+#pragma unroll
+            for (int c = 0; c < NPAD / 16; ++c) {
+                if (16 * c < mq) { // uniform across the warp
+                    float d[16];
+                    tm_load16(dq + uint32_t(16 * c), d);
+                    tm_wait_ld();
+                    if (row < a.n) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (16 * c + 4 * q < mq)
+                                dst[4 * c + q] =
+                                    make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
+                    }
+                }
+            }
+        }
+        __threadfence();
+        __syncthreads();
+        __shared__ int s_last;
+        if (threadIdx.x == 0)
+            s_last = atomicAdd(a.counters + rb, 1) == a.splits - 1;
+        __syncthreads();
+        if (s_last) {
+            __threadfence();
+            const int row_end = row0 + 128 < a.n ? row0 + 128 : a.n;
+            const int quads = mq / 4;
+            const int items = (row_end - row0) * quads; // (row, token quad), quads fastest
+            const float4 *base = reinterpret_cast<const float4 *>(a.partial + int64_t(row0) * mq);
+            const int64_t split_stride = rows_pad * quads; // in float4
+            // the splits of one (row, quad), loaded together, added in split order
+            auto split_sum = [&](int off) {
+                float4 p[kTcMaxGlobalSplits];
+#pragma unroll
+                for (int q = 0; q < kTcMaxGlobalSplits; ++q) {
+                    p[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (q < a.splits)
+                        p[q] = ld_cg_f32x4(base + q * split_stride + off);
+                }
+                float4 v = p[0];
+#pragma unroll
+                for (int q = 1; q < kTcMaxGlobalSplits; ++q) {
+                    if (q < a.splits) {
+                        v.x += p[q].x;
+                        v.y += p[q].y;
+                        v.z += p[q].z;
+                        v.w += p[q].w;
+                    }
+                }
+                return v;
+            };
+            for (int it = threadIdx.x; it < items; it += kTcThreads) {
+                const int rl = it / quads;
+                const int q4 = it - rl * quads;
+                const int orow = row0 + rl;
+                if (a.act == kActSiluMul && (rl & 8))
+                    continue; // an up row: added with its gate row (rl - 8)
+                const float4 v = split_sum(it);
+                const float out[4] = {v.x, v.y, v.z, v.w};
+                const float sc = kFp8 ? __ldg(a.scale + orow) : 1.0f;
+                const int col = out_col(orow, a.act != kActPlain, a.half);
+                if (a.act != kActSiluMul) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (4 * q4 + e < a.m)
+                            a.y[int64_t(4 * q4 + e) * a.ldy + col] = to_bf16(kFp8 ? sc * out[e] : out[e]);
+                } else {
+                    const float4 vu = split_sum(it + 8 * quads);
+                    const float up[4] = {vu.x, vu.y, vu.z, vu.w};
+                    const float scu = kFp8 ? __ldg(a.scale + orow + 8) : 1.0f;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (4 * q4 + e < a.m)
+                            a.y[int64_t(4 * q4 + e) * a.ldy + col] =
+                                silu_mul_bf16(kFp8 ? sc * out[e] : out[e], kFp8 ? scu * up[e] : up[e]);
+                }
+            }
+            if (threadIdx.x == 0)
+                a.counters[rb] = 0; // ready for the next call on this workspace
+        }
     } else {
         // Split K across the CTAs of a cluster (rank = split): each CTA parks
         // its partial tile in its own shared memory (the stages are free:
@@ -690,6 +793,7 @@ cudaError_t launch_tc(bool fp8, const Plan &plan, const GemvArgs &a, cudaStream_
     if (!encode_x_map(&tmx, a, plan.npad))
         return cudaErrorInvalidValue;
     GemvArgs aa = a;
+    aa.gsplit = plan.splits > 1 && plan.cluster == 1; // the splits meet in the workspace
     void *args[] = {&aa, &tmx};
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(unsigned(plan.grid));
@@ -699,8 +803,9 @@ cudaError_t launch_tc(bool fp8, const Plan &plan, const GemvArgs &a, cudaStream_
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    // a cluster: the splits of one row block (they exchange partial tiles)
-    const int csz = plan.splits;
+    // a cluster: the splits of one row block (they exchange partial tiles),
+    // unless they meet in the workspace
+    const int csz = plan.cluster;
     attr[1].id = cudaLaunchAttributeClusterDimension;
     attr[1].val.clusterDim.x = unsigned(csz);
     attr[1].val.clusterDim.y = 1;

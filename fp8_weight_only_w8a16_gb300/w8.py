@@ -64,7 +64,7 @@ class PlanInfo(ctypes.Structure):
                 ("row_tiles_per_warp", ctypes.c_int32), ("warps_k", ctypes.c_int32),
                 ("depth", ctypes.c_int32), ("row_groups", ctypes.c_int32),
                 ("splits", ctypes.c_int32), ("k_blocks_per_warp_max", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("cluster", ctypes.c_int32)]
 
 
 def _load():

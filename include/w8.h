@@ -202,10 +202,17 @@ typedef struct {
                                 the FP8 depth; bf16 rings hold fewer, larger blocks;
                                 the depth never changes a summation order) */
     int32_t row_groups;      /* CTAs along N */
-    int32_t splits;          /* CTAs along K (kernel 1: the CTAs of one cluster, which add
-                                their partial sums on chip and need no workspace) */
+    int32_t splits;          /* CTAs along K */
     int32_t k_blocks_per_warp_max; /* most 32-column K blocks one warp streams */
-    size_t workspace_bytes;  /* 0 unless a kernel-0 plan splits K */
+    size_t workspace_bytes;  /* 0 unless the splits add their partial sums through the
+                                workspace (every kernel-0 plan with splits > 1; kernel 1
+                                when cluster is 1) */
+    int32_t cluster;         /* kernel 1: CTAs of a thread-block cluster, the splits of a
+                                row block when they add their partial sums on chip
+                                (cluster == splits, no workspace), or 1 when K is split
+                                into more ranges than a power of two that fill the SMs
+                                evenly (up to 8) and the last CTA of a row block adds
+                                them from the workspace; kernel 0: 1 */
 } w8_plan;
 
 typedef struct w8_build w8_build; /* opaque, host-side, library-owned */

@@ -247,18 +247,30 @@ def test_plan_invariants(n, k, m):
         # padded to 16, about two CTAs per SM, at least one 4-block stage per split
         assert p.kernel == 1 and p.block == 352
         npad = -(-m // 16) * 16 if m <= 64 else min(x for x in (96, 128, 192, 256) if x >= m)
+        occ = 2 if npad <= 64 else 1
         assert p.row_groups == -(-n // 128) and p.n_tiles * 8 == npad
-        assert p.splits in (1, 2, 4, 8) and (p.splits == 1 or kb // p.splits >= 4)
+        assert p.splits == 1 or kb // p.splits >= 4
         assert p.grid <= 2 * 152 or p.splits == 1
         assert p.k_blocks_per_warp_max == -(-kb // p.splits)
+        if p.cluster == 1 and p.splits > 1:
+            # K ranges that meet in the workspace: as many as fill the
+            # resident slots (at most 8), more than the power-of-two
+            # cluster plan would take
+            assert npad <= 64 and (2 < p.splits <= 8 or p.row_groups * 2 <= occ * 152)
+            assert p.splits == min(8, occ * 152 // p.row_groups, kb // 32)
+            assert p.grid <= occ * 152
+            assert p.workspace_bytes >= p.splits * rt * 16 * m * 4
+            return
+        assert p.cluster == p.splits and p.splits in (1, 2, 4, 8)
         nw, nb = {16: (5, 6), 32: (4, 5), 48: (4, 3), 64: (3, 3), 96: (5, 5), 128: (5, 4),
                   192: (4, 3), 256: (4, 2)}[npad]  # FP8 stage slots
         # about 100 KB (two CTAs per SM) up to 64 tokens, about 200 KB (one) above
         limit = 104 * 1024 if npad <= 64 else 208 * 1024
         assert p.smem_bytes == nw * 8 * 4 * 512 + nb * 4 * npad * 64 <= limit
-        assert p.grid <= (2 if npad <= 64 else 1) * 152 or p.splits == 1
+        assert p.grid <= occ * 152 or p.splits == 1
         assert p.workspace_bytes == 0  # split partials meet on chip
         return
+    assert p.cluster == 1
     assert p.block == 256
     assert p.warps_k in (1, 2, 4, 8) and p.depth >= 1
     assert 1 <= p.splits <= kb

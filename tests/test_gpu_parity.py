@@ -350,19 +350,26 @@ def test_workspace_reuse_graph_replay_and_errors(w8):
 
 
 @pytest.mark.parametrize("n,k,m", [(6144, 2048, 32), (6200, 1000, 17), (7000, 512, 64),
-                                   (28672, 512, 64), (6144, 2048, 48), (6144, 1000, 64),
-                                   (6144, 2048, 33)])
+                                   (28672, 512, 64), (6144, 8192, 48), (6144, 1000, 64),
+                                   (6144, 8192, 33), (6160, 8192, 20)])
 def test_tensor_memory_kernel_clusters_and_graph_replay(w8, n, k, m):
     """Planes of >= 48 row blocks with >= 17 tokens run the tensor-memory
     kernel; with split K its CTAs form a cluster (up to 8 splits) and add
-    their partial tiles on chip (28672 rows: no split).  Repeated calls and a
-    CUDA-graph replay give identical bits, within tolerance, and every bounded
-    wait of the kernel ended normally (device status 0)."""
+    their partial tiles on chip (28672 rows: no split), or, on planes of few
+    row blocks and long K (48-49 row blocks x 8192: 6 splits), add them
+    through the workspace (a ragged last row block included).  Repeated calls and a CUDA-graph replay give identical bits,
+    within tolerance, and every bounded wait of the kernel ended normally
+    (device status 0)."""
     plane, x_all = _case(45, n, k, m)
     x = np.ascontiguousarray(x_all[:m])
     b, _src = bind_plane(w8, plane)
     p = b.plan(0, m)
-    assert p.kernel == 1 and p.workspace_bytes == 0
+    assert p.kernel == 1
+    if k == 8192:
+        assert p.cluster == 1 and p.splits == 6 and p.workspace_bytes > 0
+    else:
+        assert p.cluster == p.splits and p.workspace_bytes == 0
+    ws = b.new_workspace()
     w8.device_status(reset=True)
     y1 = run_gemv(w8, b, 0, x, n)
     y2 = run_gemv(w8, b, 0, x, n)
@@ -372,11 +379,11 @@ def test_tensor_memory_kernel_clusters_and_graph_replay(w8, n, k, m):
     yd = torch.zeros((m, n), dtype=torch.int16, device=dev())
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
-        w8.w8_gemv(b, 0, xd, yd, None, stream=s)
+        w8.w8_gemv(b, 0, xd, yd, ws, stream=s)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        w8.w8_gemv(b, 0, xd, yd, None)
+        w8.w8_gemv(b, 0, xd, yd, ws)
     yd.zero_()
     for _ in range(3):
         g.replay()
@@ -490,7 +497,7 @@ def test_lm_head_full_size_sampled(w8):
 # ---------------------------------------------------------------------------
 
 LARGE_M = [(300, 700, 100), (100, 64, 200), (256, 512, 65), (6144, 2048, 128),
-           (6144, 1000, 192), (2624, 6144, 256), (28672, 512, 256)]
+           (6144, 1000, 192), (2624, 6144, 256), (28672, 512, 256), (6144, 4096, 96)]
 
 
 @pytest.mark.parametrize("dtype", ["e4m3fn", "bf16"])
@@ -498,12 +505,12 @@ LARGE_M = [(300, 700, 100), (100, 64, 200), (256, 512, 65), (6144, 2048, 128),
 def test_large_token_counts_within_tolerance(w8, dtype, n, k, m):
     """Above 64 tokens every call runs the tensor-memory kernel with the
     tokens padded to 96, 128, 192 or 256 (one CTA per SM, 512 TMEM columns),
-    split K in clusters and shared activation tiles where the plan has them;
+    split K in clusters (the workspace splits serve 17..64 tokens only);
     ragged N, K and token counts; sampled rows on the large planes."""
     plane, x = _case(n + k + m, n, k, m, dtype)
     b, _src = bind_plane(w8, plane)
     p = b.plan(0, m)
-    assert p.kernel == 1 and p.workspace_bytes == 0
+    assert p.kernel == 1 and p.workspace_bytes == 0 and p.cluster == p.splits
     w8.device_status(reset=True)
     y = run_gemv(w8, b, 0, x, n, fp8=(dtype == "e4m3fn"))
     rows = None
@@ -541,17 +548,18 @@ def test_large_token_counts_graph_replay(w8):
     n, k, m = 6144, 1024, 256
     plane, x = _case(91, n, k, m)
     b, _src = bind_plane(w8, plane)
+    ws = b.new_workspace()
     w8.device_status(reset=True)
     y1 = run_gemv(w8, b, 0, x, n)
     xd = to_dev(x)
     yd = torch.zeros((m, n), dtype=torch.int16, device=dev())
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
-        w8.w8_gemv(b, 0, xd, yd, None, stream=s)
+        w8.w8_gemv(b, 0, xd, yd, ws, stream=s)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        w8.w8_gemv(b, 0, xd, yd, None)
+        w8.w8_gemv(b, 0, xd, yd, ws)
     yd.zero_()
     for _ in range(3):
         g.replay()
