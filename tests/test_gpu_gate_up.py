@@ -83,10 +83,11 @@ def _case(seed, n, k, m, dtype="e4m3fn"):
 
 
 # (2I, K, m): register-ring plans with and without split K, tensor-memory
-# plans (m >= 17 on >= 48 blocks of 128 rows) with and without a cluster
+# plans (m >= 17 on >= 48 blocks of 128 rows) with and without a cluster, and
+# one whose K splits meet in the workspace (6144 x 8192 at 24 tokens)
 GATED_SHAPES = [(16, 32, 1), (64, 96, 3), (160, 1000, 8), (32, 6144, 5), (4096, 6144, 8),
                 (512, 3000, 16), (6144, 1024, 32), (6144, 2048, 20), (7168, 512, 64),
-                (512, 700, 100), (7168, 512, 256)]
+                (512, 700, 100), (7168, 512, 256), (6144, 8192, 24)]
 
 
 @pytest.mark.parametrize("dtype", ["e4m3fn", "bf16"])
