@@ -417,6 +417,7 @@ static void fill_plan(const w8::Plan &pl, w8_plan *out)
     out->k_blocks_per_warp_max = pl.kbs_max;
     out->workspace_bytes = pl.ws_bytes;
     out->cluster = pl.tc ? pl.cluster : 1;
+    out->ctas_per_sm = pl.occ;
 }
 
 w8_status w8_plan_shape(int64_t n, int64_t k, int m, int sm_count, w8_plan *out)
@@ -436,7 +437,7 @@ static void fill_plan_dt(int32_t dtype, int64_t n, int64_t k, int m, int sms, w8
     const w8::Plan pl = plan_for(dtype, n, k, m, sms);
     fill_plan(pl, out);
     if (dtype == W8_DT_BF16)
-        out->depth = pl.tc ? w8::tc_stages(false, pl.npad).nw * w8::kTcStageBlocks
+        out->depth = pl.tc ? w8::tc_stages(false, pl.npad, pl.occ).nw * w8::kTcStageBlocks
                            : w8::depth_w(pl.nt, pl.r, false, pl.occ);
     if (dtype == W8_DT_MXFP4)
         out->depth = w8::depth_w_dt(pl.nt, pl.r, w8::kDtFp4, pl.occ);

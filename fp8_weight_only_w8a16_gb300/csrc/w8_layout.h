@@ -239,11 +239,14 @@ inline int64_t plan_ctas(int64_t rt, int r, int wk, int splits)
 // row tiles leave most SMs idle.
 // The tensor-memory kernel (w8_tc.cu): CTAs of 128 rows x a K range, eleven
 // warps.  Up to 64 tokens: 2 CTAs per SM (256 tensor-memory columns and about
-// 100 KB of shared memory each); from 65 to 256 tokens (padded to 96, 128,
-// 192 or 256): 1 CTA per SM (512 columns: the accumulator, then A stages;
-// about 200 KB).  K is split across the CTAs of a cluster (up to 8) until
-// about the resident CTAs are busy, keeping at least one stage of K blocks
-// per split; the partial sums meet in distributed shared memory, so no
+// 100 KB of shared memory each), or at 49..64 tokens 1 CTA per SM with deeper
+// rings where one wave of such CTAs fills the SMs; from 65 to 256 tokens
+// (padded to 96, 128, 192 or 256): 1 CTA per SM (512 columns: the
+// accumulator, then A stages; about 200 KB).  K is split across the CTAs of
+// a cluster (up to 8) until about the resident CTAs are busy, keeping at
+// least one stage of K blocks per split; the partial sums meet in
+// distributed shared memory -- or, on planes of few row blocks up to 64
+// tokens, K is split into more ranges whose partial sums meet in the
 // workspace.
 constexpr int kTcMinM = 17;       // decode tokens from which the tc kernel may run
 constexpr int kTcMinRowBlocks = 48; // ... on planes of at least this many 128-row blocks
@@ -262,13 +265,18 @@ W8_HD constexpr int tc_occ(int npad) { return npad <= 64 ? kTcCtasPerSm : 1; }
 // Stage slots of the tensor-memory kernel in shared memory: nw weight stages
 // (8 row tiles x 4 K blocks of packed runs, filled by bulk copies) and nb
 // activation stages (4 K blocks x npad tokens): about 100 KB per CTA up to 64
-// tokens (two CTAs share an SM), about 200 KB above.
+// tokens (two CTAs share an SM), about 200 KB above.  At 64 tokens a second
+// instance runs one CTA per SM (occ 1) with deeper rings, 192 KB: 8 FP8 or 4
+// bf16 weight stages of 4 K blocks, and 4 activation stages (measured on
+// o_proj bf16 at 64 tokens: 56.1 us with 2 + 2 bf16 stages, 52.6 with 4 + 4,
+// 51.6 with 3 + 4; q_b 20.2, 19.6, 19.9).
 struct TcStages {
     int nw, nb;
 };
-W8_HD constexpr TcStages tc_stages(bool fp8, int npad)
+W8_HD constexpr TcStages tc_stages(bool fp8, int npad, int occ)
 {
-    return fp8 ? (npad <= 16 ? TcStages{5, 6} : npad <= 32 ? TcStages{4, 5}
+    return (occ == 1 && npad == 64) ? (fp8 ? TcStages{8, 4} : TcStages{4, 4})
+         : fp8 ? (npad <= 16 ? TcStages{5, 6} : npad <= 32 ? TcStages{4, 5}
                   : npad <= 48 ? TcStages{4, 3} : npad <= 64 ? TcStages{3, 3}
                   : npad <= 96 ? TcStages{5, 5} : npad <= 128 ? TcStages{5, 4}
                   : npad <= 192 ? TcStages{4, 3} : TcStages{4, 2})
@@ -277,25 +285,26 @@ W8_HD constexpr TcStages tc_stages(bool fp8, int npad)
                   : npad <= 96 ? TcStages{3, 4} : npad <= 128 ? TcStages{3, 3}
                   : npad <= 192 ? TcStages{2, 3} : TcStages{2, 2});
 }
-W8_HD constexpr int tc_smem_bytes(bool fp8, int npad)
+W8_HD constexpr int tc_smem_bytes(bool fp8, int npad, int occ)
 {
-    return tc_stages(fp8, npad).nw * 8 * 4 * (fp8 ? kRunFp8 : kRunBf16) +
-           tc_stages(fp8, npad).nb * 4 * npad * 64;
+    return tc_stages(fp8, npad, occ).nw * 8 * 4 * (fp8 ? kRunFp8 : kRunBf16) +
+           tc_stages(fp8, npad, occ).nb * 4 * npad * 64;
 }
 constexpr int kTcMaxSplits = 8;  // CTAs per cluster (the portable cluster size)
 constexpr int kTcMaxGlobalSplits = 8; // K ranges of a row block that meet in the workspace
 constexpr int kTcMinGlobalSplitBlocks = 32; // ... each at least this many K blocks (8 stages),
                                             // so that the stream outweighs the reduction
 
-inline Plan make_tc_plan(int64_t n, int64_t k, int m, int sm_count)
+// The tensor-memory plan for occ CTAs per SM.
+inline Plan make_tc_plan_occ(int64_t n, int64_t k, int m, int sm_count, int occ)
 {
     Plan p{};
     p.tc = true;
     p.npad = tc_npad(m);
     p.nt = p.npad / 8;
     p.r = 8;  // row tiles per CTA
-    p.dw = tc_stages(true, p.npad).nw * kTcStageBlocks; // weight blocks staged ahead (FP8)
-    p.occ = tc_occ(p.npad);
+    p.dw = tc_stages(true, p.npad, occ).nw * kTcStageBlocks; // weight blocks staged ahead (FP8)
+    p.occ = occ;
     p.wk = 1;
     p.rt = ceil_div(n, kTileN);
     p.kb = ceil_div(k, kTileK);
@@ -341,8 +350,26 @@ inline Plan make_tc_plan(int64_t n, int64_t k, int m, int sm_count)
     p.row_groups = int(rbs);
     p.grid = int(rbs * splits);
     p.kbs_max = int(ceil_div(p.kb, splits));
-    p.smem = tc_smem_bytes(true, p.npad); // the FP8 instance (bf16: its own table)
+    p.smem = tc_smem_bytes(true, p.npad, occ); // the FP8 instance (bf16: its own table)
     return p;
+}
+
+// At 49..64 tokens, one CTA per SM with the deeper ring where one wave of
+// those CTAs, each on its own K range with no cluster, covers at least 3/4
+// of the SMs (o_proj's 48 row blocks x 3 K ranges = 144 CTAs, q_b's 128 row
+// blocks); two CTAs per SM otherwise.  Measured on 152 SMs: o_proj FP8 at 64
+// tokens 52.4 -> 46.7 us, bf16 59.5 -> 52.6, q_b 18.6 -> 17.3; the same
+// instance below 49 tokens was slower (o_proj at 32 tokens 31.9 -> 36.4), and
+// on planes of more row blocks than SMs (kv_b's 224: two waves) much slower.
+inline Plan make_tc_plan(int64_t n, int64_t k, int m, int sm_count)
+{
+    if (tc_npad(m) == 64) {
+        const Plan d = make_tc_plan_occ(n, k, m, sm_count, 1);
+        const int64_t sms = sm_count > 0 ? sm_count : 1;
+        if (d.cluster == 1 && d.grid <= sms && 4 * int64_t(d.grid) >= 3 * sms)
+            return d;
+    }
+    return make_tc_plan_occ(n, k, m, sm_count, tc_occ(tc_npad(m)));
 }
 
 // Which kernel a shape gets (measured on GB300 over the GLM-5.2 projections):

@@ -74,13 +74,13 @@ namespace {
 constexpr int kTcKs = 4;         // K blocks per stage
 // Tensor memory of one CTA: the accumulator D in columns [0, NPAD) -- 64
 // columns reserved up to 64 tokens -- then A stages of 64 columns (4 K
-// blocks x 16): 3 in 256 columns up to 64 tokens (two CTAs share an SM's 512
-// columns), up to 4 in 512 columns above.
-W8_HD constexpr int tc_tmem_cols(int npad) { return npad <= 64 ? 256 : 512; }
+// blocks x 16): 3 in 256 columns where two CTAs share an SM's 512 columns,
+// up to 4 in 512 columns where one CTA has the SM.
+W8_HD constexpr int tc_tmem_cols(int occ) { return occ == 2 ? 256 : 512; }
 W8_HD constexpr int tc_acol(int npad) { return npad <= 64 ? 64 : npad; }
-W8_HD constexpr int tc_a_stages(int npad)
+W8_HD constexpr int tc_a_stages(int npad, int occ)
 {
-    return (tc_tmem_cols(npad) - tc_acol(npad)) / 64 < 4 ? (tc_tmem_cols(npad) - tc_acol(npad)) / 64 : 4;
+    return (tc_tmem_cols(occ) - tc_acol(npad)) / 64 < 4 ? (tc_tmem_cols(occ) - tc_acol(npad)) / 64 : 4;
 }
 constexpr int kTcThreads = kTcThreadsPerCta; // 8 converters, activations, issuer, weights
 static_assert(kTcThreads == 352, "eleven warps");
@@ -296,15 +296,15 @@ __device__ __forceinline__ float4 cluster_sum4(uint32_t off, int splits)
     return v;
 }
 
-template <bool kFp8, int NPAD>
-__global__ void __launch_bounds__(kTcThreads, tc_occ(NPAD))
+template <bool kFp8, int NPAD, int OCC>
+__global__ void __launch_bounds__(kTcThreads, OCC)
     tc_gemv_kernel(const GemvArgs a, const __grid_constant__ CUtensorMap tmx)
 {
     constexpr int kRun = kFp8 ? kRunFp8 : kRunBf16;
-    constexpr int kNW = tc_stages(kFp8, NPAD).nw; // weight stages (shared memory)
-    constexpr int kNB = tc_stages(kFp8, NPAD).nb; // activation stages (shared memory)
-    constexpr int kNA = tc_a_stages(NPAD);        // A stages (tensor memory)
-    constexpr uint32_t kTmemCols = tc_tmem_cols(NPAD);
+    constexpr int kNW = tc_stages(kFp8, NPAD, OCC).nw; // weight stages (shared memory)
+    constexpr int kNB = tc_stages(kFp8, NPAD, OCC).nb; // activation stages (shared memory)
+    constexpr int kNA = tc_a_stages(NPAD, OCC);        // A stages (tensor memory)
+    constexpr uint32_t kTmemCols = tc_tmem_cols(OCC);
     constexpr int kACol = tc_acol(NPAD);
     static_assert(kNA >= 3 && kACol + kNA * 64 <= int(kTmemCols) && kACol >= NPAD, "tensor memory map");
     constexpr int kTileW = kTcKs * kRun;          // one row tile's runs of a stage
@@ -319,9 +319,10 @@ __global__ void __launch_bounds__(kTcThreads, tc_occ(NPAD))
     constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(NPAD >> 3) << 17) |
                                 (uint32_t(128 >> 4) << 24);
     static_assert(NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 256, "M = 128 needs N in 16..256, step 16");
-    static_assert(128 * kRedPitch * 4 <= tc_smem_bytes(kFp8, NPAD),
+    static_assert(OCC == tc_occ(NPAD) || (OCC == 1 && NPAD == 64), "the planner's instances");
+    static_assert(128 * kRedPitch * 4 <= tc_smem_bytes(kFp8, NPAD, OCC),
                   "the exchange tile reuses the stages' shared memory");
-    static_assert(kNW * kStageW + kNB * kStageB == tc_smem_bytes(kFp8, NPAD), "stage geometry");
+    static_assert(kNW * kStageW + kNB * kStageB == tc_smem_bytes(kFp8, NPAD, OCC), "stage geometry");
 
     extern __shared__ __align__(1024) uint8_t s_dyn[]; // kNW weight stages, then kNB B stages
     __shared__ __align__(8) uint64_t bar_full_w[kNW], bar_empty_w[kNW];
@@ -713,17 +714,19 @@ __global__ void __launch_bounds__(kTcThreads, tc_occ(NPAD))
 }
 
 template <bool kFp8>
-void *tc_instance(int npad)
+void *tc_instance(int npad, int occ)
 {
+    if (occ != tc_occ(npad))
+        return npad == 64 && occ == 1 ? reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 64, 1>) : nullptr;
     switch (npad) {
-    case 16: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 16>);
-    case 32: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 32>);
-    case 48: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 48>);
-    case 64: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 64>);
-    case 96: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 96>);
-    case 128: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 128>);
-    case 192: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 192>);
-    case 256: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 256>);
+    case 16: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 16, tc_occ(16)>);
+    case 32: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 32, tc_occ(32)>);
+    case 48: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 48, tc_occ(48)>);
+    case 64: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 64, tc_occ(64)>);
+    case 96: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 96, tc_occ(96)>);
+    case 128: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 128, tc_occ(128)>);
+    case 192: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 192, tc_occ(192)>);
+    case 256: return reinterpret_cast<void *>(&tc_gemv_kernel<kFp8, 256, tc_occ(256)>);
     default: return nullptr;
     }
 }
@@ -734,12 +737,16 @@ constexpr int kTcNpads[] = {16, 32, 48, 64, 96, 128, 192, 256};
 cudaError_t prepare_tc_kernels()
 {
     for (int npad : kTcNpads) {
-        for (int f = 0; f < 2; ++f) {
-            void *fn = f ? tc_instance<true>(npad) : tc_instance<false>(npad);
-            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 tc_smem_bytes(f == 1, npad));
-            if (e != cudaSuccess)
-                return e;
+        for (int occ = 1; occ <= 2; ++occ) {
+            for (int f = 0; f < 2; ++f) {
+                void *fn = f ? tc_instance<true>(npad, occ) : tc_instance<false>(npad, occ);
+                if (!fn)
+                    continue;
+                cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     tc_smem_bytes(f == 1, npad, occ));
+                if (e != cudaSuccess)
+                    return e;
+            }
         }
     }
     return cudaSuccess;
@@ -786,7 +793,7 @@ bool encode_x_map(CUtensorMap *map, const GemvArgs &a, int npad)
 
 cudaError_t launch_tc(bool fp8, const Plan &plan, const GemvArgs &a, cudaStream_t s)
 {
-    void *fn = fp8 ? tc_instance<true>(plan.npad) : tc_instance<false>(plan.npad);
+    void *fn = fp8 ? tc_instance<true>(plan.npad, plan.occ) : tc_instance<false>(plan.npad, plan.occ);
     if (!fn)
         return cudaErrorInvalidValue;
     alignas(64) CUtensorMap tmx;
@@ -798,7 +805,7 @@ cudaError_t launch_tc(bool fp8, const Plan &plan, const GemvArgs &a, cudaStream_
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(unsigned(plan.grid));
     cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = size_t(tc_smem_bytes(fp8, plan.npad));
+    cfg.dynamicSmemBytes = size_t(tc_smem_bytes(fp8, plan.npad, plan.occ));
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -26,7 +26,7 @@ DT_E4M3FN_B128 = 7  # FP8 codes with one fp32 factor per 128 x 128 block
 SRC_ROW_MAJOR, SRC_GATE_UP = 0, 1
 LAYOUT_MMA_16x32, LAYOUT_MMA_16x32_GATE_UP = 1, 2
 MAX_M = 256
-ABI_VERSION = 7  # W8_ABI_VERSION of include/w8.h (the structs below follow it)
+ABI_VERSION = 8  # W8_ABI_VERSION of include/w8.h (the structs below follow it)
 
 STATUS = {
     0: "W8_OK", 1: "W8_ERR_NULL", 2: "W8_ERR_DTYPE", 3: "W8_ERR_UNPADDED", 4: "W8_ERR_BIAS",
@@ -64,7 +64,8 @@ class PlanInfo(ctypes.Structure):
                 ("row_tiles_per_warp", ctypes.c_int32), ("warps_k", ctypes.c_int32),
                 ("depth", ctypes.c_int32), ("row_groups", ctypes.c_int32),
                 ("splits", ctypes.c_int32), ("k_blocks_per_warp_max", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_size_t), ("cluster", ctypes.c_int32)]
+                ("workspace_bytes", ctypes.c_size_t), ("cluster", ctypes.c_int32),
+                ("ctas_per_sm", ctypes.c_int32)]
 
 
 def _load():

@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define W8_ABI_VERSION 7
+#define W8_ABI_VERSION 8
 
 /* A cudaStream_t: the runtime's stream type is this same pointer type. */
 typedef struct CUstream_st *w8_stream;
@@ -213,6 +213,11 @@ typedef struct {
                                 into more ranges than a power of two that fill the SMs
                                 evenly (up to 8) and the last CTA of a row block adds
                                 them from the workspace; kernel 0: 1 */
+    int32_t ctas_per_sm;     /* CTAs one SM holds at once (the occupancy the launch is
+                                built for): kernel 1 two up to 64 tokens, except one
+                                (with a deeper weight ring) at 49..64 tokens where one
+                                wave of unclustered CTAs covers at least 3/4 of the SMs;
+                                one above 64 tokens */
 } w8_plan;
 
 typedef struct w8_build w8_build; /* opaque, host-side, library-owned */

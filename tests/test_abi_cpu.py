@@ -43,7 +43,7 @@ def test_every_declared_function_is_exported():
 
 
 def test_abi_version_and_status_strings():
-    assert w8.lib.w8_abi_version() == 7
+    assert w8.lib.w8_abi_version() == 8
     for code in range(15):
         assert w8.status_str(code)
     assert w8.status_str(99) == "unknown status"
@@ -231,7 +231,7 @@ def test_packed_offset_rejects_bad_arguments():
 
 SHAPES = [(256, 512), (2624, 6144), (6144, 16384), (4096, 6144), (6144, 2048),
           (16384, 2048), (28672, 512), (4096, 2048), (128, 6144), (32, 6144),
-          (154880, 6144), (1, 1), (37, 77), (100, 4096)]
+          (154880, 6144), (1, 1), (37, 77), (100, 4096), (8192, 4096), (6144, 8192)]
 
 
 @pytest.mark.parametrize("n,k", SHAPES)
@@ -248,6 +248,22 @@ def test_plan_invariants(n, k, m):
         assert p.kernel == 1 and p.block == 352
         npad = -(-m // 16) * 16 if m <= 64 else min(x for x in (96, 128, 192, 256) if x >= m)
         occ = 2 if npad <= 64 else 1
+        deep = npad == 64 and p.ctas_per_sm == 1
+        if npad == 64:
+            # one CTA per SM (a deeper ring) exactly where one wave of
+            # unclustered CTAs covers 3/4 of the SMs or more
+            rg = -(-n // 128)
+            sg = min(8, 152 // rg)
+            while sg > 1 and kb // sg < 32:
+                sg -= 1
+            cl = 1
+            while cl < 8 and rg * cl * 2 <= 152 and kb // (cl * 2) >= 4:
+                cl *= 2
+            one_wave = rg * (sg if sg > cl else cl)
+            assert deep == ((sg > cl or cl == 1) and 114 <= one_wave <= 152)
+            if deep:
+                occ = 1
+        assert p.ctas_per_sm == occ
         assert p.row_groups == -(-n // 128) and p.n_tiles * 8 == npad
         assert p.splits == 1 or kb // p.splits >= 4
         assert p.grid <= 2 * 152 or p.splits == 1
@@ -256,7 +272,7 @@ def test_plan_invariants(n, k, m):
             # K ranges that meet in the workspace: as many as fill the
             # resident slots (at most 8), more than the power-of-two
             # cluster plan would take
-            assert npad <= 64 and (2 < p.splits <= 8 or p.row_groups * 2 <= occ * 152)
+            assert npad <= 64 and (2 < p.splits <= 8 or p.row_groups * 2 <= occ * 152 or deep)
             assert p.splits == min(8, occ * 152 // p.row_groups, kb // 32)
             assert p.grid <= occ * 152
             assert p.workspace_bytes >= p.splits * rt * 16 * m * 4
@@ -264,8 +280,10 @@ def test_plan_invariants(n, k, m):
         assert p.cluster == p.splits and p.splits in (1, 2, 4, 8)
         nw, nb = {16: (5, 6), 32: (4, 5), 48: (4, 3), 64: (3, 3), 96: (5, 5), 128: (5, 4),
                   192: (4, 3), 256: (4, 2)}[npad]  # FP8 stage slots
-        # about 100 KB (two CTAs per SM) up to 64 tokens, about 200 KB (one) above
-        limit = 104 * 1024 if npad <= 64 else 208 * 1024
+        if deep:
+            nw, nb = 8, 4
+        # about 100 KB (two CTAs per SM), about 200 KB (one)
+        limit = 104 * 1024 if occ == 2 else 208 * 1024
         assert p.smem_bytes == nw * 8 * 4 * 512 + nb * 4 * npad * 64 <= limit
         assert p.grid <= occ * 152 or p.splits == 1
         assert p.workspace_bytes == 0  # split partials meet on chip
@@ -297,7 +315,7 @@ def test_plan_invariants(n, k, m):
 
 
 PLAN_FIELDS = ("kernel", "grid", "block", "smem_bytes", "n_tiles", "row_tiles_per_warp",
-               "warps_k", "row_groups", "splits", "workspace_bytes")
+               "warps_k", "row_groups", "splits", "workspace_bytes", "cluster", "ctas_per_sm")
 
 
 @pytest.mark.parametrize("n,k", SHAPES)
@@ -311,6 +329,11 @@ def test_plan_shape_dtype_row_and_bf16_planes_match_the_shape_plan(n, k, m):
         assert all(getattr(p, f) == getattr(base, f) for f in PLAN_FIELDS), dt
         assert p.k_blocks_per_warp_max == base.k_blocks_per_warp_max
     assert w8.plan_shape_dtype(n, k, m, 152, w8.DT_E4M3FN).depth == base.depth
+    if base.kernel == 1 and base.ctas_per_sm == 1 and m <= 64:
+        # the one-CTA-per-SM instance at 49..64 tokens: 8 FP8 or 4 bf16
+        # weight stages of 4 K blocks
+        assert base.depth == 32
+        assert w8.plan_shape_dtype(n, k, m, 152, w8.DT_BF16).depth == 16
 
 
 @pytest.mark.parametrize("n,k", SHAPES)

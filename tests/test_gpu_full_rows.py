@@ -10,8 +10,10 @@ bench uses (the plan of this GPU's SM count):
 * o_proj E4M3 [6144, 16384] at 8 tokens: the register ring, 3 CTAs per SM;
 * fused_qkv_a_proj E4M3 [2624, 6144] at 16 tokens: the register ring with
   two token groups;
-* q_b_proj E4M3 [16384, 2048] at 64 tokens: the tensor-memory kernel with
+* q_b_proj E4M3 [16384, 2048] at 48 tokens: the tensor-memory kernel with
   split-K clusters;
+* o_proj E4M3 [6144, 16384] at 64 tokens: the tensor-memory kernel with one
+  CTA per SM and the deeper ring, 3 K ranges meeting in the workspace;
 * kv_b_proj E4M3 [28672, 512] at 256 tokens: the tensor-memory kernel, one
   CTA per SM over two waves;
 * o_proj MXFP4 [6144, 16384] at 8 tokens and fused_qkv_a_proj block-scaled
@@ -55,16 +57,21 @@ def _assert_within(y, y64, mag):
 
 
 @pytest.mark.parametrize("n,k,m,kernel", [(6144, 16384, 8, 0), (2624, 6144, 16, 0),
-                                          (16384, 2048, 64, 1), (28672, 512, 256, 1)],
-                         ids=["o_proj_m8", "fused_qkv_a_m16", "q_b_m64", "kv_b_m256"])
+                                          (16384, 2048, 48, 1), (6144, 16384, 64, 1),
+                                          (28672, 512, 256, 1)],
+                         ids=["o_proj_m8", "fused_qkv_a_m16", "q_b_m48", "o_proj_m64",
+                              "kv_b_m256"])
 def test_every_row_e4m3(w8, n, k, m, kernel):
     plane, x_all = synth.workload(n, k, "e4m3fn", seed=11)
     x = np.ascontiguousarray(x_all[:m])
     b = w8.bind([w8.Plane.from_tensor(to_dev(plane.w), to_dev(plane.scale))])
     p = b.plan(0, m)
     assert p.kernel == kernel
-    if kernel == 1 and m == 64:
-        assert p.splits > 1  # a cluster adds its split partial tiles
+    sms = torch.cuda.get_device_properties(dev()).multi_processor_count
+    if kernel == 1 and m == 48:
+        assert p.splits > 1 and p.cluster == p.splits  # a cluster adds its split partial tiles
+    if kernel == 1 and m == 64 and sms == 152:
+        assert p.ctas_per_sm == 1 and p.splits == 3 and p.cluster == 1
     if kernel == 1 and m == 256:
         assert p.grid > torch.cuda.get_device_properties(dev()).multi_processor_count
     w8.device_status(reset=True)

@@ -199,6 +199,27 @@ def test_unit_scale_fp8_equals_bf16_path(w8, n, k, m):
     assert np.array_equal(y8, y16)
 
 
+@pytest.mark.parametrize("n,k,m", [(6144, 8192, 64), (16384, 512, 50)])
+def test_unit_scale_fp8_equals_bf16_path_one_cta_per_sm(w8, n, k, m):
+    """The one-CTA-per-SM tensor-memory instance (49..64 tokens) of both
+    weight formats: an FP8 plane with unit scales gives the bits of the bf16
+    plane of its decoded values, and the bf16 path is within tolerance."""
+    plane, x_all = _case(n + k + m, n, k, m)
+    plane.scale = np.ones(n, np.float32)
+    x = np.ascontiguousarray(x_all[:m])
+    b8, _s8 = bind_plane(w8, plane)
+    wide = _widened_bf16_plane(plane)
+    b16, _s16 = bind_plane(w8, wide)
+    if torch.cuda.get_device_properties(dev()).multi_processor_count == 152:
+        assert b8.plan(0, m).ctas_per_sm == 1 and b16.plan(0, m).ctas_per_sm == 1
+    w8.device_status(reset=True)
+    y8 = run_gemv(w8, b8, 0, x, n, fp8=True)
+    y16 = run_gemv(w8, b16, 0, x, n, fp8=False)
+    assert np.array_equal(y8, y16)
+    _check_tol(wide, x, y16)
+    assert w8.device_status() == 0
+
+
 @pytest.mark.parametrize("j", [-4, 5])
 @pytest.mark.parametrize("n,k,m", [(300, 3000, 8), (6144, 1000, 40)])
 def test_power_of_two_scale_commutes(w8, j, n, k, m):
@@ -349,26 +370,39 @@ def test_workspace_reuse_graph_replay_and_errors(w8):
     assert torch.all(yd2 == 0)  # no refused call wrote anything
 
 
-@pytest.mark.parametrize("n,k,m", [(6144, 2048, 32), (6200, 1000, 17), (7000, 512, 64),
-                                   (28672, 512, 64), (6144, 8192, 48), (6144, 1000, 64),
-                                   (6144, 8192, 33), (6160, 8192, 20)])
-def test_tensor_memory_kernel_clusters_and_graph_replay(w8, n, k, m):
+@pytest.mark.parametrize("n,k,m,kind", [(6144, 2048, 32, "cluster"), (6200, 1000, 17, "cluster"),
+                                        (7000, 512, 64, "cluster"), (28672, 512, 64, "cluster"),
+                                        (6144, 1000, 64, "cluster"),
+                                        (6144, 8192, 48, "ws"), (6144, 8192, 33, "ws"),
+                                        (6160, 8192, 20, "ws"),
+                                        (6144, 8192, 64, "deep_ws"), (6160, 8192, 57, "deep_ws"),
+                                        (16384, 512, 50, "deep")])
+def test_tensor_memory_kernel_clusters_and_graph_replay(w8, n, k, m, kind):
     """Planes of >= 48 row blocks with >= 17 tokens run the tensor-memory
     kernel; with split K its CTAs form a cluster (up to 8 splits) and add
     their partial tiles on chip (28672 rows: no split), or, on planes of few
     row blocks and long K (48-49 row blocks x 8192: 6 splits), add them
-    through the workspace (a ragged last row block included).  Repeated calls and a CUDA-graph replay give identical bits,
-    within tolerance, and every bounded wait of the kernel ended normally
-    (device status 0)."""
+    through the workspace (a ragged last row block included).  At 49..64
+    tokens, where one wave of unclustered CTAs covers 3/4 of the SMs, the
+    instance with one CTA per SM and the deeper ring runs (48-49 row blocks
+    x 3 K ranges through the workspace; 128 row blocks with no split).
+    Repeated calls and a CUDA-graph replay give identical bits, within
+    tolerance, and every bounded wait of the kernel ended normally (device
+    status 0)."""
     plane, x_all = _case(45, n, k, m)
     x = np.ascontiguousarray(x_all[:m])
     b, _src = bind_plane(w8, plane)
     p = b.plan(0, m)
     assert p.kernel == 1
-    if k == 8192:
+    sms = torch.cuda.get_device_properties(dev()).multi_processor_count
+    if kind == "ws":
         assert p.cluster == 1 and p.splits == 6 and p.workspace_bytes > 0
-    else:
-        assert p.cluster == p.splits and p.workspace_bytes == 0
+    elif kind == "cluster":
+        assert p.cluster == p.splits and p.workspace_bytes == 0 and p.ctas_per_sm == 2
+    elif sms == 152:  # the deep instance: its choice depends on the SM count
+        assert p.ctas_per_sm == 1 and p.cluster == 1 and p.smem_bytes > 150 * 1024
+        assert p.splits == (3 if kind == "deep_ws" else 1)
+        assert (p.workspace_bytes > 0) == (kind == "deep_ws")
     ws = b.new_workspace()
     w8.device_status(reset=True)
     y1 = run_gemv(w8, b, 0, x, n)
