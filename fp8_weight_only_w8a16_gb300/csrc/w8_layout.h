@@ -285,10 +285,13 @@ W8_HD constexpr TcStages tc_stages(bool fp8, int npad, int occ)
                   : npad <= 96 ? TcStages{3, 4} : npad <= 128 ? TcStages{3, 3}
                   : npad <= 192 ? TcStages{2, 3} : TcStages{2, 2});
 }
+// Dynamic shared memory of a CTA: the stages, plus room to start them on a
+// 1024-byte boundary (the activation stages' swizzle atoms).
+constexpr int kTcSmemAlign = 1024;
 W8_HD constexpr int tc_smem_bytes(bool fp8, int npad, int occ)
 {
     return tc_stages(fp8, npad, occ).nw * 8 * 4 * (fp8 ? kRunFp8 : kRunBf16) +
-           tc_stages(fp8, npad, occ).nb * 4 * npad * 64;
+           tc_stages(fp8, npad, occ).nb * 4 * npad * 64 + kTcSmemAlign;
 }
 constexpr int kTcMaxSplits = 8;  // CTAs per cluster (the portable cluster size)
 constexpr int kTcMaxGlobalSplits = 8; // K ranges of a row block that meet in the workspace

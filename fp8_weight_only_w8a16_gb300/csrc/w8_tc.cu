@@ -21,11 +21,11 @@
 //     tcgen05.st (TMEM lanes 32 (w % 4) + 16 (w / 4) .., the lane quarter warp
 //     w may reach), in natural K order (below);
 //   warp 8 (activations): after the dependency wait, one thread copies the
-//     activation tiles with tensor-map bulk copies (TMA): one 8-column x
-//     tokens box per K group, landing as the 8-row x 16-byte core matrices
-//     of the tensor cores' K-major layout; columns past K arrive as zeros,
-//     rows past the tokens are not copied (their accumulator columns are
-//     never stored);
+//     activation tiles with tensor-map bulk copies (TMA): one 64-column x
+//     tokens box per half stage, each token's 128 bytes a row of the
+//     tensor cores' 128-byte-swizzled K-major layout (8-row x 128-byte
+//     atoms); columns past K arrive as zeros, rows past the tokens are not
+//     copied (their accumulator columns are never stored);
 //   warp 9 (issuer): one thread issues the tensor-core steps
 //     D[128 x NPAD] += A[128 x 16] (TMEM) * B[16 x NPAD] (shared memory) and
 //     commits them to the stages' "empty" barriers.
@@ -153,12 +153,16 @@ __device__ __forceinline__ void tm_wait_ld()
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor, K-major, no swizzle: 8-row x 16-byte core
-// matrices; lbo = byte stride between core matrices along K, sbo = along N.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte
+// swizzle layout: rows of 128 bytes (64 bf16 along K) in atoms of 8 rows
+// (1024 bytes, 1024-byte aligned), sbo = the byte stride between atoms along
+// N; the leading-byte offset is unused in this layout (field 1).  A step of
+// 16 columns starts 32 bytes further into the row; the swizzle is applied to
+// the absolute address, as the tensor-map copy that wrote the rows did.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t sbo)
 {
-    return uint64_t((addr >> 4) & 0x3FFFu) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
-           (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46);
+    return uint64_t((addr >> 4) & 0x3FFFu) | (uint64_t(1) << 16) | (uint64_t((sbo >> 4) & 0x3FFFu) << 32) |
+           (uint64_t(1) << 46) | (uint64_t(2) << 61);
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]: bf16 inputs, fp32 accumulate, M = 128.
@@ -183,12 +187,23 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
 }
+// An L2 policy that marks the lines it fetches first to leave: the weights
+// stream through once, and the activations and partial sums they would
+// otherwise push out of L2 are read again (measured: 2-4 % on FP8 planes at
+// 17-64 tokens, 8 % on bf16 o_proj at 32 tokens).
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
 // Bulk asynchronous copy global -> shared (16-byte aligned, a multiple of 16
-// bytes) whose completion counts `bytes` on the barrier's transaction count.
+// bytes) whose completion counts `bytes` on the barrier's transaction count;
+// its lines leave L2 first.
 __device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar)
 {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy_evict_first())
                  : "memory");
 }
 // 16 bytes of fp32 through L2 only (partial sums other CTAs wrote).
@@ -309,11 +324,10 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
     static_assert(kNA >= 3 && kACol + kNA * 64 <= int(kTmemCols) && kACol >= NPAD, "tensor memory map");
     constexpr int kTileW = kTcKs * kRun;          // one row tile's runs of a stage
     constexpr int kStageW = 8 * kTileW;
-    constexpr int kBlockB = NPAD * 64;            // activation bytes of one K block
-    constexpr int kStepB = NPAD * 32;             // ... of one 16-column step
-    constexpr int kStageB = kTcKs * kBlockB;
-    constexpr uint32_t kLbo = NPAD * 16;          // core matrices along K
-    constexpr uint32_t kSbo = 128;                // core matrices along the tokens
+    constexpr int kHalfB = NPAD * 128;            // activation bytes of 64 columns (2 K blocks)
+    constexpr int kStageB = 2 * kHalfB;           // ... of a stage (4 K blocks)
+    static_assert(kTcKs * kTileK == 128 && kHalfB % 1024 == 0 && kStageW % 1024 == 0,
+                  "swizzle atoms stay 1024-byte aligned");
     constexpr int kRedPitch = NPAD + 4;           // floats per row of the split-K exchange tile
     // instruction descriptor: D f32, A and B bf16, both K-major, N = NPAD, M = 128
     constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(NPAD >> 3) << 17) |
@@ -322,9 +336,10 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
     static_assert(OCC == tc_occ(NPAD) || (OCC == 1 && NPAD == 64), "the planner's instances");
     static_assert(128 * kRedPitch * 4 <= tc_smem_bytes(kFp8, NPAD, OCC),
                   "the exchange tile reuses the stages' shared memory");
-    static_assert(kNW * kStageW + kNB * kStageB == tc_smem_bytes(kFp8, NPAD, OCC), "stage geometry");
+    static_assert(kNW * kStageW + kNB * kStageB + kTcSmemAlign == tc_smem_bytes(kFp8, NPAD, OCC),
+                  "stage geometry");
 
-    extern __shared__ __align__(1024) uint8_t s_dyn[]; // kNW weight stages, then kNB B stages
+    extern __shared__ __align__(16) uint8_t s_dyn[]; // kNW weight stages, then kNB B stages
     __shared__ __align__(8) uint64_t bar_full_w[kNW], bar_empty_w[kNW];
     __shared__ __align__(8) uint64_t bar_full_a[kNA], bar_empty_a[kNA];
     __shared__ __align__(8) uint64_t bar_full_b[kNB], bar_empty_b[kNB];
@@ -341,8 +356,11 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
     const int nst = (cnb + kTcKs - 1) / kTcKs;          // stages
     const int row0 = rb * 128;
     const int tile0 = rb * 8;
-    uint8_t *const s_w = s_dyn;
-    uint8_t *const s_b = s_dyn + kNW * kStageW;
+    // the stages start at the first 1024-byte boundary of the dynamic shared
+    // memory (the swizzle atoms of the activation stages need it; the launch
+    // adds kTcSmemAlign bytes for the shift)
+    uint8_t *const s_w = s_dyn + ((1024u - (smem_u32(s_dyn) & 1023u)) & 1023u);
+    uint8_t *const s_b = s_w + kNW * kStageW;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kNW; ++s) {
@@ -440,10 +458,12 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
             atomicOr(&g_tc_status, 1);
     } else if (warp == kWarpAct) {
         // ---- activations: x -> B tiles in shared memory (tensor-map copies) -----
-        // Lane 4j + k copies K group k of block j of the stage (16 copies in
-        // parallel), each an 8-column x min(m, NPAD)-row box (rows past m
-        // keep whatever the slot held: they meet only the accumulator columns
-        // of tokens >= m, which are never stored).
+        // Lane h < 2 copies columns 64h..64h+63 of the stage (K blocks 2h,
+        // 2h+1) as one 64-column x min(m, NPAD)-row box into its half of the
+        // slot (rows past m keep whatever the slot held: they meet only the
+        // accumulator columns of tokens >= m, which are never stored); a
+        // last stage of one or three blocks copies a whole half, whose
+        // columns past the CTA's range no step reads.
         pdl_wait(); // x may be the previous kernel's output
         bool ok = true;
         for (int st = 0; st < nst && ok; ++st) {
@@ -453,13 +473,13 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
             if (!ok)
                 break;
             const int nb = cnb - st * kTcKs < kTcKs ? cnb - st * kTcKs : kTcKs;
+            const int nh = (nb + 1) >> 1; // 64-column halves to copy
             if (lane == 0)
-                mbar_expect_tx(&bar_full_b[s], uint32_t(nb * 4 * 16 * (a.m < NPAD ? a.m : NPAD)));
+                mbar_expect_tx(&bar_full_b[s], uint32_t(nh * 128 * (a.m < NPAD ? a.m : NPAD)));
             __syncwarp();
-            const int j = lane >> 2, kg = lane & 3;
-            if (j < nb) {
-                const uint32_t dst = smem_u32(s_b + s * kStageB + j * kBlockB + kg * NPAD * 16);
-                const int c0 = (cb0 + st * kTcKs + j) * kTileK + 8 * kg;
+            if (lane < nh) {
+                const uint32_t dst = smem_u32(s_b + s * kStageB + lane * kHalfB);
+                const int c0 = (cb0 + st * kTcKs) * kTileK + 64 * lane;
                 tma_load_2d(dst, &tmx, c0, 0, &bar_full_b[s]);
             }
         }
@@ -471,7 +491,7 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
         // offsets (the address field holds addr >> 4, and every shared-memory
         // address stays below 256 KB, so adding never carries out of it); a
         // full stage is issued unrolled, a partial last stage block by block.
-        const uint64_t bdesc0 = smem_desc(smem_u32(s_b), kLbo, kSbo);
+        const uint64_t bdesc0 = smem_desc_sw128(smem_u32(s_b), 1024);
         bool ok = true;
         for (int st = 0; st < nst && ok; ++st) {
             const int sa_ = st % kNA, sb = st % kNB;
@@ -489,14 +509,14 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
 #pragma unroll
                     for (int q = 0; q < 2; ++q)
                         umma_ts(tbase, at + uint32_t(j * 16 + q * 8),
-                                bd + uint64_t((j * kBlockB + q * kStepB) >> 4), kIdesc,
+                                bd + uint64_t(((j >> 1) * kHalfB + ((j & 1) * 2 + q) * 32) >> 4), kIdesc,
                                 uint32_t(st | j | q));
             } else {
                 for (int j = 0; j < nb; ++j)
 #pragma unroll
                     for (int q = 0; q < 2; ++q)
                         umma_ts(tbase, at + uint32_t(j * 16 + q * 8),
-                                bd + uint64_t((j * kBlockB + q * kStepB) >> 4), kIdesc,
+                                bd + uint64_t(((j >> 1) * kHalfB + ((j & 1) * 2 + q) * 32) >> 4), kIdesc,
                                 uint32_t(st | j | q));
             }
             umma_commit(&bar_empty_a[sa_]);
@@ -770,7 +790,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 }
 
 // The activations x [m][ldx] bf16 as a 2-D tensor (K columns, m rows) read in
-// 8-column x npad-row boxes; outside K or m the boxes are zero.
+// 64-column (128-byte) x min(m, npad)-row boxes with the 128-byte swizzle;
+// outside K the boxes are zero.
 bool encode_x_map(CUtensorMap *map, const GemvArgs &a, int npad)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
@@ -782,10 +803,10 @@ bool encode_x_map(CUtensorMap *map, const GemvArgs &a, int npad)
     // (they feed only accumulator columns that are never stored), so no copy
     // reads past the tensor's last row (measured: boxes with out-of-range
     // rows, filled by the copy engine, made 17..31 tokens slower than 32)
-    const cuuint32_t box[2] = {8, cuuint32_t(a.m < npad ? a.m : npad)};
+    const cuuint32_t box[2] = {64, cuuint32_t(a.m < npad ? a.m : npad)};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(a.x), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

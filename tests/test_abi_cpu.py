@@ -282,9 +282,10 @@ def test_plan_invariants(n, k, m):
                   192: (4, 3), 256: (4, 2)}[npad]  # FP8 stage slots
         if deep:
             nw, nb = 8, 4
-        # about 100 KB (two CTAs per SM), about 200 KB (one)
-        limit = 104 * 1024 if occ == 2 else 208 * 1024
-        assert p.smem_bytes == nw * 8 * 4 * 512 + nb * 4 * npad * 64 <= limit
+        # about 100 KB (two CTAs per SM), about 200 KB (one), plus 1 KB to
+        # start the stages on a 1024-byte boundary
+        limit = 105 * 1024 if occ == 2 else 209 * 1024
+        assert p.smem_bytes == nw * 8 * 4 * 512 + nb * 4 * npad * 64 + 1024 <= limit
         assert p.grid <= occ * 152 or p.splits == 1
         assert p.workspace_bytes == 0  # split partials meet on chip
         return
