@@ -383,6 +383,41 @@ def test_plan_shape_dtype_refusals():
     assert e.value.name == "W8_ERR_SHAPE"
 
 
+TC_SHAPES = [(256, 512), (2624, 6144), (6144, 16384), (6144, 2048), (16384, 2048), (28672, 512),
+             (4096, 2048), (160, 6144), (6144, 8192), (8192, 4096), (20480, 2048), (37, 77)]
+
+
+@pytest.mark.parametrize("sms", [1, 2, 8, 66, 132, 148, 160, 264])
+def test_tensor_memory_plans_on_other_sm_counts(sms):
+    """The tensor-memory plan's invariants hold whatever the SM count: the
+    grid tiles row blocks x K ranges, the splits meet on chip (a cluster of
+    at most 8) or in the workspace (cluster 1, workspace > 0), every K block
+    is covered, the shared memory fits the CTAs per SM the plan is built
+    for, and the one-CTA-per-SM instance at 49..64 tokens appears only where
+    one wave of unclustered CTAs covers 3/4 of the SMs or more."""
+    seen = 0
+    for n, k in TC_SHAPES:
+        kb = -(-k // 32)
+        for m in (17, 33, 49, 64, 65, 128, 256):
+            p = w8.plan_shape(n, k, m, sms)
+            if p.kernel != 1:
+                continue
+            seen += 1
+            assert p.grid == p.row_groups * p.splits and p.row_groups == -(-n // 128)
+            assert p.ctas_per_sm in (1, 2) and 1 <= p.cluster <= 8
+            assert p.cluster in (1, p.splits)
+            assert p.k_blocks_per_warp_max * p.splits >= kb
+            assert (p.workspace_bytes > 0) == (p.splits > 1 and p.cluster == 1)
+            if m <= 64 and p.ctas_per_sm == 1:
+                assert -(-m // 16) * 16 == 64 and p.cluster == 1
+                assert p.grid <= sms and 4 * p.grid >= 3 * sms
+            if m > 64:
+                assert p.ctas_per_sm == 1 and p.workspace_bytes == 0
+            # two CTAs of 352 threads share an SM's 228 KB, one may take 227 KB
+            assert p.smem_bytes <= (113 if p.ctas_per_sm == 2 else 227) * 1024
+    assert seen > 0
+
+
 def test_plan_does_not_depend_on_anything_but_shape():
     a = w8.plan_shape(2624, 6144, 4, 152)
     b = w8.plan_shape(2624, 6144, 4, 152)
